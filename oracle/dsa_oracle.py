@@ -1,0 +1,391 @@
+"""Plain float64 CPU oracle of the DSA decode path.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; never by the product path.  It shares
+no code with the CUDA library.
+
+What it computes, and where the pages define it:
+
+* ``indexer_logits`` -- the lightning-indexer score
+  I[t, s] = sum_j w[t, j] * ReLU(q^I[t, j] . k^I[s])  over 64 FP8 heads of
+  128 dims ("MTP and sparse attention: NSA and DSA", section "Sparse
+  attention: NSA and DSA").  The FP8 values are dequantised with their
+  per-token fp32 scales (the same page: "the indexer key (FP8 + scale)").
+* ``visible_lengths`` -- with n_q query tokens per request over S cached
+  tokens, query i sees S - (n_q - 1 - i) tokens ("[SGLang] NSA (Narrow Sparse
+  Attention)", section "init_forward_metadata": seqlens_expanded, worked
+  example 3 queries over 10 tokens -> 8, 9, 10).
+* ``topk`` -- per query token, the k = 2048 highest-scoring visible tokens
+  ("Sparse attention: NSA and DSA"; "Multi-layer Indexer" abstract).  Ties go
+  to the lower token index; the result is a set, returned sorted.
+* ``sparse_mla`` -- absorbed-form MLA attention over only the selected latent
+  rows: K is the 576-dim latent row, V its first 512 dims ("[SGLang] NSA",
+  section "forward_decode": q_nope 512 + q_rope 64, kv_cache_dim =
+  kv_lora_rank + qk_rope_head_dim).
+* ``sparse_mla_split`` / ``merge`` -- the selected tokens cut into blocks; per
+  block an online softmax giving Mid_O and Mid_O_LogExpSum; then a cross-block
+  online-softmax merge ("Deepseek Details", section "DSA", stages 2 and 3).
+* ``decode_bytes`` / ``decode_flops`` -- the per-layer cost model printed in
+  "Sparse attention: NSA and DSA" (its code cell and output table).
+
+Pinned by ``tests/test_oracle_pins.py``: every function above is checked
+against something other than itself (the pages' printed numbers and worked
+example, torch's FP8/bf16 conversions, torch's float64 scaled-dot-product
+attention, brute-force sorting, invariances and closed forms).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+PAGE_SIZE = 64
+INDEX_HEADS = 64
+INDEX_DIM = 128
+LATENT_DIM = 576
+V_DIM = 512
+
+__all__ = [
+    "PAGE_SIZE", "INDEX_HEADS", "INDEX_DIM", "LATENT_DIM", "V_DIM",
+    "e4m3_table", "decode_e4m3", "decode_bf16", "visible_lengths",
+    "physical_rows", "indexer_logits", "indexer_logits_at", "topk",
+    "selection_count", "split_bounds", "sparse_mla", "sparse_mla_split",
+    "merge", "decode_layer", "pair_flops_mla", "pair_flops_indexer",
+    "token_bytes_latent", "token_bytes_index", "decode_bytes",
+    "decode_flops", "dense_decode_bytes", "dense_decode_flops",
+    "layer_bytes", "layer_flops",
+]
+
+
+# ---------------------------------------------------------------------------
+# Number formats
+# ---------------------------------------------------------------------------
+
+def _e4m3_value(b: int) -> float:
+    """OCP FP8 E4M3 ("fn"): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits.
+
+    Exponent field 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there is
+    no infinity, so the largest finite magnitude is 1.75 * 2^8 = 448.
+    """
+    sign = -1.0 if b & 0x80 else 1.0
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+_E4M3 = np.array([_e4m3_value(b) for b in range(256)], dtype=np.float64)
+
+
+def e4m3_table() -> np.ndarray:
+    return _E4M3.copy()
+
+
+def decode_e4m3(u8: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 bytes -> float64 (exact)."""
+    return _E4M3[np.asarray(u8, dtype=np.uint8)]
+
+
+def decode_bf16(u16: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 (exact: bf16 is the top half of fp32)."""
+    bits = np.asarray(u16, dtype=np.uint16).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Batch geometry
+# ---------------------------------------------------------------------------
+
+def visible_lengths(seqlens, q_per_req: int) -> np.ndarray:
+    """Tokens visible to each query row, rows ordered request-major.
+
+    Request r holds S_r cached tokens, its q_per_req new tokens included;
+    query i of r sees S_r - (q_per_req - 1 - i) of them.
+    """
+    s = np.asarray(seqlens, dtype=np.int64)
+    i = np.arange(q_per_req, dtype=np.int64)
+    return (s[:, None] - (q_per_req - 1 - i)[None, :]).reshape(-1)
+
+
+def physical_rows(page_table_row, positions, page_size: int = PAGE_SIZE) -> np.ndarray:
+    """Logical token positions of one request -> rows of the paged cache."""
+    pos = np.asarray(positions, dtype=np.int64)
+    pages = np.asarray(page_table_row, dtype=np.int64)[pos // page_size]
+    return pages * page_size + pos % page_size
+
+
+# ---------------------------------------------------------------------------
+# Stage 1: lightning indexer
+# ---------------------------------------------------------------------------
+
+def indexer_logits_at(q_fp8_t, q_scale_t, w_t, k_fp8, k_scale, rows, with_bound=True):
+    """Index scores of one query token against the cache rows ``rows``.
+
+    Returns (I, E): I[s] = sum_j w_j * max(0, qhat_j . khat_s) with
+    qhat = e4m3(q) * q_scale and khat = e4m3(k) * k_scale; E[s] is the sum of
+    the absolute values of every product in that expression,
+    sum_j |w_j| * sum_d |qhat_jd * khat_sd|, the scale of the rounding error.
+    """
+    qhat = decode_e4m3(q_fp8_t).reshape(INDEX_HEADS, INDEX_DIM) * float(q_scale_t)
+    khat = decode_e4m3(k_fp8[rows]).reshape(len(rows), INDEX_DIM) * \
+        np.asarray(k_scale, dtype=np.float64)[rows][:, None]
+    w = np.asarray(w_t, dtype=np.float64).reshape(INDEX_HEADS)
+    dots = khat @ qhat.T                       # [n, 64]
+    score = np.maximum(dots, 0.0) @ w          # [n]
+    if not with_bound:
+        return score, None
+    bound = (np.abs(khat) @ np.abs(qhat).T) @ np.abs(w)
+    return score, bound
+
+
+def indexer_logits(q_fp8, q_scale, w, k_fp8, k_scale, page_table, seqlens,
+                   q_per_req: int, with_bound: bool = True):
+    """Index scores of every query row against its visible tokens.
+
+    Returns (I, E) of shape [T, max_vis]; entries at positions >= the row's
+    visible length are -inf in I and 0 in E.
+    """
+    vis = visible_lengths(seqlens, q_per_req)
+    T = vis.shape[0]
+    width = int(max(1, vis.max()))
+    I = np.full((T, width), -np.inf)
+    E = np.zeros((T, width)) if with_bound else None
+    for t in range(T):
+        r = t // q_per_req
+        n = int(vis[t])
+        if n <= 0:
+            continue
+        rows = physical_rows(page_table[r], np.arange(n))
+        s, e = indexer_logits_at(q_fp8[t], q_scale[t], w[t], k_fp8, k_scale, rows, with_bound)
+        I[t, :n] = s
+        if with_bound:
+            E[t, :n] = e
+    return I, E
+
+
+# ---------------------------------------------------------------------------
+# Stage 2: top-k
+# ---------------------------------------------------------------------------
+
+def selection_count(vis, k: int) -> np.ndarray:
+    """How many tokens a query selects: all of them when it sees <= k."""
+    return np.minimum(np.maximum(np.asarray(vis, dtype=np.int64), 0), k)
+
+
+def topk(scores, vis, k: int) -> np.ndarray:
+    """Per row, the min(k, vis) visible positions with the largest score.
+
+    ``scores`` are compared exactly as given (pass the fp32 tensor to compare
+    with a fp32 kernel); -0.0 and +0.0 are equal; equal scores are ordered by
+    lower position first.  Each row of the result lists the selected set in
+    ascending position order, padded with -1 to k entries.
+    """
+    scores = np.asarray(scores)
+    vis = np.asarray(vis, dtype=np.int64)
+    T = scores.shape[0]
+    out = np.full((T, k), -1, dtype=np.int64)
+    for t in range(T):
+        n = int(max(vis[t], 0))
+        m = min(k, n)
+        if m == 0:
+            continue
+        row = scores[t, :n].astype(np.float64) + 0.0   # -0.0 + 0.0 == +0.0
+        pos = np.arange(n)
+        order = np.lexsort((pos, -row))                # score desc, then position asc
+        out[t, :m] = np.sort(order[:m])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Stage 3: sparse MLA over the selected latent rows
+# ---------------------------------------------------------------------------
+
+def _attend(qh, rows_lat, sm_scale):
+    """Softmax attention of H query heads over n latent rows.
+
+    qh [H, 576], rows_lat [n, 576] (float64).  K = the 576-dim row, V = its
+    first 512 dims.  Returns (O [H, 512], lse [H]) with the natural-log
+    log-sum-exp of the scaled logits; n == 0 gives O = 0, lse = -inf.
+    """
+    H = qh.shape[0]
+    if rows_lat.shape[0] == 0:
+        return np.zeros((H, V_DIM)), np.full(H, -np.inf)
+    x = sm_scale * (qh @ rows_lat.T)            # [H, n]
+    m = x.max(axis=1, keepdims=True)
+    p = np.exp(x - m)
+    l = p.sum(axis=1, keepdims=True)
+    o = (p @ rows_lat[:, :V_DIM]) / l
+    return o, (m + np.log(l))[:, 0]
+
+
+def _selected_rows(idx_row, n_pos, vis_t, page_table_row):
+    """Rows of the cache attended by one query: entries at positions < n_pos
+    that name a visible token (0 <= idx < vis); other entries are skipped."""
+    ids = np.asarray(idx_row[:n_pos], dtype=np.int64)
+    ids = ids[(ids >= 0) & (ids < vis_t)]
+    return physical_rows(page_table_row, ids)
+
+
+def sparse_mla(q_bits, kv_bits, idx, page_table, seqlens, q_per_req: int, sm_scale: float,
+               tokens=None):
+    """Attention of each query row over the tokens its index row selects.
+
+    q_bits [T, H, 576] and kv_bits [rows, 576] are bf16 bit patterns.  Query
+    row t reads positions [0, min(k, vis_t)) of idx[t]; entries there that are
+    negative or >= vis_t are skipped.  Returns (O [T, H, 512], lse [T, H]).
+    ``tokens`` restricts the computation to a subset of rows (others are NaN).
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    H = q_bits.shape[1]
+    vis = visible_lengths(seqlens, q_per_req)
+    n_sel = selection_count(vis, k)
+    O = np.full((T, H, V_DIM), np.nan)
+    L = np.full((T, H), np.nan)
+    for t in (range(T) if tokens is None else tokens):
+        r = t // q_per_req
+        rows = _selected_rows(idx[t], int(n_sel[t]), int(vis[t]), page_table[r])
+        qh = decode_bf16(q_bits[t])
+        lat = decode_bf16(kv_bits[rows])
+        O[t], L[t] = _attend(qh, lat, sm_scale)
+    return O, L
+
+
+def split_bounds(k: int, num_splits: int, n_pos: int):
+    """Positions [lo, hi) of each split of one query's index row.
+
+    The row's first k positions are cut into num_splits chunks of C
+    positions, C = 64 * ceil(ceil(k / num_splits) / 64) (whole 64-token tiles);
+    chunk s covers [s*C, (s+1)*C) clipped to the n_pos positions the query
+    reads.  (The pages leave the block size open; this is the library's.)
+    """
+    per = -(-k // num_splits)
+    C = 64 * (-(-per // 64))
+    out = []
+    for s in range(num_splits):
+        lo = min(s * C, n_pos)
+        hi = min((s + 1) * C, n_pos)
+        out.append((lo, hi))
+    return out
+
+
+def sparse_mla_split(q_bits, kv_bits, idx, page_table, seqlens, q_per_req: int,
+                     sm_scale: float, num_splits: int, tokens=None):
+    """Per-split partial attention: Mid_O [T, H, S, 512] (each block's output
+    normalised by its own softmax sum) and Mid_O_LogExpSum [T, H, S]."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    H = q_bits.shape[1]
+    vis = visible_lengths(seqlens, q_per_req)
+    n_sel = selection_count(vis, k)
+    mid_o = np.full((T, H, num_splits, V_DIM), np.nan)
+    mid_l = np.full((T, H, num_splits), np.nan)
+    for t in (range(T) if tokens is None else tokens):
+        r = t // q_per_req
+        qh = decode_bf16(q_bits[t])
+        for s, (lo, hi) in enumerate(split_bounds(k, num_splits, int(n_sel[t]))):
+            ids = np.asarray(idx[t, lo:hi], dtype=np.int64)
+            ids = ids[(ids >= 0) & (ids < vis[t])]
+            lat = decode_bf16(kv_bits[physical_rows(page_table[r], ids)])
+            mid_o[t, :, s], mid_l[t, :, s] = _attend(qh, lat, sm_scale)
+    return mid_o, mid_l
+
+
+def merge(mid_o, mid_lse):
+    """Cross-split online-softmax merge.
+
+    With L = max_s lse_s: O = sum_s exp(lse_s - L) * Mid_O_s / sum_s
+    exp(lse_s - L) and lse = L + log(sum_s exp(lse_s - L)).  Splits with
+    lse = -inf contribute nothing; if every split is empty, O = 0 and
+    lse = -inf.
+    """
+    mid_o = np.asarray(mid_o, dtype=np.float64)
+    mid_lse = np.asarray(mid_lse, dtype=np.float64)
+    L = mid_lse.max(axis=-1, keepdims=True)
+    empty = ~np.isfinite(L)
+    Ls = np.where(empty, 0.0, L)
+    wgt = np.where(np.isfinite(mid_lse), np.exp(mid_lse - Ls), 0.0)
+    tot = wgt.sum(axis=-1, keepdims=True)
+    safe = np.where(tot > 0, tot, 1.0)
+    O = (wgt[..., None] * np.where(np.isfinite(mid_lse)[..., None], mid_o, 0.0)).sum(axis=-2) / safe
+    lse = np.where(tot > 0, Ls + np.log(safe), -np.inf)[..., 0]
+    return O, lse
+
+
+def decode_layer(inputs: dict, score_dtype=np.float32):
+    """The whole decode layer: indexer -> top-k -> sparse MLA.
+
+    The index scores are rounded to ``score_dtype`` before the selection, so
+    that the selection is taken in the precision of the scores a kernel
+    writes (fp32).  Returns dict(scores, bound, idx, out, lse).
+    """
+    nq = inputs["q_per_req"]
+    I, E = indexer_logits(inputs["q_fp8"], inputs["q_scale"], inputs["w"],
+                          inputs["k_fp8"], inputs["k_scale"], inputs["page_table"],
+                          inputs["seqlens"], nq)
+    vis = visible_lengths(inputs["seqlens"], nq)
+    sc = I.astype(score_dtype)
+    idx = topk(sc, vis, inputs["topk"])
+    out, lse = sparse_mla(inputs["q"], inputs["kv"], idx, inputs["page_table"],
+                          inputs["seqlens"], nq, inputs["sm_scale"])
+    return dict(scores=I, bound=E, idx=idx, out=out, lse=lse)
+
+
+# ---------------------------------------------------------------------------
+# Cost model ("Sparse attention: NSA and DSA": code cell and output table)
+# ---------------------------------------------------------------------------
+
+def pair_flops_mla(num_heads: int = 128, dc: int = 512, rope: int = 64) -> int:
+    """Absorbed MLA FLOPs per (query, key): QK over 576 dims + PV over 512."""
+    return 2 * num_heads * (dc + rope) + 2 * num_heads * dc
+
+
+def pair_flops_indexer(heads: int = INDEX_HEADS, dim: int = INDEX_DIM) -> int:
+    return 2 * heads * dim
+
+
+def token_bytes_latent(dc: int = 512, rope: int = 64) -> int:
+    return (dc + rope) * 2
+
+
+def token_bytes_index(dim: int = INDEX_DIM) -> int:
+    return dim + 4
+
+
+def dense_decode_flops(L: int, num_heads: int = 128) -> int:
+    return L * pair_flops_mla(num_heads)
+
+
+def decode_flops(L: int, k: int = 2048, num_heads: int = 128) -> int:
+    return L * pair_flops_indexer() + min(L, k) * pair_flops_mla(num_heads)
+
+
+def dense_decode_bytes(L: int) -> int:
+    return L * token_bytes_latent()
+
+
+def decode_bytes(L: int, k: int = 2048) -> int:
+    return L * token_bytes_index() + min(L, k) * token_bytes_latent()
+
+
+def layer_bytes(seqlens, q_per_req: int, k: int) -> int:
+    """Algorithmic HBM bytes of one decode layer over a batch.
+
+    Index keys (128 FP8 bytes + a 4-byte scale per cached token) are read once
+    per request and serve all its query tokens; each query token gathers its
+    selected latent rows (1152 bytes each).
+    """
+    vis = visible_lengths(seqlens, q_per_req)
+    s = np.asarray(seqlens, dtype=np.int64)
+    return int(s.sum() * token_bytes_index() + selection_count(vis, k).sum() * token_bytes_latent())
+
+
+def layer_flops(seqlens, q_per_req: int, k: int, num_heads: int):
+    """(indexer FLOPs, attention FLOPs) of one decode layer over a batch."""
+    vis = visible_lengths(seqlens, q_per_req)
+    idx = int(np.maximum(vis, 0).sum()) * pair_flops_indexer()
+    att = int(selection_count(vis, k).sum()) * pair_flops_mla(num_heads)
+    return idx, att

@@ -1,0 +1,346 @@
+"""Pins of the float64 oracle to things other than itself (CPU only).
+
+Each test checks the oracle against printed values on the pages, a library
+routine for a special case, a brute-force computation on tiny inputs, an
+invariance or a closed form, chosen so that a plausible slip in the oracle (a
+dropped ReLU, a wrong scale, a transposed page index, a reversed tie rule, a
+wrong visibility offset, a dropped softmax term) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from deepseek_sparse_attention_lightning_gb300 import workloads as W
+
+
+def _read_golden(golden_dir, name):
+    rows = []
+    with open(os.path.join(golden_dir, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- formats
+
+def test_e4m3_decode_matches_torch_all_bytes():
+    b = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.decode_e4m3(b)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert nan.sum() == 2                       # 0x7F and 0xFF only
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_bf16_decode_matches_torch():
+    x = torch.randn(4096, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.decode_bf16(bits), x.to(torch.float64).numpy())
+
+
+# ---------------------------------------------------------------- geometry
+
+def test_visible_lengths_worked_example(golden_dir):
+    g = {r[0]: r[1:] for r in _read_golden(golden_dir, "mtp_visible_lengths.txt")}
+    nq, s = int(g["q_per_req"][0]), int(g["seqlen"][0])
+    want = [int(v) for v in g["visible"]]
+    assert O.visible_lengths([s], nq).tolist() == want
+    # two requests keep request-major order
+    assert O.visible_lengths([s, 5], nq).tolist() == want + [3, 4, 5]
+
+
+def test_physical_rows_follow_page_table():
+    table = np.array([7, 2, 9])
+    pos = np.array([0, 63, 64, 130])
+    assert O.physical_rows(table, pos).tolist() == [7 * 64, 7 * 64 + 63, 2 * 64, 9 * 64 + 2]
+
+
+# ---------------------------------------------------------------- indexer
+
+def _small(**kw):
+    base = dict(batch=2, q_per_req=2, num_heads=16, topk=64, seqlen=(200, 330),
+                heavy="count:8", paged=True, seed=11)
+    base.update(kw)
+    return W.make_workload(W.small_spec("mtp_32k", **base))
+
+
+def _logits(a, **over):
+    d = dict(a)
+    d.update(over)
+    return O.indexer_logits(d["q_fp8"], d["q_scale"], d["w"], d["k_fp8"], d["k_scale"],
+                            d["page_table"], d["seqlens"], d["q_per_req"])
+
+
+def test_indexer_head_permutation_invariance():
+    a = W.host_arrays(_small())
+    I, _ = _logits(a)
+    perm = np.random.default_rng(0).permutation(O.INDEX_HEADS)
+    I2, _ = _logits(a, q_fp8=a["q_fp8"][:, perm], w=a["w"][:, perm])
+    fin = np.isfinite(I)
+    assert np.allclose(I[fin], I2[fin], rtol=1e-12, atol=1e-12)
+    # a permutation of the weights alone changes the scores
+    I3, _ = _logits(a, w=a["w"][:, perm])
+    assert not np.allclose(I[fin], I3[fin])
+
+
+def test_indexer_page_table_equivariance():
+    wl = _small(paged=False)
+    a = W.host_arrays(wl)
+    I, _ = _logits(a)
+    # move every physical page elsewhere and rewrite the table to match
+    npg = wl.num_pages
+    perm = np.random.default_rng(1).permutation(npg)        # old page p -> new page perm[p]
+    k8 = np.empty_like(a["k_fp8"])
+    ks = np.empty_like(a["k_scale"])
+    for p in range(npg):
+        k8[perm[p] * 64:(perm[p] + 1) * 64] = a["k_fp8"][p * 64:(p + 1) * 64]
+        ks[perm[p] * 64:(perm[p] + 1) * 64] = a["k_scale"][p * 64:(p + 1) * 64]
+    table = np.where(a["page_table"] >= 0, perm[np.maximum(a["page_table"], 0)], -1)
+    I2, _ = _logits(a, k_fp8=k8, k_scale=ks, page_table=table)
+    assert np.array_equal(I, I2)
+
+
+def test_indexer_scale_homogeneity():
+    a = W.host_arrays(_small())
+    I, _ = _logits(a)
+    I_k, _ = _logits(a, k_scale=a["k_scale"] * 2.0)
+    I_q, _ = _logits(a, q_scale=a["q_scale"] * 4.0)
+    fin = np.isfinite(I)
+    assert np.allclose(I_k[fin], 2.0 * I[fin], rtol=1e-13, atol=0)
+    assert np.allclose(I_q[fin], 4.0 * I[fin], rtol=1e-13, atol=0)
+
+
+def test_indexer_relu_makes_nonnegative_weights_give_nonnegative_scores():
+    a = W.host_arrays(_small())
+    wpos = np.abs(a["w"])
+    I, _ = _logits(a, w=wpos)
+    fin = np.isfinite(I)
+    assert (I[fin] >= 0).all()
+    # and the data do contain negative head dots, so the ReLU mattered:
+    qhat = O.decode_e4m3(a["q_fp8"][0]) * a["q_scale"][0]
+    khat = O.decode_e4m3(a["k_fp8"][:64]) * a["k_scale"][:64, None]
+    assert (khat @ qhat.T < 0).mean() > 0.3
+    I_neg, _ = _logits(a, w=-wpos)
+    assert (I_neg[fin] <= 0).all()
+
+
+def test_indexer_sum_of_relus_closed_form():
+    # head 0 query = the key, head 1 query = minus the key, w = (1, 1, 0, ...):
+    # sum_j w_j ReLU(q_j . k) = ReLU(|k|^2) + ReLU(-|k|^2) = |k|^2 (scaled);
+    # ReLU of the weighted sum would give 0 instead.
+    rng = np.random.default_rng(3)
+    k8 = rng.integers(0, 0x7E, size=(64, 128), dtype=np.uint8)  # finite bytes
+    q8 = np.zeros((1, 64, 128), dtype=np.uint8)
+    q8[0, 0] = k8[5]
+    q8[0, 1] = k8[5] ^ 0x80                                     # flip the sign bit
+    w = np.zeros((1, 64))
+    w[0, 0] = w[0, 1] = 1.0
+    sq, sk = np.array([0.5]), np.full(64, 0.25)
+    I, E = O.indexer_logits(q8, sq, w, k8, sk, np.array([[0]]), np.array([64]), 1)
+    kv = O.decode_e4m3(k8[5])
+    assert I[0, 5] == pytest.approx(float(kv @ kv) * 0.5 * 0.25, rel=1e-14)
+    assert E[0, 5] == pytest.approx(2 * float(kv @ kv) * 0.5 * 0.25, rel=1e-14)
+
+
+def test_indexer_positive_case_is_a_matrix_vector_product():
+    # with every FP8 value positive all head dots are positive, the ReLU is the
+    # identity and I = khat . (sum_j w_j qhat_j): one library matvec.
+    rng = np.random.default_rng(4)
+    k8 = rng.integers(0x08, 0x70, size=(128, 128), dtype=np.uint8)
+    q8 = rng.integers(0x08, 0x70, size=(1, 64, 128), dtype=np.uint8)
+    w = rng.random((1, 64))
+    sq, sk = np.array([0.01]), rng.random(128) + 0.5
+    I, E = O.indexer_logits(q8, sq, w, k8, sk, np.array([[0, 1]]), np.array([128]), 1)
+    khat = O.decode_e4m3(k8) * sk[:, None]
+    qsum = np.einsum("j,jd->d", w[0], O.decode_e4m3(q8[0]) * sq[0])
+    ref = np.dot(khat, qsum)
+    assert np.allclose(I[0], ref, rtol=1e-12)
+    assert np.allclose(E[0], I[0], rtol=1e-12)     # all terms positive: bound == value
+
+
+def test_indexer_masks_invisible_positions_and_bound_dominates():
+    wl = _small()
+    a = W.host_arrays(wl)
+    I, E = _logits(a)
+    vis = O.visible_lengths(a["seqlens"], a["q_per_req"])
+    for t, n in enumerate(vis):
+        assert np.isfinite(I[t, :n]).all()
+        assert np.isneginf(I[t, n:]).all()
+    fin = np.isfinite(I)
+    assert (E[fin] >= np.abs(I[fin]) * (1 - 1e-12)).all()
+
+
+def test_planted_heavy_tokens_score_high():
+    wl = W.make_workload(W.small_spec("tiny_4k", seqlen=1024, topk=128, heavy="count:16"))
+    a = W.host_arrays(wl)
+    I, _ = _logits(a)
+    heavy = wl.heavy[0]
+    rank = (I[0][None, :] > I[0][heavy][:, None]).sum(axis=1)
+    assert (rank < 0.01 * 1024 + len(heavy)).all()
+
+
+# ---------------------------------------------------------------- top-k
+
+def _brute_topk(row, n, k):
+    order = sorted(range(n), key=lambda i: (-float(row[i]), i))
+    return sorted(order[:min(k, n)])
+
+
+@pytest.mark.parametrize("n", [1, 5, 17, 64])
+def test_topk_matches_brute_force_sort(n):
+    rng = np.random.default_rng(n)
+    for k in {1, 3, max(1, n - 1), n, n + 5}:
+        # few distinct values so that ties are frequent
+        scores = rng.integers(-4, 5, size=(3, 80)).astype(np.float32) * 0.5
+        vis = np.array([n, max(0, n - 2), n])
+        got = O.topk(scores, vis, k)
+        for t in range(3):
+            want = _brute_topk(scores[t], int(vis[t]), k)
+            m = len(want)
+            assert got[t, :m].tolist() == want
+            assert (got[t, m:] == -1).all()
+
+
+def test_topk_ties_go_to_lower_index_and_signed_zero_is_equal():
+    scores = np.zeros((2, 10), dtype=np.float32)
+    scores[1, ::2] = -0.0
+    got = O.topk(scores, np.array([10, 10]), 4)
+    assert got[0].tolist() == [0, 1, 2, 3]
+    assert got[1].tolist() == [0, 1, 2, 3]
+
+
+def test_topk_selects_everything_when_k_exceeds_visible():
+    scores = np.random.default_rng(2).standard_normal((2, 50)).astype(np.float32)
+    got = O.topk(scores, np.array([50, 20]), 64)
+    assert got[0, :50].tolist() == list(range(50)) and (got[0, 50:] == -1).all()
+    assert got[1, :20].tolist() == list(range(20)) and (got[1, 20:] == -1).all()
+
+
+# ---------------------------------------------------------------- sparse MLA
+
+def _mla_inputs(seqlens=(90, 130), nq=1, H=16, seed=7):
+    wl = W.make_workload(W.small_spec("mtp_32k", batch=len(seqlens), q_per_req=nq,
+                                      num_heads=H, topk=256, heavy="none", seed=seed),
+                         seqlens=list(seqlens))
+    return wl, W.host_arrays(wl)
+
+
+def test_sparse_mla_all_selected_equals_dense_sdpa():
+    wl, a = _mla_inputs(seqlens=(90, 130), nq=2)
+    vis = O.visible_lengths(a["seqlens"], 2)
+    k = 256                                             # k >= every visible length
+    idx = np.full((len(vis), k), -1)
+    for t, n in enumerate(vis):
+        idx[t, :n] = np.arange(n)
+    out, lse = O.sparse_mla(a["q"], a["kv"], idx, a["page_table"], a["seqlens"], 2, a["sm_scale"])
+    for t, n in enumerate(vis):
+        r = t // 2
+        rows = O.physical_rows(a["page_table"][r], np.arange(n))
+        lat = torch.from_numpy(O.decode_bf16(a["kv"][rows]))          # [n, 576]
+        q = torch.from_numpy(O.decode_bf16(a["q"][t]))                 # [H, 576]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[None, :, None, :], lat[None, None].expand(1, q.shape[0], n, 576),
+            lat[None, None, :, :512].expand(1, q.shape[0], n, 512), scale=a["sm_scale"])
+        assert np.allclose(out[t], ref[0, :, 0].numpy(), rtol=1e-10, atol=1e-12)
+        ref_lse = torch.logsumexp(a["sm_scale"] * (q @ lat.T), dim=1).numpy()
+        assert np.allclose(lse[t], ref_lse, rtol=1e-12)
+
+
+def test_sparse_mla_index_order_invariance_and_padding():
+    wl, a = _mla_inputs(seqlens=(300,), nq=1)
+    rng = np.random.default_rng(9)
+    sel = np.sort(rng.choice(300, size=40, replace=False))
+    idx = np.full((1, 64), -1)
+    idx[0, :40] = sel
+    o1, l1 = O.sparse_mla(a["q"], a["kv"], idx, a["page_table"], a["seqlens"], 1, a["sm_scale"])
+    idx2 = idx.copy()
+    idx2[0, :40] = rng.permutation(sel)
+    o2, l2 = O.sparse_mla(a["q"], a["kv"], idx2, a["page_table"], a["seqlens"], 1, a["sm_scale"])
+    assert np.allclose(o1, o2, rtol=1e-12, atol=1e-14) and np.allclose(l1, l2, rtol=1e-13)
+    # a different set gives a different result (the test can fail)
+    idx3 = idx.copy()
+    idx3[0, 0] = [i for i in range(300) if i not in set(sel)][0]
+    o3, _ = O.sparse_mla(a["q"], a["kv"], idx3, a["page_table"], a["seqlens"], 1, a["sm_scale"])
+    assert not np.allclose(o1, o3)
+
+
+def test_sparse_mla_single_token_closed_form():
+    wl, a = _mla_inputs(seqlens=(100,), nq=1)
+    idx = np.full((1, 64), -1)
+    idx[0, 0] = 37
+    out, lse = O.sparse_mla(a["q"], a["kv"], idx, a["page_table"], a["seqlens"], 1, a["sm_scale"])
+    row = O.decode_bf16(a["kv"][O.physical_rows(a["page_table"][0], [37])[0]])
+    q = O.decode_bf16(a["q"][0])
+    assert np.allclose(out[0], np.broadcast_to(row[:512], out[0].shape), rtol=0, atol=1e-15)
+    assert np.allclose(lse[0], a["sm_scale"] * (q @ row), rtol=1e-13)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 32])
+def test_split_then_merge_equals_single_pass(splits):
+    wl, a = _mla_inputs(seqlens=(700, 1500), nq=2, seed=13)
+    vis = O.visible_lengths(a["seqlens"], 2)
+    k = 2048
+    rng = np.random.default_rng(splits)
+    idx = np.full((len(vis), k), -1)
+    for t, n in enumerate(vis):
+        m = min(k, n, 1200)                      # some rows shorter than k
+        idx[t, :m] = rng.choice(n, size=m, replace=False)
+    o, l = O.sparse_mla(a["q"], a["kv"], idx, a["page_table"], a["seqlens"], 2, a["sm_scale"])
+    mo, ml = O.sparse_mla_split(a["q"], a["kv"], idx, a["page_table"], a["seqlens"], 2,
+                                a["sm_scale"], splits)
+    om, lm = O.merge(mo, ml)
+    assert np.allclose(om, o, rtol=1e-12, atol=1e-12)
+    assert np.allclose(lm, l, rtol=1e-12, atol=1e-12)
+
+
+def test_split_bounds_cover_positions_once():
+    for k, s, n in [(2048, 9, 2048), (2048, 32, 1000), (100, 7, 100), (2048, 1, 5)]:
+        b = O.split_bounds(k, s, n)
+        covered = np.concatenate([np.arange(lo, hi) for lo, hi in b])
+        assert covered.tolist() == list(range(n))
+        assert all((lo % 64 == 0) or lo == n for lo, _ in b)
+
+
+def test_merge_ignores_empty_splits():
+    rng = np.random.default_rng(0)
+    mo = rng.standard_normal((3, 2, 512))
+    ml = np.array([[0.3, -np.inf], [-np.inf, -np.inf], [-np.inf, 1.5]])
+    o, l = O.merge(mo, ml)
+    assert np.allclose(o[0], mo[0, 0]) and l[0] == pytest.approx(0.3)
+    assert np.allclose(o[1], 0.0) and np.isneginf(l[1])
+    assert np.allclose(o[2], mo[2, 1]) and l[2] == pytest.approx(1.5)
+
+
+# ---------------------------------------------------------------- cost model
+
+def test_cost_model_reproduces_printed_table(golden_dir):
+    rows = _read_golden(golden_dir, "cost_model_table.txt")
+    table = [r for r in rows if r[0].isdigit()]
+    named = {r[0]: float(r[1]) for r in rows if not r[0].isdigit()}
+    assert len(table) == 3
+    for L, dg, sg, cr, dm, sm, rr in table:
+        L = int(L)
+        dense_f, dsa_f = O.dense_decode_flops(L), O.decode_flops(L)
+        dense_b, dsa_b = O.dense_decode_bytes(L), O.decode_bytes(L)
+        assert f"{dense_f / 1e9:.2f}" == dg and f"{dsa_f / 1e9:.2f}" == sg
+        assert f"{dense_f / dsa_f:.1f}" == cr
+        assert f"{dense_b / 2 ** 20:.1f}" == dm and f"{dsa_b / 2 ** 20:.1f}" == sm
+        assert f"{dense_b / dsa_b:.1f}" == rr
+    assert round(O.pair_flops_mla() / 1e3) == named["pair_mla_kflops"]
+    assert round(O.pair_flops_indexer() / 1e3) == named["pair_indexer_kflops"]
+    assert round(100 * O.token_bytes_index() / O.token_bytes_latent()) == named["index_cache_overhead_pct"]
+
+
+def test_layer_bytes_single_query_matches_cost_model():
+    for L in (4096, 32768, 131072):
+        assert O.layer_bytes([L], 1, 2048) == O.decode_bytes(L)
+        fi, fa = O.layer_flops([L], 1, 2048, 128)
+        assert fi + fa == O.decode_flops(L)
