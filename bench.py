@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""DSA decode-layer benchmark: indexer -> top-k -> sparse MLA -> merge.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload long_128k]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole decode layer
+over one synthetic batch (default: 8 requests x 131072 cached tokens, one
+query token each, k = 2048, 128 MLA heads), inputs resident in HBM.  Every
+step is timed with CUDA events on the launching stream; L2 is flushed (a
+256 MB write) between steps, outside the timed events.  Per-stage events from
+the library's timed entry point give the dominant kernel's (the indexer's)
+duration for the roofline.  `--impl reference` times the float64 CPU oracle on
+a bounded sample of the same workload.
+
+Multi-GPU (torchrun): one process per GPU, each runs its own batch (requests
+are independent; no data-path collective); value = all ranks' query tokens /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA decode layer µs and tokens/s at 128K ctx, k=2048; achieved HBM GB/s vs 8 TB/s"
+UNIT = "query-tokens/s"
+TARGET_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="long_128k")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def indexer_traffic(workload: str):
+    """DRAM bytes per indexer launch from the committed ncu summary, if that
+    summary was taken on the current indexer source."""
+    src = os.path.join(ROOT, "deepseek_sparse_attention_lightning_gb300", "csrc", "indexer.cu")
+    summ = os.path.join(ROOT, "profiles", f"indexer_{workload}.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        fields = {}
+        for line in open(summ):
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+        if fields.get("indexer_cu_sha256") != sha:
+            return None
+        return float(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def dist_max(x: float, world: int) -> float:
+    """Maximum of ``x`` over the ranks (the slowest rank's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(tokens_per_step: int, steps: int, world: int, total_ms_max: float) -> float:
+    """Whole-job query tokens per second: every rank ran ``steps`` steps of
+    ``tokens_per_step`` query tokens; the job took the slowest rank's time."""
+    return tokens_per_step * steps * world / (total_ms_max / 1e3)
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def accounting(spec, seqlens):
+    """Algorithmic bytes/FLOPs of one decode layer: index keys (128 FP8 B +
+    4 B scale per cached token, read once per request) + gathered latent rows
+    (1152 B per selected token per query); FLOPs 16384 per (query, visible key)
+    in the indexer and 2H*576 + 2H*512 per (query, selected key) in MLA."""
+    nq, k, H = spec.q_per_req, spec.topk, spec.num_heads
+    idx_bytes = sum(int(s) * 132 for s in seqlens)
+    sel = 0
+    vis_total = 0
+    for s in seqlens:
+        for i in range(nq):
+            v = max(int(s) - (nq - 1 - i), 0)
+            vis_total += v
+            sel += min(v, k)
+    att_bytes = sel * 1152
+    return dict(query_tokens=len(seqlens) * nq, layer_bytes=idx_bytes + att_bytes,
+                indexer_bytes=idx_bytes, attention_bytes=att_bytes,
+                indexer_flops=vis_total * 16384, attention_flops=sel * (2 * H * 576 + 2 * H * 512))
+
+
+# ---------------------------------------------------------------------------
+# CPU (oracle) leg
+# ---------------------------------------------------------------------------
+
+def oracle_rows_per_second(wl, seconds: float):
+    """Times the float64 oracle on whole requests of the workload (one request
+    at a time, its data already in host memory) until ``seconds`` elapse."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from deepseek_sparse_attention_lightning_gb300 import workloads as W
+
+    spec = wl.spec
+    nq = spec.q_per_req
+    seqlens = wl.seqlens.cpu().numpy()
+    table = wl.page_table.cpu().numpy()
+    done_rows, spent, requests = 0, 0.0, 0
+    for r in range(spec.batch):
+        S = int(seqlens[r])
+        rows = torch.from_numpy(O.physical_rows(table[r], np.arange(S))).to(wl.k_fp8.device)
+        t0, t1 = r * nq, (r + 1) * nq
+        inputs = dict(
+            seqlens=np.array([S]), page_table=np.arange((S + 63) // 64)[None, :], q_per_req=nq,
+            q_fp8=wl.q_fp8[t0:t1].cpu().numpy(), q_scale=wl.q_scale[t0:t1].cpu().numpy(),
+            w=wl.w[t0:t1].cpu().numpy(), k_fp8=wl.k_fp8[rows].cpu().numpy(),
+            k_scale=wl.k_scale[rows].cpu().numpy(), q=W.bf16_bits(wl.q[t0:t1]),
+            kv=W.bf16_bits(wl.kv[rows]), sm_scale=spec.sm_scale, topk=spec.topk)
+        pad = (-S) % 64
+        if pad:
+            inputs["k_fp8"] = np.concatenate([inputs["k_fp8"], np.zeros((pad, 128), np.uint8)])
+            inputs["k_scale"] = np.concatenate([inputs["k_scale"], np.ones(pad, np.float32)])
+            inputs["kv"] = np.concatenate([inputs["kv"], np.zeros((pad, 576), np.uint16)])
+        start = time.perf_counter()
+        O.decode_layer(inputs)
+        spent += time.perf_counter() - start
+        done_rows += nq
+        requests += 1
+        if spent >= seconds:
+            break
+    return done_rows / spent, done_rows, spent, requests
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import torch
+    from deepseek_sparse_attention_lightning_gb300 import workloads as W
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = W.make_workload(args.workload, device=dev)
+    units = accounting(wl.spec, wl.seqlens.cpu().tolist())
+    per_step = []
+    rows = 0
+    budget = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        rps, n, spent, nreq = oracle_rows_per_second(wl, budget)
+        if i >= args.warmup:
+            per_step.append(spent / n)
+            rows += n
+    sec_per_row = sum(per_step) / len(per_step)
+    value = 1.0 / sec_per_row
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec_per_row * 1e3 * units["query_tokens"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": wl.spec.batch, "q_per_req": wl.spec.q_per_req,
+                   "seqlen": wl.spec.seqlen, "topk": wl.spec.topk, "heads": wl.spec.num_heads},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{rows} query rows (whole requests, one at a time) of the "
+                                   f"{args.workload} workload, float64 numpy oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import torch
+    from deepseek_sparse_attention_lightning_gb300 import api, build
+    from deepseek_sparse_attention_lightning_gb300 import workloads as W
+
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = W.make_workload(args.workload, device=dev)
+    spec = wl.spec
+    seqlens = wl.seqlens.cpu().tolist()
+    units = accounting(spec, seqlens)
+    T, H, k = spec.num_tokens, spec.num_heads, spec.topk
+    desc = api.workload_desc(wl)
+    splits = api.dsa_num_splits_auto(desc)
+    ws = api.alloc_workspace(wl, splits)
+    out = torch.empty((T, H, 512), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def layer(stage_events=None):
+        api.dsa_decode_fused(desc, wl.q_fp8, wl.q_scale, wl.w, wl.k_fp8, wl.k_scale, wl.q, wl.kv,
+                             out, ws, wl.max_seqlen, spec.sm_scale, splits, stream=stream,
+                             stage_events=stage_events)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        layer()
+    torch.cuda.synchronize()
+    if api.dsa_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for row in ev:          # create the events (torch creates them lazily on record)
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    # keep the host ahead of the device so no step waits on a launch
+    torch.cuda._sleep(20_000_000)
+    for i in range(K):
+        flush.zero_()
+        layer(ev[i])
+        if i % 256 == 255:
+            torch.cuda._sleep(2_000_000)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clocks = sampler.stop()
+    if api.dsa_get_device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+    step_ms = [ev[i][0].elapsed_time(ev[i][4]) for i in range(K)]
+    idx_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    topk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    mla_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    merge_ms = [ev[i][3].elapsed_time(ev[i][4]) for i in range(K)]
+    total_ms = sum(step_ms)
+    total_ms_max = dist_max(total_ms, world)
+    ms_per_step = total_ms_max / K
+    value = throughput(units["query_tokens"], K, world, total_ms_max)
+
+    # ---- end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: t.cpu().pin_memory() for n, t in
+                   (("q_fp8", wl.q_fp8), ("q_scale", wl.q_scale), ("w", wl.w), ("q", wl.q),
+                    ("seqlens", wl.seqlens), ("page_table", wl.page_table))}
+        dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        ddesc = api.make_desc(dev_in["seqlens"], dev_in["page_table"], spec.q_per_req, H, k,
+                              wl.num_pages)
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = out_host.numel() * out_host.element_size()
+        KE = max(1, min(K, 500))
+        e_start = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+        e_end = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+        for i in range(KE + 3):
+            flush.zero_()
+            j = i - 3
+            if j >= 0:
+                e_start[j].record()
+            for n in host_in:
+                dev_in[n].copy_(host_in[n], non_blocking=True)
+            api.dsa_decode_fused(ddesc, dev_in["q_fp8"], dev_in["q_scale"], dev_in["w"], wl.k_fp8,
+                                 wl.k_scale, dev_in["q"], wl.kv, out, ws, wl.max_seqlen,
+                                 spec.sm_scale, splits, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+            if j >= 0:
+                e_end[j].record()
+        torch.cuda.synchronize()
+        e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_start, e_end))
+        e2e_ms = dist_max(e2e_ms, world)
+        e2e = {"value": throughput(units["query_tokens"], KE, world, e2e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / KE,
+               "note": "per-step inputs (index/MLA queries, weights, scales, seqlens, page table) "
+                       "copied from pinned host memory and the output read back; the KV caches "
+                       "stay resident in HBM as model state"}
+        if not torch.allclose(out_host, out.cpu()):
+            raise RuntimeError("e2e output differs from the device output")
+
+    # ---- CPU oracle baseline (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rps, n, spent, nreq = oracle_rows_per_second(wl, args.cpu_seconds)
+        cpu = {"value": rps, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{n} query rows ({nreq} whole requests of {args.workload}, one at a time, "
+                         f"{spent:.1f} s), float64 numpy oracle (BLAS threads = cores)"}
+
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    idx_mean_ms = statistics.mean(idx_ms)
+    idx_gbs = units["indexer_bytes"] / (idx_mean_ms / 1e3) / 1e9
+    layer_gbs = units["layer_bytes"] / (ms_per_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 (indexer) + bf16 (MLA), fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": spec.batch, "q_per_req": spec.q_per_req,
+                   "seqlen": spec.seqlen, "topk": k, "heads": H, "index_heads": 64,
+                   "page_size": 64, "num_splits": splits,
+                   "l2": "flushed between steps (256 MB write, outside the timed events)",
+                   "parallelism": f"replicas x{world} (independent batches per GPU)"},
+        "us_per_layer": ms_per_step * 1e3,
+        "layer_bytes": units["layer_bytes"],
+        "layer_gbs": layer_gbs,
+        "layer_frac_of_8tbs": layer_gbs / TARGET_HBM_GBS,
+        "layer_frac_of_measured_hbm": layer_gbs / hbm,
+        "stage_us": {"indexer": idx_mean_ms * 1e3, "topk": statistics.mean(topk_ms) * 1e3,
+                     "sparse_mla": statistics.mean(mla_ms) * 1e3,
+                     "merge": statistics.mean(merge_ms) * 1e3},
+        "roofline": {"kernel": "indexer_kernel", "bound": "hbm", "achieved": idx_gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": idx_gbs / hbm,
+                     "traffic": indexer_traffic(args.workload),
+                     "algorithmic_bytes": units["indexer_bytes"],
+                     "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * (3 + (1 if splits > 1 else 0)),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,281 @@
+"""ctypes binding of libdsa.so: the C ABI of include/dsa.h, same names.
+
+Argument marshalling only: every step of the decode path runs in the
+library's CUDA kernels.  Tensors are torch CUDA tensors (torch provides device
+memory and streams); each wrapper checks dtype, device and contiguity, passes
+raw pointers, and raises ``DSAError`` on a non-zero status.  There is no CPU
+fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_float, c_int32, c_int64, c_size_t, c_void_p
+
+import torch
+
+from . import build as _build
+
+DSA_OK = 0
+STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
+                3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE_CHECK",
+                6: "DSA_ERR_TIMEOUT"}
+PAGE_SIZE = 64
+
+
+class DSAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class DecodeDesc(ctypes.Structure):
+    _fields_ = [("batch", c_int32), ("q_per_req", c_int32), ("num_heads", c_int32),
+                ("topk", c_int32), ("page_size", c_int32), ("max_pages", c_int32),
+                ("num_pages", c_int32), ("seqlens", c_void_p), ("page_table", c_void_p)]
+
+
+_SIGS = {
+    "dsa_indexer_logits": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_int64, c_void_p]),
+    "dsa_topk": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_int64, c_void_p, c_void_p,
+                           c_size_t, c_void_p]),
+    "dsa_topk_workspace_bytes": (c_size_t, [ctypes.POINTER(DecodeDesc), c_int64]),
+    "dsa_sparse_mla_decode_split": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p,
+                                              c_void_p, c_int32, c_float, c_void_p, c_void_p,
+                                              c_void_p]),
+    "dsa_merge": (c_int32, [c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dsa_decode_fused": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_float, c_int32, c_int32, c_void_p, c_void_p, c_size_t,
+                                   c_void_p]),
+    "dsa_decode_fused_timed": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_float, c_int32, c_int32, c_void_p, c_void_p,
+                                         c_size_t, c_void_p, ctypes.POINTER(c_void_p)]),
+    "dsa_workspace_bytes": (c_size_t, [ctypes.POINTER(DecodeDesc), c_int32, c_int32]),
+    "dsa_num_splits_auto": (c_int32, [ctypes.POINTER(DecodeDesc)]),
+    "dsa_status_str": (ctypes.c_char_p, [c_int32]),
+    "dsa_get_device_error": (c_int32, [c_void_p]),
+    "dsa_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libdsa.so (built in-tree by ``build.build()``); raises if absent."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libdsa.so not built at {path}: run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != DSA_OK:
+        raise DSAError(status, where)
+
+
+def _ptr(t, dtype, name, ndim=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got {t.dim()}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _u16(t: torch.Tensor, name):
+    if t.dtype == torch.bfloat16:
+        return _ptr(t, torch.bfloat16, name)
+    return _ptr(t, torch.int16, name)
+
+
+def make_desc(seqlens: torch.Tensor, page_table: torch.Tensor, q_per_req: int, num_heads: int,
+              topk: int, num_pages: int) -> DecodeDesc:
+    """Descriptor of one decode batch (keeps no reference to the tensors)."""
+    B = int(seqlens.shape[0])
+    return DecodeDesc(batch=B, q_per_req=int(q_per_req), num_heads=int(num_heads),
+                      topk=int(topk), page_size=PAGE_SIZE, max_pages=int(page_table.shape[1]),
+                      num_pages=int(num_pages),
+                      seqlens=_ptr(seqlens, torch.int32, "seqlens", 1),
+                      page_table=_ptr(page_table, torch.int32, "page_table", 2))
+
+
+def dsa_indexer_logits(desc, q_fp8, q_scale, w, k_fp8, k_scale, logits, ld=None, stream=None):
+    ld = int(logits.shape[-1]) if ld is None else int(ld)
+    _check(lib().dsa_indexer_logits(
+        ctypes.byref(desc), _ptr(q_fp8, torch.uint8, "q_fp8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(w, torch.float32, "w"), _ptr(k_fp8, torch.uint8, "k_fp8"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(logits, torch.float32, "logits"), ld,
+        _stream(stream)), "dsa_indexer_logits")
+
+
+def dsa_topk_workspace_bytes(desc, ld) -> int:
+    return int(lib().dsa_topk_workspace_bytes(ctypes.byref(desc), int(ld)))
+
+
+def dsa_topk(desc, logits, topk_idx, ws, ld=None, stream=None):
+    ld = int(logits.shape[-1]) if ld is None else int(ld)
+    _check(lib().dsa_topk(ctypes.byref(desc), _ptr(logits, torch.float32, "logits"), ld,
+                          _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(ws, torch.uint8, "ws"),
+                          ws.numel(), _stream(stream)), "dsa_topk")
+
+
+def dsa_sparse_mla_decode_split(desc, q, kv, topk_idx, num_splits, sm_scale, mid_o, mid_lse,
+                                stream=None):
+    _check(lib().dsa_sparse_mla_decode_split(
+        ctypes.byref(desc), _u16(q, "q"), _u16(kv, "kv"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        int(num_splits), float(sm_scale), _ptr(mid_o, torch.float32, "mid_o"),
+        _ptr(mid_lse, torch.float32, "mid_lse"), _stream(stream)), "dsa_sparse_mla_decode_split")
+
+
+def dsa_merge(num_rows, num_splits, mid_o, mid_lse, out, out_lse=None, stream=None):
+    _check(lib().dsa_merge(int(num_rows), int(num_splits), _ptr(mid_o, torch.float32, "mid_o"),
+                           _ptr(mid_lse, torch.float32, "mid_lse"), _ptr(out, torch.float32, "out"),
+                           _ptr(out_lse, torch.float32, "out_lse"), _stream(stream)), "dsa_merge")
+
+
+def dsa_workspace_bytes(desc, max_seqlen, num_splits=0) -> int:
+    return int(lib().dsa_workspace_bytes(ctypes.byref(desc), int(max_seqlen), int(num_splits)))
+
+
+def dsa_num_splits_auto(desc) -> int:
+    return int(lib().dsa_num_splits_auto(ctypes.byref(desc)))
+
+
+def dsa_decode_fused(desc, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, out, ws, max_seqlen,
+                     sm_scale, num_splits=0, topk_in=None, topk_out=None, stream=None,
+                     stage_events=None):
+    """``stage_events``: optional list of 5 torch.cuda.Event (timing enabled)."""
+    if stage_events is not None:
+        arr = (c_void_p * 5)(*[ev.cuda_event if ev is not None else None for ev in stage_events])
+        _check(lib().dsa_decode_fused_timed(
+            ctypes.byref(desc), _ptr(q_fp8, torch.uint8, "q_fp8"),
+            _ptr(q_scale, torch.float32, "q_scale"), _ptr(w, torch.float32, "w"),
+            _ptr(k_fp8, torch.uint8, "k_fp8"), _ptr(k_scale, torch.float32, "k_scale"),
+            _u16(q, "q"), _u16(kv, "kv"), _ptr(topk_in, torch.int32, "topk_in"),
+            _ptr(topk_out, torch.int32, "topk_out"), float(sm_scale), int(num_splits),
+            int(max_seqlen), _ptr(out, torch.float32, "out"), _ptr(ws, torch.uint8, "ws"),
+            ws.numel(), _stream(stream), arr), "dsa_decode_fused_timed")
+        return
+    _check(lib().dsa_decode_fused(
+        ctypes.byref(desc), _ptr(q_fp8, torch.uint8, "q_fp8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(w, torch.float32, "w"), _ptr(k_fp8, torch.uint8, "k_fp8"),
+        _ptr(k_scale, torch.float32, "k_scale"), _u16(q, "q"), _u16(kv, "kv"),
+        _ptr(topk_in, torch.int32, "topk_in"), _ptr(topk_out, torch.int32, "topk_out"),
+        float(sm_scale), int(num_splits), int(max_seqlen), _ptr(out, torch.float32, "out"),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "dsa_decode_fused")
+
+
+def dsa_get_device_error(stream=None) -> int:
+    return int(lib().dsa_get_device_error(_stream(stream)))
+
+
+def dsa_status_str(status: int) -> str:
+    return lib().dsa_status_str(int(status)).decode()
+
+
+def dsa_version() -> str:
+    return lib().dsa_version().decode()
+
+
+# ---------------------------------------------------------------------------
+# Convenience layer over a synthetic ``workloads.Workload`` (allocates outputs
+# with torch, then calls the ABI above).
+# ---------------------------------------------------------------------------
+
+def workload_desc(wl) -> DecodeDesc:
+    s = wl.spec
+    return make_desc(wl.seqlens, wl.page_table, s.q_per_req, s.num_heads, s.topk, wl.num_pages)
+
+
+def logits_ld(wl) -> int:
+    return wl.max_pages * PAGE_SIZE
+
+
+def run_indexer(wl, layer: int = 0, stream=None) -> torch.Tensor:
+    lc = wl.layers[layer]
+    T = wl.spec.num_tokens
+    ld = logits_ld(wl)
+    logits = torch.full((T, ld), float("nan"), device=wl.q_fp8.device, dtype=torch.float32)
+    dsa_indexer_logits(workload_desc(wl), wl.q_fp8, wl.q_scale, wl.w, lc.k_fp8, lc.k_scale,
+                       logits, ld, stream)
+    return logits
+
+
+def run_topk(wl, logits: torch.Tensor, stream=None) -> torch.Tensor:
+    desc = workload_desc(wl)
+    ld = int(logits.shape[1])
+    ws = torch.empty(dsa_topk_workspace_bytes(desc, ld), dtype=torch.uint8, device=logits.device)
+    out = torch.empty((wl.spec.num_tokens, wl.spec.topk), dtype=torch.int32, device=logits.device)
+    dsa_topk(desc, logits, out, ws, ld, stream)
+    return out
+
+
+def run_sparse_mla_split(wl, topk_idx, num_splits=0, layer: int = 0, stream=None):
+    lc = wl.layers[layer]
+    desc = workload_desc(wl)
+    S = dsa_num_splits_auto(desc) if num_splits == 0 else num_splits
+    T, H = wl.spec.num_tokens, wl.spec.num_heads
+    mid_o = torch.empty((T, H, S, 512), dtype=torch.float32, device=lc.q.device)
+    mid_lse = torch.empty((T, H, S), dtype=torch.float32, device=lc.q.device)
+    dsa_sparse_mla_decode_split(desc, lc.q, lc.kv, topk_idx, S, wl.spec.sm_scale, mid_o, mid_lse,
+                                stream)
+    return mid_o, mid_lse
+
+
+def run_merge(mid_o, mid_lse, stream=None):
+    T, H, S, _ = mid_o.shape
+    out = torch.empty((T, H, 512), dtype=torch.float32, device=mid_o.device)
+    lse = torch.empty((T, H), dtype=torch.float32, device=mid_o.device)
+    dsa_merge(T * H, S, mid_o, mid_lse, out, lse, stream)
+    return out, lse
+
+
+def alloc_workspace(wl, num_splits=0) -> torch.Tensor:
+    desc = workload_desc(wl)
+    n = dsa_workspace_bytes(desc, wl.max_seqlen, num_splits)
+    return torch.empty(n, dtype=torch.uint8, device=wl.q_fp8.device)
+
+
+def run_decode(wl, ws=None, num_splits=0, layer: int = 0, topk_in=None, topk_out=None,
+               out=None, stream=None, stage_events=None) -> torch.Tensor:
+    lc = wl.layers[layer]
+    T, H = wl.spec.num_tokens, wl.spec.num_heads
+    if ws is None:
+        ws = alloc_workspace(wl, num_splits)
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.float32, device=lc.q.device)
+    dsa_decode_fused(workload_desc(wl), wl.q_fp8, wl.q_scale, wl.w, lc.k_fp8, lc.k_scale, lc.q,
+                     lc.kv, out, ws, wl.max_seqlen, wl.spec.sm_scale, num_splits, topk_in,
+                     topk_out, stream, stage_events)
+    return out

@@ -1,0 +1,337 @@
+// dsa_api.cu -- the C ABI of libdsa.so (declared and documented in
+// include/dsa.h): argument validation, workspace layout, TMA descriptor
+// encoding and the launch sequence of the decode layer.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "dsa.h"
+#include "dsa_internal.h"
+
+namespace dsa {
+
+namespace {
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_sm_count[64] = {0};
+}  // namespace
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle swizzle) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) return g_sm_count[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev >= 0 && dev < 64) g_sm_count[dev] = n;
+  return n;
+}
+
+}  // namespace dsa
+
+namespace {
+
+using dsa::kHistBins;
+using dsa::kCounterWords;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+dsa_status check_desc(const dsa_decode_desc* d) {
+  if (!d) return DSA_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->q_per_req < 1 || d->num_heads < 1 || d->topk < 1 || d->max_pages < 1 ||
+      d->num_pages < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (!d->seqlens || !d->page_table || !aligned(d->seqlens, 4) || !aligned(d->page_table, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (d->batch > DSA_MAX_BATCH || d->q_per_req > DSA_MAX_Q_PER_REQ) return DSA_ERR_UNSUPPORTED;
+  if (d->num_heads > 128 || d->num_heads % 16 != 0) return DSA_ERR_UNSUPPORTED;
+  if (d->topk > DSA_MAX_TOPK || d->page_size != DSA_PAGE_SIZE) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->num_pages) * DSA_PAGE_SIZE >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE >= (int64_t(1) << 31))
+    return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+int rows_of(const dsa_decode_desc* d) { return d->batch * d->q_per_req; }
+
+int max_splits(const dsa_decode_desc* d) { return (d->topk + 63) / 64; }
+
+int resolve_splits(const dsa_decode_desc* d, int32_t num_splits) {
+  return num_splits == 0 ? dsa_num_splits_auto(d) : num_splits;
+}
+
+dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+struct TopkWs {
+  size_t hist, counters, cand, total;
+};
+
+TopkWs topk_ws_layout(int T, int64_t ld) {
+  TopkWs w;
+  w.hist = 0;
+  w.counters = w.hist + size_t(T) * kHistBins * 4;
+  w.cand = align256(w.counters + size_t(T) * kCounterWords * 4);
+  w.total = align256(w.cand + size_t(T) * size_t(ld) * 8);
+  return w;
+}
+
+struct FusedWs {
+  int64_t ld;
+  size_t logits, hist, counters, cand, topk, mid_o, mid_lse, total;
+};
+
+FusedWs fused_ws_layout(const dsa_decode_desc* d, int32_t max_seqlen, int splits) {
+  FusedWs w;
+  const int T = rows_of(d);
+  w.ld = ((static_cast<int64_t>(max_seqlen) + 127) / 128) * 128;
+  w.logits = 0;
+  w.hist = align256(w.logits + size_t(T) * size_t(w.ld) * 4);
+  w.counters = w.hist + size_t(T) * kHistBins * 4;
+  w.cand = align256(w.counters + size_t(T) * kCounterWords * 4);
+  w.topk = align256(w.cand + size_t(T) * size_t(w.ld) * 8);
+  w.mid_o = align256(w.topk + size_t(T) * size_t(d->topk) * 4);
+  const size_t mo = splits > 1 ? size_t(T) * d->num_heads * splits * dsa::kVDim * 4 : 0;
+  w.mid_lse = align256(w.mid_o + mo);
+  w.total = align256(w.mid_lse + size_t(T) * d->num_heads * splits * 4);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_str(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE_CHECK: return "DSA_ERR_DEVICE_CHECK";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+const char* dsa_version(void) { return "dsa-gb300 0.1 (sm_103a)"; }
+
+int32_t dsa_num_splits_auto(const dsa_decode_desc* d) {
+  if (!d || d->batch < 1 || d->q_per_req < 1 || d->topk < 1) return 1;
+  const int T = rows_of(d);
+  const int sms = dsa::device_sm_count();
+  int s = sms / (2 * T);
+  if (s < 1) s = 1;
+  if (s > max_splits(d)) s = max_splits(d);
+  return s;
+}
+
+dsa_status dsa_indexer_logits(const dsa_decode_desc* d, const uint8_t* q_fp8, const float* q_scale,
+                              const float* w, const uint8_t* k_fp8, const float* k_scale,
+                              float* logits, int64_t ld, void* stream) {
+  dsa_status st = check_desc(d);
+  if (st != DSA_OK) return st;
+  if (!q_fp8 || !q_scale || !w || !k_fp8 || !k_scale || !logits) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q_fp8, 16) || !aligned(k_fp8, 16) || !aligned(logits, 16) || !aligned(q_scale, 4) ||
+      !aligned(w, 4) || !aligned(k_scale, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (ld < static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE || ld % 4 != 0)
+    return DSA_ERR_INVALID_ARG;
+  dsa::IndexerLaunch a{};
+  a.q_fp8 = q_fp8; a.q_scale = q_scale; a.w = w; a.k_fp8 = k_fp8; a.k_scale = k_scale;
+  a.seqlens = d->seqlens; a.page_table = d->page_table; a.logits = logits; a.ld = ld;
+  a.hist = nullptr; a.batch = d->batch; a.nq = d->q_per_req; a.max_pages = d->max_pages;
+  a.num_pages = d->num_pages; a.topk = d->topk; a.skip_short = 0;
+  return cuda_status(dsa::launch_indexer(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_topk_workspace_bytes(const dsa_decode_desc* d, int64_t ld) {
+  if (!d || d->batch < 1 || d->q_per_req < 1 || ld < 1) return 0;
+  return topk_ws_layout(rows_of(d), ld).total;
+}
+
+dsa_status dsa_topk(const dsa_decode_desc* d, const float* logits, int64_t ld, int32_t* topk_idx,
+                    void* ws, size_t ws_bytes, void* stream) {
+  dsa_status st = check_desc(d);
+  if (st != DSA_OK) return st;
+  if (!logits || !topk_idx || !aligned(logits, 16) || !aligned(topk_idx, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (ld < static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE || ld % 4 != 0)
+    return DSA_ERR_INVALID_ARG;
+  const TopkWs lay = topk_ws_layout(rows_of(d), ld);
+  if (!ws || !aligned(ws, 16) || ws_bytes < lay.total) return DSA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  cudaError_t e = cudaMemsetAsync(base + lay.hist, 0, lay.cand - lay.hist, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  dsa::TopkLaunch a{};
+  a.seqlens = d->seqlens; a.logits = logits; a.ld = ld; a.out = topk_idx;
+  a.hist = reinterpret_cast<uint32_t*>(base + lay.hist);
+  a.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
+  a.cand = reinterpret_cast<uint2*>(base + lay.cand);
+  a.batch = d->batch; a.nq = d->q_per_req; a.k = d->topk; a.hist_ready = 0;
+  return cuda_status(dsa::launch_topk(a, s));
+}
+
+dsa_status dsa_sparse_mla_decode_split(const dsa_decode_desc* d, const uint16_t* q,
+                                       const uint16_t* kv, const int32_t* topk_idx,
+                                       int32_t num_splits, float sm_scale, float* mid_o,
+                                       float* mid_lse, void* stream) {
+  dsa_status st = check_desc(d);
+  if (st != DSA_OK) return st;
+  if (!q || !kv || !topk_idx || !mid_o || !mid_lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(mid_o, 16) || !aligned(topk_idx, 4) ||
+      !aligned(mid_lse, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  const int splits = resolve_splits(d, num_splits);
+  if (splits < 1 || splits > max_splits(d)) return DSA_ERR_INVALID_ARG;
+  dsa::MlaLaunch a{};
+  a.q = q; a.kv = kv; a.topk_idx = topk_idx; a.seqlens = d->seqlens; a.page_table = d->page_table;
+  a.mid_o = mid_o; a.mid_lse = mid_lse; a.batch = d->batch; a.nq = d->q_per_req;
+  a.heads = d->num_heads; a.k = d->topk; a.max_pages = d->max_pages; a.num_pages = d->num_pages;
+  a.num_splits = splits; a.sm_scale = sm_scale;
+  return cuda_status(dsa::launch_sparse_mla(a, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_merge(int32_t num_rows, int32_t num_splits, const float* mid_o, const float* mid_lse,
+                     float* out, float* out_lse, void* stream) {
+  if (num_rows < 0 || num_splits < 1) return DSA_ERR_INVALID_ARG;
+  if (num_splits > 32) return DSA_ERR_UNSUPPORTED;
+  if (num_rows == 0) return DSA_OK;
+  if (!mid_o || !mid_lse || !out || !aligned(mid_o, 16) || !aligned(out, 16) ||
+      !aligned(mid_lse, 4) || (out_lse && !aligned(out_lse, 4)))
+    return DSA_ERR_INVALID_ARG;
+  return cuda_status(dsa::launch_merge(num_rows, num_splits, mid_o, mid_lse, out, out_lse,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_workspace_bytes(const dsa_decode_desc* d, int32_t max_seqlen, int32_t num_splits) {
+  if (!d || d->batch < 1 || d->q_per_req < 1 || d->topk < 1 || d->num_heads < 1 ||
+      max_seqlen < 1 || num_splits < 0)
+    return 0;
+  return fused_ws_layout(d, max_seqlen, resolve_splits(d, num_splits)).total;
+}
+
+dsa_status dsa_decode_fused(const dsa_decode_desc* d, const uint8_t* q_fp8, const float* q_scale,
+                            const float* w, const uint8_t* k_fp8, const float* k_scale,
+                            const uint16_t* q, const uint16_t* kv, const int32_t* topk_in,
+                            int32_t* topk_out, float sm_scale, int32_t num_splits,
+                            int32_t max_seqlen, float* out, void* ws, size_t ws_bytes,
+                            void* stream) {
+  return dsa_decode_fused_timed(d, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, topk_in, topk_out,
+                                sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream,
+                                nullptr);
+}
+
+dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8,
+                                  const float* q_scale, const float* w, const uint8_t* k_fp8,
+                                  const float* k_scale, const uint16_t* q, const uint16_t* kv,
+                                  const int32_t* topk_in, int32_t* topk_out, float sm_scale,
+                                  int32_t num_splits, int32_t max_seqlen, float* out, void* ws,
+                                  size_t ws_bytes, void* stream, void* const* stage_events) {
+  dsa_status st = check_desc(d);
+  if (st != DSA_OK) return st;
+  if (!q || !kv || !out || !aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16))
+    return DSA_ERR_INVALID_ARG;
+  if (!topk_in && (!q_fp8 || !q_scale || !w || !k_fp8 || !k_scale || !aligned(q_fp8, 16) ||
+                   !aligned(k_fp8, 16) || !aligned(q_scale, 4) || !aligned(w, 4) ||
+                   !aligned(k_scale, 4)))
+    return DSA_ERR_INVALID_ARG;
+  if ((topk_in && !aligned(topk_in, 4)) || (topk_out && !aligned(topk_out, 4)))
+    return DSA_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  if (max_seqlen < 1 || static_cast<int64_t>(max_seqlen) > static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE)
+    return DSA_ERR_INVALID_ARG;
+  const int splits = resolve_splits(d, num_splits);
+  if (splits < 1 || splits > max_splits(d)) return DSA_ERR_INVALID_ARG;
+  if (splits > 32) return DSA_ERR_UNSUPPORTED;
+  const FusedWs lay = fused_ws_layout(d, max_seqlen, splits);
+  if (!ws || !aligned(ws, 256) || ws_bytes < lay.total) return DSA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const int T = rows_of(d);
+
+  auto mark = [&](int i) -> bool {
+    return !stage_events || !stage_events[i] ||
+           cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s) == cudaSuccess;
+  };
+  const int32_t* idx = topk_in;
+  if (!topk_in) {
+    int32_t* sel = topk_out ? topk_out : reinterpret_cast<int32_t*>(base + lay.topk);
+    cudaError_t e = cudaMemsetAsync(base + lay.hist, 0, lay.cand - lay.hist, s);
+    if (e != cudaSuccess || !mark(0)) return DSA_ERR_CUDA;
+    dsa::IndexerLaunch ia{};
+    ia.q_fp8 = q_fp8; ia.q_scale = q_scale; ia.w = w; ia.k_fp8 = k_fp8; ia.k_scale = k_scale;
+    ia.seqlens = d->seqlens; ia.page_table = d->page_table;
+    ia.logits = reinterpret_cast<float*>(base + lay.logits); ia.ld = lay.ld;
+    ia.hist = reinterpret_cast<uint32_t*>(base + lay.hist);
+    ia.batch = d->batch; ia.nq = d->q_per_req; ia.max_pages = d->max_pages;
+    ia.num_pages = d->num_pages; ia.topk = d->topk; ia.skip_short = 1;
+    e = dsa::launch_indexer(ia, s);
+    if (e != cudaSuccess || !mark(1)) return DSA_ERR_CUDA;
+    dsa::TopkLaunch ta{};
+    ta.seqlens = d->seqlens; ta.logits = ia.logits; ta.ld = lay.ld; ta.out = sel;
+    ta.hist = ia.hist; ta.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
+    ta.cand = reinterpret_cast<uint2*>(base + lay.cand);
+    ta.batch = d->batch; ta.nq = d->q_per_req; ta.k = d->topk; ta.hist_ready = 1;
+    e = dsa::launch_topk(ta, s);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    idx = sel;
+  } else if (!mark(0) || !mark(1)) {
+    return DSA_ERR_CUDA;
+  }
+  if (!mark(2)) return DSA_ERR_CUDA;
+  dsa::MlaLaunch ma{};
+  ma.q = q; ma.kv = kv; ma.topk_idx = idx; ma.seqlens = d->seqlens; ma.page_table = d->page_table;
+  ma.mid_o = splits > 1 ? reinterpret_cast<float*>(base + lay.mid_o) : out;
+  ma.mid_lse = reinterpret_cast<float*>(base + lay.mid_lse);
+  ma.batch = d->batch; ma.nq = d->q_per_req; ma.heads = d->num_heads; ma.k = d->topk;
+  ma.max_pages = d->max_pages; ma.num_pages = d->num_pages; ma.num_splits = splits;
+  ma.sm_scale = sm_scale;
+  cudaError_t e = dsa::launch_sparse_mla(ma, s);
+  if (e != cudaSuccess || !mark(3)) return DSA_ERR_CUDA;
+  if (splits > 1) {
+    e = dsa::launch_merge(T * d->num_heads, splits, ma.mid_o, ma.mid_lse, out, nullptr, s);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  if (!mark(4)) return DSA_ERR_CUDA;
+  return DSA_OK;
+}
+
+dsa_status dsa_get_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  const int codes[4] = {dsa::fetch_error_indexer(), dsa::fetch_error_topk(), dsa::fetch_error_mla(),
+                        dsa::fetch_error_merge()};
+  for (int c : codes)
+    if (c != 0) return static_cast<dsa_status>(c);
+  return DSA_OK;
+}
+
+}  // extern "C"

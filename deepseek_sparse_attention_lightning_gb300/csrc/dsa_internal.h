@@ -1,0 +1,95 @@
+// dsa_internal.h -- declarations shared by the translation units of libdsa.so
+// (launchers and device-error accessors).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dsa {
+
+constexpr int kIndexHeads = 64;
+constexpr int kIndexDim = 128;
+constexpr int kLatentDim = 576;
+constexpr int kVDim = 512;
+constexpr int kPage = 64;
+constexpr int kHistBins = 2048;     // top 11 bits of the order-preserving score key
+constexpr int kHistShift = 21;
+constexpr int kTopkChunk = 8192;    // logits per CTA in the top-k passes
+constexpr int kCounterWords = 4;    // per query row: selected, candidates, ticket, spare
+
+struct IndexerLaunch {
+  const uint8_t* q_fp8;
+  const float* q_scale;
+  const float* w;
+  const uint8_t* k_fp8;
+  const float* k_scale;
+  const int32_t* seqlens;
+  const int32_t* page_table;
+  float* logits;
+  int64_t ld;
+  uint32_t* hist;       // [T][kHistBins] or nullptr
+  int batch, nq, max_pages, num_pages, topk;
+  int skip_short;       // skip requests whose queries all see <= topk tokens
+};
+
+struct TopkLaunch {
+  const int32_t* seqlens;
+  const float* logits;
+  int64_t ld;
+  int32_t* out;         // [T][k]
+  uint32_t* hist;       // [T][kHistBins], zeroed (or filled by the indexer)
+  uint32_t* counters;   // [T][kCounterWords], zeroed
+  uint2* cand;          // [T][ld]
+  int batch, nq, k;
+  int hist_ready;       // 1: hist already holds the row histograms
+};
+
+struct MlaLaunch {
+  const uint16_t* q;
+  const uint16_t* kv;
+  const int32_t* topk_idx;
+  const int32_t* seqlens;
+  const int32_t* page_table;
+  float* mid_o;
+  float* mid_lse;
+  int batch, nq, heads, k, max_pages, num_pages, num_splits;
+  float sm_scale;
+};
+
+cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t s);
+cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s);
+cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t s);
+cudaError_t launch_merge(int rows, int splits, const float* mid_o, const float* mid_lse,
+                         float* out, float* out_lse, cudaStream_t s);
+
+// Each translation unit keeps its own device error word; these read and clear
+// them (synchronous).  Return 0 or a dsa_status code.
+int fetch_error_indexer();
+int fetch_error_topk();
+int fetch_error_mla();
+int fetch_error_merge();
+
+// Host helpers (dsa_api.cu).
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                    uint32_t box_outer, CUtensorMapSwizzle swizzle);
+int device_sm_count();
+
+}  // namespace dsa
+
+// Defines the per-TU device error word and its host accessor.
+#define DSA_DEFINE_ERROR_WORD(NAME)                                                    \
+  namespace dsa {                                                                      \
+  static __device__ int g_error_word = 0;                                              \
+  __device__ __forceinline__ void raise_error(int code) {                              \
+    atomicCAS(&g_error_word, 0, code);                                                 \
+  }                                                                                    \
+  int fetch_error_##NAME() {                                                           \
+    int v = 0, zero = 0;                                                               \
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return 4;  \
+    if (v != 0) cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));                  \
+    return v;                                                                          \
+  }                                                                                    \
+  }

@@ -1,0 +1,385 @@
+// indexer.cu -- stage 1, the lightning indexer, on tcgen05 tensor cores.
+//
+// Score ("MTP and sparse attention: NSA and DSA", section "Sparse attention:
+// NSA and DSA"):  I[t,s] = sum_j w[t,j] * ReLU(q^I[t,j] . k^I[s]),
+// 64 heads x 128 dims in FP8 E4M3 with one fp32 scale per token.  With
+// positive scales, I[t,s] = ks[s] * sum_j (w[t,j] * qs[t]) * ReLU(q8[t,j] . k8[s]).
+//
+// Mapping: one MMA tile is 128 cached tokens (two 64-token pages) x the
+// 64 * n_q index heads of one request's query tokens, K = 128 FP8 bytes:
+//   D[token, head] = sum_d k8[token, d] * q8[head, d]   (tcgen05 kind::f8f6f4,
+//   fp32 accumulator in TMEM).
+// Each of the 128 TMEM lanes then holds one token's row of head dots, so the
+// epilogue thread that owns the lane applies ReLU, the per-head weights and the
+// key scale with no cross-thread reduction, writes the fp32 logit and counts it
+// in a shared-memory histogram of the top 11 key bits (the first top-k pass).
+//
+// Warp roles (256 threads, one persistent CTA per SM):
+//   warp 0   TMA producer: one 8 KB box per page into an 8-stage ring, and the
+//            request's FP8 queries (double-buffered) when the request changes;
+//   warp 1   MMA issuer (one thread) and TMEM owner;
+//   warps 4-7 epilogue (one thread per TMEM lane / token).
+// Keys are streamed exactly once per request; every query token of the
+// request is served by the same key tile (N = 64 * n_q).
+#include "dsa_ptx.cuh"
+#include "dsa_internal.h"
+
+DSA_DEFINE_ERROR_WORD(indexer)
+
+namespace dsa {
+namespace {
+
+constexpr int kTile = 128;                      // tokens per MMA tile (M)
+constexpr int kStageBytes = kTile * kIndexDim;  // 16 KB of FP8 keys
+constexpr int kThreads = 256;
+constexpr int kEpiWarp0 = 4;
+constexpr int kMaxBatch = 1024;
+
+template <int NQ>
+struct Cfg {
+  static constexpr int kN = 64 * NQ;
+  static constexpr int kStages = NQ >= 3 ? 6 : 8;
+  static constexpr int kQBytes = kN * kIndexDim;
+  static constexpr int kTmemCols = (2 * kN <= 128) ? 128 : ((2 * kN <= 256) ? 256 : 512);
+  static constexpr int kOffStages = 0;
+  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffHist = kOffQ + 2 * kQBytes;
+  static constexpr int kOffW = kOffHist + NQ * kHistBins * 4;
+  static constexpr int kOffPrefix = kOffW + kN * 4;
+  static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 4) * 4;
+  static constexpr int kOffBar = kOffScratch + 64 * 4;
+  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffTmemSlot + 16 + 1024;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Exclusive prefix sum over the 256 threads of the block (one value each).
+__device__ __forceinline__ int block_excl_scan_256(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < 8 ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < 8) scratch[8 + lane] = w;
+  }
+  __syncthreads();
+  const int warp_off = warp ? scratch[8 + warp - 1] : 0;
+  *total = scratch[15];
+  return warp_off + x - v;
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_q, const IndexerLaunch p) {
+  using C = Cfg<NQ>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const uint32_t sbase = smem_u32(smem);
+  int* prefix = reinterpret_cast<int*>(smem + C::kOffPrefix);
+  int* scratch = reinterpret_cast<int*>(smem + C::kOffScratch);
+  uint32_t* shist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
+  float* wbuf = reinterpret_cast<float*>(smem + C::kOffW);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
+  const uint32_t bar0 = sbase + C::kOffBar;
+#define KV_FULL(s) (bar0 + 8u * (s))
+#define KV_EMPTY(s) (bar0 + 8u * (C::kStages + (s)))
+#define Q_FULL(b) (bar0 + 8u * (2 * C::kStages + (b)))
+#define Q_EMPTY(b) (bar0 + 8u * (2 * C::kStages + 2 + (b)))
+#define ACC_FULL(b) (bar0 + 8u * (2 * C::kStages + 4 + (b)))
+#define ACC_EMPTY(b) (bar0 + 8u * (2 * C::kStages + 6 + (b)))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = p.batch;
+
+  // Tiles per request (requests whose every query selects all tokens are
+  // skipped when asked), then their prefix sums.
+  {
+    int cnt[4], sum = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = threadIdx.x * 4 + e;
+      int c = 0;
+      if (r < B) {
+        const int S = p.seqlens[r];
+        if (S > 0 && !(p.skip_short && S <= p.topk)) c = (S + kTile - 1) / kTile;
+      }
+      cnt[e] = c;
+      sum += c;
+    }
+    int total;
+    int run = block_excl_scan_256(sum, scratch, &total);
+    if (threadIdx.x == 0) prefix[0] = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = threadIdx.x * 4 + e;
+      run += cnt[e];
+      if (r < B) prefix[r + 1] = run;
+    }
+  }
+  for (int i = threadIdx.x; i < NQ * kHistBins; i += kThreads) shist[i] = 0u;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(KV_FULL(s), 1);
+      mbar_init(KV_EMPTY(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(Q_FULL(b), 1);
+      mbar_init(Q_EMPTY(b), 1);
+      mbar_init(ACC_FULL(b), 1);
+      mbar_init(ACC_EMPTY(b), 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = prefix[B];
+  const int G = gridDim.x;
+  const int g0 = static_cast<int>((static_cast<long long>(blockIdx.x) * total) / G);
+  const int g1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / G);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && g0 < g1) {
+      prefetch_tmap(&tmap_k);
+      prefetch_tmap(&tmap_q);
+      const uint64_t pol_k = policy_evict_first();
+      const uint64_t pol_q = policy_evict_last();
+      int r = 0, cur = -1, seg = -1;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int g = g0; g < g1; ++g) {
+        while (prefix[r + 1] <= g) ++r;
+        const int j = g - prefix[r];
+        if (r != cur) {
+          cur = r;
+          ++seg;
+          const int qb = seg & 1;
+          if (seg >= 2 && !mbar_wait(Q_EMPTY(qb), ((seg >> 1) - 1) & 1)) { ok = false; break; }
+          mbar_expect_tx(Q_FULL(qb), C::kQBytes);
+          tma_load_2d(sbase + C::kOffQ + qb * C::kQBytes, &tmap_q, 0, r * C::kN, Q_FULL(qb), pol_q);
+        }
+        const uint32_t st = it % C::kStages;
+        if (it >= C::kStages && !mbar_wait(KV_EMPTY(st), ((it / C::kStages) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int S = p.seqlens[r];
+        const int npg = (S + kPage - 1) / kPage;
+        const int* row = p.page_table + static_cast<long long>(r) * p.max_pages;
+        const int pg0 = row[2 * j];
+        const int pg1 = (2 * j + 1 < npg) ? row[2 * j + 1] : pg0;
+        // An out-of-range page id reads past the cache end (TMA fills zeros);
+        // the epilogue reports it and masks the tokens.
+        const int y0 = (pg0 >= 0 && pg0 < p.num_pages) ? pg0 * kPage : p.num_pages * kPage;
+        const int y1 = (pg1 >= 0 && pg1 < p.num_pages) ? pg1 * kPage : p.num_pages * kPage;
+        const uint32_t dst = sbase + C::kOffStages + st * kStageBytes;
+        mbar_expect_tx(KV_FULL(st), kStageBytes);
+        tma_load_2d(dst, &tmap_k, 0, y0, KV_FULL(st), pol_k);
+        tma_load_2d(dst + kPage * kIndexDim, &tmap_k, 0, y1, KV_FULL(st), pol_k);
+        ++it;
+      }
+      if (!ok) raise_error(kErrTimeout);
+      // No copy may still be in flight when the CTA exits.
+      const uint32_t n = it < static_cast<uint32_t>(C::kStages) ? it : C::kStages;
+      for (uint32_t s = 0; s < n; ++s) {
+        const uint32_t u = it - 1 - ((it - 1 - s) % C::kStages);
+        mbar_wait(KV_FULL(s), (u / C::kStages) & 1);
+      }
+      if (seg >= 0) mbar_wait(Q_FULL(seg & 1), (seg >> 1) & 1);
+      if (seg >= 1) mbar_wait(Q_FULL((seg - 1) & 1), ((seg - 1) >> 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && g0 < g1) {
+      constexpr uint32_t idesc = make_idesc(0, 0, 0, 0, C::kN, 128);
+      int r = 0, cur = -1, seg = -1;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int g = g0; g < g1; ++g) {
+        while (prefix[r + 1] <= g) ++r;
+        if (r != cur) {
+          if (seg >= 0) tc_commit(Q_EMPTY(seg & 1));
+          cur = r;
+          ++seg;
+          if (!mbar_wait(Q_FULL(seg & 1), (seg >> 1) & 1)) { ok = false; break; }
+        }
+        const uint32_t st = it % C::kStages;
+        if (!mbar_wait(KV_FULL(st), (it / C::kStages) & 1)) { ok = false; break; }
+        const uint32_t ab = it & 1;
+        if (it >= 2 && !mbar_wait(ACC_EMPTY(ab), ((it >> 1) - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a0 = sbase + C::kOffStages + st * kStageBytes;
+        const uint32_t b0 = sbase + C::kOffQ + (seg & 1) * C::kQBytes;
+        const uint32_t d = tmem_base + ab * C::kN;
+#pragma unroll
+        for (int kk = 0; kk < kIndexDim / 32; ++kk) {
+          mma_f8_ss(d, smem_desc_sw128(a0 + kk * 32, 16, 1024),
+                    smem_desc_sw128(b0 + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(KV_EMPTY(st));
+        tc_commit(ACC_FULL(ab));
+        ++it;
+      }
+      if (seg >= 0) tc_commit(Q_EMPTY(seg & 1));
+      if (!ok) raise_error(kErrTimeout);
+      if (it > 0) mbar_wait(ACC_FULL((it - 1) & 1), ((it - 1) >> 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp - kEpiWarp0;       // TMEM lane quarter
+    const int row = q4 * 32 + lane;        // token within the tile
+    const int tid = threadIdx.x - kEpiWarp0 * 32;
+    const float ninf = __int_as_float(0xff800000);
+    int r = 0, cur = -1, S = 0;
+    uint32_t it = 0;
+    bool ok = true;
+    auto flush_hist = [&](int req) {
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        uint32_t* gh = p.hist + static_cast<long long>(req * NQ + i) * kHistBins;
+        for (int b = tid; b < kHistBins; b += 128) {
+          const uint32_t v = shist[i * kHistBins + b];
+          if (v) {
+            atomicAdd(gh + b, v);
+            shist[i * kHistBins + b] = 0u;
+          }
+        }
+      }
+      named_bar_sync(1, 128);
+    };
+    for (int g = g0; g < g1; ++g) {
+      while (prefix[r + 1] <= g) ++r;
+      if (r != cur) {
+        if (cur >= 0 && p.hist) flush_hist(cur);
+        named_bar_sync(1, 128);
+        cur = r;
+        S = p.seqlens[r];
+        for (int e = tid; e < C::kN; e += 128) {
+          const int t = r * NQ + e / kIndexHeads;
+          wbuf[e] = p.w[static_cast<long long>(t) * kIndexHeads + (e % kIndexHeads)] * p.q_scale[t];
+        }
+        named_bar_sync(1, 128);
+      }
+      const int s = (g - prefix[r]) * kTile + row;
+      bool tok_ok = s < S;
+      float sk = 0.f;
+      if (tok_ok) {
+        const int pg = p.page_table[static_cast<long long>(r) * p.max_pages + (s >> 6)];
+        if (pg < 0 || pg >= p.num_pages) {
+          raise_error(kErrCheck);
+          tok_ok = false;
+        } else {
+          sk = __ldg(p.k_scale + static_cast<long long>(pg) * kPage + (s & (kPage - 1)));
+        }
+      }
+      const uint32_t ab = it & 1;
+      if (!mbar_wait(ACC_FULL(ab), (it >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + ab * C::kN;
+      float outv[NQ];
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        uint32_t acc[64];
+        tmem_ld64(tl + i * 64, acc);
+        if (i == NQ - 1) {
+          tc_fence_before();
+          mbar_arrive(ACC_EMPTY(ab));
+        }
+        const float4* w4 = reinterpret_cast<const float4*>(wbuf + i * kIndexHeads);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const float4 ww = w4[jj];
+          s0 = fmaf(ww.x, fmaxf(__uint_as_float(acc[4 * jj + 0]), 0.f), s0);
+          s1 = fmaf(ww.y, fmaxf(__uint_as_float(acc[4 * jj + 1]), 0.f), s1);
+          s0 = fmaf(ww.z, fmaxf(__uint_as_float(acc[4 * jj + 2]), 0.f), s0);
+          s1 = fmaf(ww.w, fmaxf(__uint_as_float(acc[4 * jj + 3]), 0.f), s1);
+        }
+        outv[i] = (s0 + s1) * sk;
+      }
+      if (s < p.ld) {
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+          const int vis = S - (NQ - 1 - i);
+          const bool live = tok_ok && s < vis;
+          const float v = live ? outv[i] : ninf;
+          p.logits[static_cast<long long>(r * NQ + i) * p.ld + s] = v;
+          if (p.hist && live) atomicAdd(&shist[i * kHistBins + (float_key(v) >> kHistShift)], 1u);
+        }
+      }
+      ++it;
+    }
+    if (!ok) raise_error(kErrTimeout);
+    if (cur >= 0 && p.hist) flush_hist(cur);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+#undef KV_FULL
+#undef KV_EMPTY
+#undef Q_FULL
+#undef Q_EMPTY
+#undef ACC_FULL
+#undef ACC_EMPTY
+}
+
+template <int NQ>
+cudaError_t launch_nq(const IndexerLaunch& a, cudaStream_t stream) {
+  using C = Cfg<NQ>;
+  CUtensorMap tk, tq;
+  const uint64_t rows = static_cast<uint64_t>(a.num_pages) * kPage;
+  const uint64_t qrows = static_cast<uint64_t>(a.batch) * NQ * kIndexHeads;
+  if (!encode_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_fp8, kIndexDim, rows, kIndexDim,
+                      kIndexDim, kPage, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q_fp8, kIndexDim, qrows, kIndexDim,
+                      kIndexDim, C::kN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<NQ>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = device_sm_count();
+  indexer_kernel<NQ><<<grid, kThreads, C::kSmemBytes, stream>>>(tk, tq, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t stream) {
+  switch (a.nq) {
+    case 1: return launch_nq<1>(a, stream);
+    case 2: return launch_nq<2>(a, stream);
+    case 3: return launch_nq<3>(a, stream);
+    case 4: return launch_nq<4>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dsa

@@ -1,0 +1,388 @@
+// sparse_mla.cu -- stage 3, absorbed-form MLA over only the selected latent
+// rows, as split-KV online-softmax partials ("Deepseek Details", section
+// "DSA", stage 2: Mid_O[batch, head, block, dim] and
+// Mid_O_LogExpSum[batch, head, block]; the latent row is kv_lora_rank 512 +
+// rope 64 = 576 dims and V is its first 512 dims: "[SGLang] NSA", section
+// "forward_decode").
+//
+// One CTA = (query row t, split b, value half v).  The CTA attends the
+// selected positions of its split in tiles of 64 keys with all H (<= 128)
+// heads as the MMA M dimension, and owns output dims [256 v, 256 v + 256).
+//
+// Why halves: the fp32 output of 128 heads x 512 dims is 256 KB, all of a
+// SM's tensor memory, so one CTA keeps half of it (256 TMEM columns) and the
+// pair of CTAs of a (t, b) both compute S = Q K^T.
+//
+// Tensor memory (512 columns):
+//   [  0,256)  O   fp32 accumulator, this CTA's 256 value dims
+//   [256,320)  S   fp32 scores of the current 64-key tile
+//   [320,352)  P   bf16 probabilities (2 per column), the A operand of P V
+//   [352,512)  Q   q dims [0, 320) as bf16 pairs, the A operand of Q K^T
+// Shared memory: q dims [320, 576) (64 KB, 128B-swizzled) and two stages of
+// 64 gathered latent rows (9 atoms of 64 dims, 72 KB each).
+//
+// Per tile: S = Q K^T is 20 TMEM-A MMAs (dims 0..319) + 16 smem-A MMAs (dims
+// 320..575), M = 128, N = 64, K = 16 (kind::f16, bf16 in, fp32 out).  The
+// softmax warps (one thread per head = per TMEM lane) read S, apply the scale
+// in the exp2 domain, keep a running maximum that is raised lazily (the
+// accumulator is rescaled only when a tile's maximum exceeds it by 2^8), write
+// P to TMEM, and P V (4 MMAs, N = 256, V read MN-major from the same smem
+// stage) accumulates into O.
+//
+// Warp roles (256 threads): warp 0 gathers rows with TMA tile::gather4
+// (logical index -> page table -> cache row, fused here), warp 1 issues the
+// MMAs and owns TMEM, warps 4-7 run the softmax and the epilogue.
+#include "dsa_ptx.cuh"
+#include "dsa_internal.h"
+
+DSA_DEFINE_ERROR_WORD(mla)
+
+namespace dsa {
+namespace {
+
+constexpr int kBN = 64;                                  // keys per tile
+constexpr int kAtoms = kLatentDim / 64;                  // 9 atoms of 64 dims
+constexpr int kAtomBytes = kBN * 128;                    // 8 KB
+constexpr int kStageBytes = kAtoms * kAtomBytes;         // 72 KB
+constexpr int kQTmemDims = 320;
+constexpr int kQSmemAtoms = (kLatentDim - kQTmemDims) / 64;  // 4
+constexpr int kQAtomBytes = 128 * 128;                   // 128 heads x 64 dims bf16
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kOffQ + kQSmemAtoms * kQAtomBytes;
+constexpr int kOffRows = kOffStage + 2 * kStageBytes;
+constexpr int kOffMask = kOffRows + 2 * kBN * 4;
+constexpr int kOffBar = kOffMask + 2 * 8;
+constexpr int kNumBars = 10;
+constexpr int kOffSlot = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffSlot + 16 + 1024;
+constexpr int kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
+constexpr int kTmemCols = 512;
+constexpr int kThreads = 256;
+constexpr int kSoftWarp0 = 4;
+constexpr float kRescaleLog2 = 8.0f;
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                      const __grid_constant__ CUtensorMap tmap_kv, const MlaLaunch p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int split = blockIdx.x >> 1, half = blockIdx.x & 1, t = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = p.heads, S = p.num_splits, k = p.k;
+  const int r = t / p.nq, qi = t % p.nq;
+  const int vis = p.seqlens[r] - (p.nq - 1 - qi);
+  const int n = vis <= 0 ? 0 : (vis < k ? vis : k);
+  const int per = (k + S - 1) / S;
+  const int chunk = kBN * ((per + kBN - 1) / kBN);
+  const int start = split * chunk;
+  const int end = min(start + chunk, n);
+  const int ntiles = end > start ? (end - start + kBN - 1) / kBN : 0;
+  const float ninf = __int_as_float(0xff800000);
+
+  float* out_base = p.mid_o + (static_cast<long long>(t) * H * S + split) * kVDim + half * 256;
+  if (ntiles == 0) {
+    // Empty block: Mid_O = 0, Mid_LSE = -inf.
+    for (int e = threadIdx.x; e < H * 64; e += kThreads) {
+      const int h = e >> 6, c = e & 63;
+      reinterpret_cast<float4*>(out_base + static_cast<long long>(h) * S * kVDim)[c] =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (half == 0)
+      for (int h = threadIdx.x; h < H; h += kThreads)
+        p.mid_lse[(static_cast<long long>(t) * H + h) * S + split] = ninf;
+    return;
+  }
+
+  uint8_t* smem = align1024(smem_raw);
+  const uint32_t sbase = smem_u32(smem);
+  int* rows_s = reinterpret_cast<int*>(smem + kOffRows);
+  unsigned long long* mask_s = reinterpret_cast<unsigned long long*>(smem + kOffMask);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+  const uint32_t bar0 = sbase + kOffBar;
+  const uint32_t Q_FULL = bar0, Q_TMEM = bar0 + 8, S_FULL = bar0 + 16, S_FREE = bar0 + 24,
+                 P_FULL = bar0 + 32, PV_DONE = bar0 + 40;
+#define KV_FULL(s) (bar0 + 48u + 8u * (s))
+#define KV_EMPTY(s) (bar0 + 64u + 8u * (s))
+
+  if (threadIdx.x == 0) {
+    mbar_init(Q_FULL, 1);
+    mbar_init(Q_TMEM, 128);
+    mbar_init(S_FULL, 1);
+    mbar_init(S_FREE, 128);
+    mbar_init(P_FULL, 128);
+    mbar_init(PV_DONE, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(KV_FULL(s), 1);
+      mbar_init(KV_EMPTY(s), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int* ptab = p.page_table + static_cast<long long>(r) * p.max_pages;
+    const int* idx_row = p.topk_idx + static_cast<long long>(t) * k;
+    int safe_row = 0;
+    {
+      const int pg0 = ptab[0];
+      if (pg0 >= 0 && pg0 < p.num_pages) safe_row = pg0 * kPage;
+    }
+    const uint64_t pol = policy_evict_last();
+    if (lane == 0) {
+      prefetch_tmap(&tmap_q);
+      prefetch_tmap(&tmap_kv);
+      mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
+      for (int a = 0; a < kQSmemAtoms; ++a)
+        tma_load_2d(sbase + kOffQ + a * kQAtomBytes, &tmap_q, kQTmemDims + 64 * a, t * H, Q_FULL,
+                    pol);
+    }
+    int issued = 0;
+    for (int it = 0; it < ntiles; ++it) {
+      const int st = it & 1;
+      if (it >= 2) {
+        int ok = 0;
+        if (lane == 0) ok = mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) raise_error(kErrTimeout);
+          break;
+        }
+      }
+      const int base = start + it * kBN;
+      uint32_t m[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = lane + 32 * e;
+        const int pos = base + j;
+        const int idx = pos < end ? __ldg(idx_row + pos) : -1;
+        bool valid = idx >= 0 && idx < vis;
+        if (pos < end && idx >= vis) raise_error(kErrCheck);
+        int row = safe_row;
+        if (valid) {
+          const int pg = __ldg(ptab + (idx >> 6));
+          if (pg < 0 || pg >= p.num_pages) {
+            raise_error(kErrCheck);
+            valid = false;
+          } else {
+            row = pg * kPage + (idx & (kPage - 1));
+          }
+        }
+        rows_s[st * kBN + j] = row;
+        m[e] = __ballot_sync(0xffffffffu, valid);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mask_s[st] = static_cast<unsigned long long>(m[0]) |
+                     (static_cast<unsigned long long>(m[1]) << 32);
+        mbar_expect_tx(KV_FULL(st), kStageBytes);
+        const uint32_t dst = sbase + kOffStage + st * kStageBytes;
+        for (int g = 0; g < kBN / 4; ++g) {
+          const int* rr = rows_s + st * kBN + 4 * g;
+          const int r0 = rr[0], r1 = rr[1], r2 = rr[2], r3 = rr[3];
+#pragma unroll
+          for (int a = 0; a < kAtoms; ++a)
+            tma_gather4(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r0, r1, r2, r3,
+                        KV_FULL(st), pol);
+        }
+      }
+      __syncwarp();
+      ++issued;
+    }
+    if (lane == 0) {
+      // No copy may still be in flight when the CTA exits.
+      for (int u = issued - 1; u >= 0 && u >= issued - 2; --u) mbar_wait(KV_FULL(u & 1), (u >> 1) & 1);
+      mbar_wait(Q_FULL, 0);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc(1, 1, 0, 0, kBN, 128);
+      constexpr uint32_t idesc_pv = make_idesc(1, 1, 0, 1, 256, 128);
+      const uint32_t tS = tmem + kColS, tO = tmem + kColO, tP = tmem + kColP, tQ = tmem + kColQ;
+      bool ok = mbar_wait(Q_FULL, 0) && mbar_wait(Q_TMEM, 0);
+      int pv_issued = 0;
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(P_FULL, i & 1)) return false;
+        tc_fence_after();
+        const uint32_t stage = sbase + kOffStage + (i & 1) * kStageBytes + 4 * half * kAtomBytes;
+#pragma unroll
+        for (int j = 0; j < kBN / 16; ++j)
+          mma_f16_ts(tO, tP + 8 * j, smem_desc_sw128(stage + j * 2048, kAtomBytes, 1024), idesc_pv,
+                     (i > 0 || j > 0) ? 1u : 0u);
+        tc_commit(KV_EMPTY(i & 1));
+        tc_commit(PV_DONE);
+        ++pv_issued;
+        return true;
+      };
+      for (int it = 0; it < ntiles && ok; ++it) {
+        const int st = it & 1;
+        if (!mbar_wait(KV_FULL(st), (it >> 1) & 1)) { ok = false; break; }
+        if (it >= 1 && !mbar_wait(S_FREE, (it - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t stage = sbase + kOffStage + st * kStageBytes;
+#pragma unroll
+        for (int j = 0; j < kQTmemDims / 16; ++j)
+          mma_f16_ts(tS, tQ + 8 * j, smem_desc_sw128(stage + (j >> 2) * kAtomBytes + (j & 3) * 32, 16, 1024),
+                     idesc_qk, j > 0 ? 1u : 0u);
+#pragma unroll
+        for (int j = kQTmemDims / 16; j < kLatentDim / 16; ++j) {
+          const int jq = j - kQTmemDims / 16;
+          mma_f16_ss(tS,
+                     smem_desc_sw128(sbase + kOffQ + (jq >> 2) * kQAtomBytes + (jq & 3) * 32, 16, 1024),
+                     smem_desc_sw128(stage + (j >> 2) * kAtomBytes + (j & 3) * 32, 16, 1024),
+                     idesc_qk, 1u);
+        }
+        tc_commit(S_FULL);
+        if (it >= 1 && !issue_pv(it - 1)) { ok = false; break; }
+      }
+      if (ok && !issue_pv(ntiles - 1)) ok = false;
+      if (!ok) raise_error(kErrTimeout);
+      if (pv_issued > 0) mbar_wait(PV_DONE, (pv_issued - 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp >= kSoftWarp0) {
+    // ------------------------------------------------------------ softmax
+    const int q4 = warp - kSoftWarp0;
+    const int h = q4 * 32 + lane;
+    const uint32_t lanebase = static_cast<uint32_t>(q4 * 32) << 16;
+    const bool live = h < H;
+    // q dims [0, 320) -> TMEM columns [kColQ, kColQ + 160)
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<long long>(t) * H + (live ? h : 0)) * kLatentDim);
+#pragma unroll 1
+      for (int c = 0; c < kQTmemDims / 64; ++c) {
+        uint32_t rr[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = live ? __ldg(src + c * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
+          rr[4 * u + 0] = x.x;
+          rr[4 * u + 1] = x.y;
+          rr[4 * u + 2] = x.z;
+          rr[4 * u + 3] = x.w;
+        }
+        tmem_st32(tmem + lanebase + kColQ + 32 * c, rr);
+      }
+      tc_fence_before();
+      mbar_arrive(Q_TMEM);
+    }
+    const float sc = p.sm_scale * 1.4426950408889634f;  // exp -> exp2
+    float mrun = ninf, lrun = 0.f;
+    bool ok = true;
+    for (int it = 0; it < ntiles; ++it) {
+      const int st = it & 1;
+      if (!mbar_wait(S_FULL, it & 1) || !mbar_wait(KV_FULL(st), (it >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld64(tmem + lanebase + kColS, sr);
+      tc_fence_before();
+      mbar_arrive(S_FREE);
+      const unsigned long long msk = mask_s[st];
+      float x[64];
+      float tmax = ninf;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        x[j] = ((msk >> j) & 1ull) ? __uint_as_float(sr[j]) * sc : ninf;
+        tmax = fmaxf(tmax, x[j]);
+      }
+      if (it >= 1) {
+        if (!mbar_wait(PV_DONE, (it - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const bool raise = tmax > mrun + kRescaleLog2;
+      const float mnew = raise ? tmax : mrun;
+      // O holds a partial sum under the old maximum: rescale it (warp-wide,
+      // since TMEM loads and stores are warp-collective).
+      const bool need = raise && mrun > ninf;
+      if (__any_sync(0xffffffffu, need)) {
+        const float f = need ? exp2f(mrun - mnew) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lanebase + kColO + 32 * c, o);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * f);
+          tmem_st32(tmem + lanebase + kColO + 32 * c, o);
+        }
+        lrun *= f;
+      }
+      mrun = mnew;
+      uint32_t pk[32];
+      float ls = 0.f;
+      const bool any = mrun > ninf;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const float p0 = any ? exp2f(x[2 * jj] - mrun) : 0.f;
+        const float p1 = any ? exp2f(x[2 * jj + 1] - mrun) : 0.f;
+        pk[jj] = pack_bf16x2(p0, p1);
+        ls += bf16lo_to_f32(pk[jj]) + bf16hi_to_f32(pk[jj]);
+      }
+      lrun += ls;
+      tmem_st32(tmem + lanebase + kColP, pk);
+      tc_fence_before();
+      mbar_arrive(P_FULL);
+    }
+    if (!ok) raise_error(kErrTimeout);
+    if (ok) ok = mbar_wait(PV_DONE, (ntiles - 1) & 1);
+    tc_fence_after();
+    // epilogue: O / l -> Mid_O, log-sum-exp -> Mid_LSE
+    const float inv = (ok && lrun > 0.f) ? 1.f / lrun : 0.f;
+    float* dst = out_base + static_cast<long long>(live ? h : 0) * S * kVDim;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tmem + lanebase + kColO + 32 * c, o);
+      if (live) {
+        float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          d4[u] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                              __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+      }
+    }
+    if (live && half == 0)
+      p.mid_lse[(static_cast<long long>(t) * H + h) * S + split] =
+          (ok && lrun > 0.f) ? (mrun + log2f(lrun)) * 0.6931471805599453f : ninf;
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+#undef KV_FULL
+#undef KV_EMPTY
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
+  CUtensorMap tq, tkv;
+  const uint64_t qrows = static_cast<uint64_t>(a.batch) * a.nq * a.heads;
+  const uint64_t rows = static_cast<uint64_t>(a.num_pages) * kPage;
+  if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kLatentDim, qrows,
+                      kLatentDim * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kLatentDim, rows,
+                      kLatentDim * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(2 * a.num_splits, a.batch * a.nq);
+  sparse_mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tkv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

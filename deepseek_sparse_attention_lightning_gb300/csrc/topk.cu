@@ -1,0 +1,337 @@
+// topk.cu -- stage 2, per-query top-k without a sort.
+//
+// Each query row t keeps the n = min(k, vis[t]) visible positions with the
+// largest fp32 score; equal scores go to the lower position ("MTP and sparse
+// attention: NSA and DSA", section "Sparse attention: NSA and DSA": each query
+// keeps its 2048 highest-scoring tokens).  The selection is exact.
+//
+// Scores are compared through an order-preserving 32-bit key (-0 == +0).
+//   pass 1  histogram of the top 11 key bits per row (fused into the indexer
+//           epilogue on the fused path, else topk_hist_kernel);
+//   pass 2  topk_select_kernel, many CTAs per row: finds the bin b* where the
+//           count from the top crosses k, writes every position above b*
+//           straight to the output and appends the positions in b* to a
+//           candidate list; the last CTA of the row (ticket counter) resolves
+//           the candidates with two more radix levels over the remaining 21
+//           key bits and, for exact ties, a radix select over the position,
+//           then rewrites the row in ascending position order through a
+//           shared-memory bitmap.
+#include "dsa_ptx.cuh"
+#include "dsa_internal.h"
+
+DSA_DEFINE_ERROR_WORD(topk)
+
+namespace dsa {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kSelMax = 2048;                         // positions above b* per chunk < k
+constexpr int kOffHist = 0;                           // 2048 x u32
+constexpr int kOffSel = kOffHist + kHistBins * 4;     // 2048 x i32
+constexpr int kOffCand = kOffSel + kSelMax * 4;       // kTopkChunk x uint2
+constexpr int kSmemBytes = kOffCand + kTopkChunk * 8; // 80 KB, reused as the bitmap
+constexpr int kBitmapWords = kSmemBytes / 4;
+
+__device__ __forceinline__ int visible(const int32_t* seqlens, int t, int nq) {
+  return seqlens[t / nq] - (nq - 1 - t % nq);
+}
+
+// Exclusive scan of one value per thread over a 512-thread block.
+__device__ __forceinline__ uint32_t block_excl_scan_512(uint32_t v, uint32_t* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < 16 ? scratch[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < 16) scratch[16 + lane] = w;
+  }
+  __syncthreads();
+  const uint32_t off = warp ? scratch[16 + warp - 1] : 0u;
+  return off + x - v;
+}
+
+// Over bins h[0..2048): the bin where the running count, taken from the top
+// bin down (descending) or from bin 0 up, first reaches `need` (>= 1).
+// res[0] = that bin (-1 if none), res[1] = the count strictly before it.
+__device__ void find_crossing(const uint32_t* h, uint32_t need, bool descending, int* res,
+                              uint32_t* scratch) {
+  uint32_t c[4], local = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int b = descending ? (kHistBins - 1 - 4 * threadIdx.x - e) : (4 * threadIdx.x + e);
+    c[e] = h[b];
+    local += c[e];
+  }
+  if (threadIdx.x == 0) res[0] = -1;
+  const uint32_t excl = block_excl_scan_512(local, scratch);
+  if (excl < need && excl + local >= need) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int b = descending ? (kHistBins - 1 - 4 * threadIdx.x - e) : (4 * threadIdx.x + e);
+      if (run + c[e] >= need) {
+        res[0] = b;
+        res[1] = static_cast<int>(run);
+        break;
+      }
+      run += c[e];
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads)
+    topk_hist_kernel(const TopkLaunch p) {
+  __shared__ uint32_t sh[kHistBins];
+  const int t = blockIdx.y;
+  const int vis = visible(p.seqlens, t, p.nq);
+  const int lo = blockIdx.x * kTopkChunk;
+  if (vis <= p.k || lo >= vis) return;
+  const int hi = min(vis, lo + kTopkChunk);
+  for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
+  __syncthreads();
+  const float* row = p.logits + static_cast<long long>(t) * p.ld;
+  const int vend = lo + ((hi - lo) & ~3);
+  for (int s = lo + 4 * threadIdx.x; s < vend; s += 4 * kThreads) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(row + s));
+    atomicAdd(&sh[float_key(v.x) >> kHistShift], 1u);
+    atomicAdd(&sh[float_key(v.y) >> kHistShift], 1u);
+    atomicAdd(&sh[float_key(v.z) >> kHistShift], 1u);
+    atomicAdd(&sh[float_key(v.w) >> kHistShift], 1u);
+  }
+  for (int s = vend + threadIdx.x; s < hi; s += kThreads)
+    atomicAdd(&sh[float_key(__ldg(row + s)) >> kHistShift], 1u);
+  __syncthreads();
+  uint32_t* gh = p.hist + static_cast<long long>(t) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kThreads)
+    if (sh[i]) atomicAdd(gh + i, sh[i]);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    topk_select_kernel(const TopkLaunch p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* sh = reinterpret_cast<uint32_t*>(smem + kOffHist);
+  int* ssel = reinterpret_cast<int*>(smem + kOffSel);
+  uint2* scand = reinterpret_cast<uint2*>(smem + kOffCand);
+  __shared__ uint32_t scratch[40];
+  __shared__ int res[2];
+  __shared__ int s_info[8];   // nsel, ncand, base, cbase, last, emit
+
+  const int t = blockIdx.y;
+  const int k = p.k;
+  const int vis = visible(p.seqlens, t, p.nq);
+  int32_t* out_row = p.out + static_cast<long long>(t) * k;
+
+  if (vis <= k) {
+    // Every visible token is selected (the short-context case).
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i < k; i += kThreads) out_row[i] = i < vis ? i : -1;
+    return;
+  }
+  const int nch = (vis + kTopkChunk - 1) / kTopkChunk;
+  if (static_cast<int>(blockIdx.x) >= nch) return;
+  uint32_t* counters = p.counters + static_cast<long long>(t) * kCounterWords;
+  uint2* cand_row = p.cand + static_cast<long long>(t) * p.ld;
+
+  // ---- threshold bin b*: the count of scores in bins above it is < k and
+  //      reaches k with it.
+  const uint32_t* gh = p.hist + static_cast<long long>(t) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = __ldcg(gh + i);
+  if (threadIdx.x == 0) {
+    s_info[0] = 0;
+    s_info[1] = 0;
+  }
+  __syncthreads();
+  find_crossing(sh, static_cast<uint32_t>(k), true, res, scratch);
+  const int bstar = res[0];
+  if (bstar < 0) {  // histogram inconsistent with the row
+    if (threadIdx.x == 0) raise_error(kErrCheck);
+    return;
+  }
+
+  // ---- scan this CTA's chunk of the row
+  const float* row = p.logits + static_cast<long long>(t) * p.ld;
+  const int lo = blockIdx.x * kTopkChunk;
+  const int hi = min(vis, lo + kTopkChunk);
+  const int vend = lo + ((hi - lo) & ~3);
+  const uint32_t ub = static_cast<uint32_t>(bstar);
+  auto visit = [&](int s, float x) {
+    const uint32_t key = float_key(x);
+    const uint32_t bin = key >> kHistShift;
+    if (bin > ub) {
+      const int pos = atomicAdd(&s_info[0], 1);
+      if (pos < kSelMax) ssel[pos] = s;
+    } else if (bin == ub) {
+      const int pos = atomicAdd(&s_info[1], 1);
+      scand[pos] = make_uint2(key, static_cast<uint32_t>(s));
+    }
+  };
+  for (int s = lo + 4 * threadIdx.x; s < vend; s += 4 * kThreads) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + s));
+    visit(s, v.x);
+    visit(s + 1, v.y);
+    visit(s + 2, v.z);
+    visit(s + 3, v.w);
+  }
+  for (int s = vend + threadIdx.x; s < hi; s += kThreads) visit(s, __ldcg(row + s));
+  __syncthreads();
+  const int nsel = s_info[0], ncand = s_info[1];
+  if (threadIdx.x == 0) {
+    if (nsel > kSelMax) raise_error(kErrCheck);
+    s_info[2] = nsel ? static_cast<int>(atomicAdd(counters + 0, static_cast<uint32_t>(nsel))) : 0;
+    s_info[3] = ncand ? static_cast<int>(atomicAdd(counters + 1, static_cast<uint32_t>(ncand))) : 0;
+  }
+  __syncthreads();
+  {
+    const int base = s_info[2], cbase = s_info[3];
+    const int nw = min(nsel, kSelMax);
+    for (int i = threadIdx.x; i < nw; i += kThreads)
+      if (base + i < k) out_row[base + i] = ssel[i];
+    for (int i = threadIdx.x; i < ncand; i += kThreads) cand_row[cbase + i] = scand[i];
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t ticket = atomicAdd(counters + 2, 1u);
+    s_info[4] = (ticket == static_cast<uint32_t>(nch - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_info[4]) return;
+
+  // ---- last CTA of the row: resolve the candidates of bin b*.
+  __threadfence();
+  const int nabove = static_cast<int>(__ldcg(counters + 0));
+  const int nc = static_cast<int>(__ldcg(counters + 1));
+  const uint32_t need = static_cast<uint32_t>(k - nabove);
+  const uint2* cp = cand_row;
+  if (nc <= kTopkChunk) {
+    for (int i = threadIdx.x; i < nc; i += kThreads) scand[i] = __ldcg(cand_row + i);
+    cp = scand;
+  }
+  if (threadIdx.x == 0) s_info[5] = 0;
+  __syncthreads();
+
+  uint32_t kprefix = ub << kHistShift, kmask = 0xFFFFFFFFu << kHistShift;
+  uint32_t need_l = need;
+  uint32_t cnt_eq = 0;
+  const int kshift[2] = {10, 0};
+  const int kwidth[2] = {11, 10};
+  bool ok = need >= 1;
+  for (int lvl = 0; lvl < 2 && ok; ++lvl) {
+    const int sh_ = kshift[lvl];
+    const uint32_t dm = (1u << kwidth[lvl]) - 1u;
+    for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
+    __syncthreads();
+    for (int e = threadIdx.x; e < nc; e += kThreads) {
+      const uint32_t key = cp[e].x;
+      if ((key & kmask) == kprefix) atomicAdd(&sh[(key >> sh_) & dm], 1u);
+    }
+    __syncthreads();
+    find_crossing(sh, need_l, true, res, scratch);
+    if (res[0] < 0) { ok = false; break; }
+    const uint32_t d = static_cast<uint32_t>(res[0]);
+    cnt_eq = sh[d];
+    need_l -= static_cast<uint32_t>(res[1]);
+    kprefix |= d << sh_;
+    kmask |= dm << sh_;
+    __syncthreads();
+  }
+  const uint32_t kstar = kprefix;
+  // Exact ties at the threshold key: keep the need_l lowest positions.
+  uint32_t istar = 0xFFFFFFFFu;
+  if (ok && need_l < cnt_eq) {
+    uint32_t iprefix = 0, imask = 0, need_i = need_l;
+    const int ishift[3] = {20, 10, 0};
+    const int iwidth[3] = {11, 10, 10};
+    for (int lvl = 0; lvl < 3 && ok; ++lvl) {
+      const int sh_ = ishift[lvl];
+      const uint32_t dm = (1u << iwidth[lvl]) - 1u;
+      for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
+      __syncthreads();
+      for (int e = threadIdx.x; e < nc; e += kThreads) {
+        const uint2 c = cp[e];
+        if (c.x == kstar && (c.y & imask) == iprefix) atomicAdd(&sh[(c.y >> sh_) & dm], 1u);
+      }
+      __syncthreads();
+      find_crossing(sh, need_i, false, res, scratch);
+      if (res[0] < 0) { ok = false; break; }
+      need_i -= static_cast<uint32_t>(res[1]);
+      iprefix |= static_cast<uint32_t>(res[0]) << sh_;
+      imask |= dm << sh_;
+      __syncthreads();
+    }
+    istar = iprefix;
+  }
+  if (!ok) {
+    if (threadIdx.x == 0) raise_error(kErrCheck);
+    return;
+  }
+  for (int e = threadIdx.x; e < nc; e += kThreads) {
+    const uint2 c = cp[e];
+    if (c.x > kstar || (c.x == kstar && c.y <= istar)) {
+      const int pos = atomicAdd(&s_info[5], 1);
+      if (nabove + pos < k) out_row[nabove + pos] = static_cast<int>(c.y);
+    }
+  }
+  __threadfence_block();
+  __syncthreads();
+  if (threadIdx.x == 0 && nabove + s_info[5] != k) raise_error(kErrCheck);
+
+  // ---- rewrite the row in ascending position order through a bitmap.
+  const int nwords = (vis + 31) >> 5;
+  if (nwords > kBitmapWords) return;
+  uint32_t* bm = reinterpret_cast<uint32_t*>(smem);
+  for (int i = threadIdx.x; i < nwords; i += kThreads) bm[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < k; i += kThreads) {
+    const int s = __ldcg(out_row + i);
+    if (s >= 0 && s < vis) atomicOr(&bm[s >> 5], 1u << (s & 31));
+  }
+  __syncthreads();
+  const int per = (nwords + kThreads - 1) / kThreads;
+  const int w0 = min(nwords, threadIdx.x * per), w1 = min(nwords, w0 + per);
+  uint32_t cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
+  uint32_t off = block_excl_scan_512(cnt, scratch);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = bm[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (off < static_cast<uint32_t>(k)) out_row[off] = w * 32 + b;
+      ++off;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
+  const int T = a.batch * a.nq;
+  const int chunks = static_cast<int>((a.ld + kTopkChunk - 1) / kTopkChunk);
+  dim3 grid(chunks > 0 ? chunks : 1, T);
+  if (!a.hist_ready) {
+    topk_hist_kernel<<<grid, kThreads, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  topk_select_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

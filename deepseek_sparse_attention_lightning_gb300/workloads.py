@@ -126,6 +126,16 @@ class Workload:
     def kv(self):
         return self.layers[0].kv
 
+    def to(self, device) -> "Workload":
+        """A copy with every tensor moved to ``device`` (same bytes)."""
+        mv = lambda t: t.to(device)
+        return Workload(spec=self.spec, seqlens=mv(self.seqlens), page_table=mv(self.page_table),
+                        num_pages=self.num_pages, q_fp8=mv(self.q_fp8), q_scale=mv(self.q_scale),
+                        w=mv(self.w),
+                        layers=[LayerCache(k_fp8=mv(l.k_fp8), k_scale=mv(l.k_scale), q=mv(l.q),
+                                           kv=mv(l.kv)) for l in self.layers],
+                        heavy=self.heavy)
+
     @property
     def max_pages(self) -> int:
         return int(self.page_table.shape[1])

@@ -1,0 +1,243 @@
+/*
+ * dsa.h -- C ABI of libdsa.so, the GB300 (sm_103a) decode hot path of
+ * DeepSeek Sparse Attention (DSA).
+ *
+ * The path, for each decode query token t of a batch of requests:
+ *   1. lightning indexer: I[t,s] = sum_j w[t,j] * ReLU(q^I[t,j] . k^I[s]) over
+ *      64 FP8 heads of 128 dims, for every cached token s it can see
+ *      ("MTP and sparse attention: NSA and DSA", section "Sparse attention:
+ *      NSA and DSA");
+ *   2. top-k: the k (= 2048) highest-scoring tokens (same section; "Multi-layer
+ *      Indexer" abstract);
+ *   3. sparse MLA over only those tokens against the latent cache (576 dims =
+ *      kv_lora_rank 512 + rope 64; V = the first 512 dims), as split-KV
+ *      partials Mid_O / Mid_O_LogExpSum ("Deepseek Details", section "DSA",
+ *      stage 2; "[SGLang] NSA", section "forward_decode");
+ *   4. a cross-split online-softmax merge ("Deepseek Details", section "DSA",
+ *      stage 3).
+ *
+ * Conventions for every call:
+ *   - Buffers are owned by the caller.  Pointers marked [dev] are device
+ *     pointers on the current CUDA device; the library allocates no memory and
+ *     keeps no pointer after a call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *     is the legacy default stream).  They never synchronise, except
+ *     dsa_get_device_error.
+ *   - Host-detectable errors (null or misaligned pointers, unsupported sizes,
+ *     a short workspace) are returned before anything is launched.  Errors the
+ *     kernels detect (a page id outside the cache, an index outside the visible
+ *     range, a bounded wait that ran out) are recorded in a device-side error
+ *     word and read with dsa_get_device_error; the offending access is skipped.
+ *   - Layouts are row-major and contiguous.  Query rows are ordered
+ *     request-major: row t = r * q_per_req + i is query i of request r.
+ *   - Request r holds seqlens[r] cached tokens, its q_per_req new tokens
+ *     included.  Query i of request r sees
+ *         vis[t] = seqlens[r] - (q_per_req - 1 - i)
+ *     tokens, logical positions [0, vis[t])  ("[SGLang] NSA", section
+ *     "init_forward_metadata": 3 query tokens over 10 cached tokens see 8, 9,
+ *     10).
+ *   - Both caches are paged with 64 tokens per page and share one page table:
+ *     logical position s of request r lives in cache row
+ *         page_table[r * max_pages + s / 64] * 64 + s % 64.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer or out-of-range size   */
+  DSA_ERR_UNSUPPORTED = 2,   /* a size this build does not implement           */
+  DSA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required     */
+  DSA_ERR_CUDA = 4,          /* a CUDA runtime call failed                      */
+  DSA_ERR_DEVICE_CHECK = 5,  /* a kernel found a bad page id / index (skipped)  */
+  DSA_ERR_TIMEOUT = 6        /* a kernel's bounded wait ran out                 */
+} dsa_status;
+
+#define DSA_INDEX_HEADS 64   /* lightning-indexer heads                     */
+#define DSA_INDEX_DIM 128    /* indexer head / key dim (FP8 E4M3 bytes)     */
+#define DSA_LATENT_DIM 576   /* latent row: kv_lora_rank 512 + rope 64      */
+#define DSA_V_DIM 512        /* value dims: the first 512 of the latent row */
+#define DSA_PAGE_SIZE 64     /* tokens per cache page                       */
+#define DSA_MAX_TOPK 2048
+#define DSA_MAX_BATCH 1024
+#define DSA_MAX_Q_PER_REQ 4
+
+/*
+ * One decode batch.  Sizes are host integers; seqlens and page_table are
+ * device arrays read by the kernels.
+ *   batch      B requests, 1 <= B <= DSA_MAX_BATCH.
+ *   q_per_req  n_q = 1 + MTP draft tokens, 1 <= n_q <= 4.  T = B * n_q rows.
+ *   num_heads  MLA query heads H: 16, 32, 48, ..., 128.
+ *   topk       k, 1 <= k <= 2048.
+ *   page_size  must be 64.
+ *   max_pages  columns of page_table (>= ceil(max seqlen / 64)).
+ *   num_pages  pages in each cache; rows = num_pages * 64.  Page ids outside
+ *              [0, num_pages) are reported as DSA_ERR_DEVICE_CHECK.
+ *   seqlens    [dev] int32 [B], each >= q_per_req (so every query sees itself).
+ *   page_table [dev] int32 [B, max_pages].  Entries past a request's last page
+ *              are never read.
+ */
+typedef struct dsa_decode_desc {
+  int32_t batch;
+  int32_t q_per_req;
+  int32_t num_heads;
+  int32_t topk;
+  int32_t page_size;
+  int32_t max_pages;
+  int32_t num_pages;
+  const int32_t* seqlens;
+  const int32_t* page_table;
+} dsa_decode_desc;
+
+/*
+ * Stage 1 -- lightning-indexer logits ("MTP and sparse attention: NSA and
+ * DSA", section "Sparse attention: NSA and DSA", the index score
+ * I[t,s] = sum_j w[t,j] ReLU(q^I[t,j] . k^I[s]), computed in FP8).
+ *
+ * With the FP8 values dequantised by their per-token scales,
+ *   logits[t*ld + s] = k_scale[row(s)] * sum_j (w[t,j] * q_scale[t]) *
+ *                      ReLU(sum_d q_fp8[t,j,d] * k_fp8[row(s),d])
+ * for s < vis[t] (both scales must be positive, so they factor out of the
+ * ReLU); fp32 result, FP8 x FP8 products accumulated in fp32 on tensor cores.
+ * Entries s >= vis[t] inside the last 128-token tile are written -inf; the rest
+ * of the row is not touched.
+ *   q_fp8   [dev] uint8 [T, 64, 128]  FP8 E4M3 index queries, 16-B aligned
+ *   q_scale [dev] float [T]           per query token, > 0
+ *   w       [dev] float [T, 64]       per-head weights
+ *   k_fp8   [dev] uint8 [num_pages*64, 128] FP8 E4M3 index-key cache, 16-B aligned
+ *   k_scale [dev] float [num_pages*64] per cached token, > 0
+ *   logits  [dev] float [T, ld_logits]; ld_logits >= max_pages*64, multiple of 4
+ */
+dsa_status dsa_indexer_logits(const dsa_decode_desc* desc, const uint8_t* q_fp8,
+                              const float* q_scale, const float* w,
+                              const uint8_t* k_fp8, const float* k_scale,
+                              float* logits, int64_t ld_logits, void* stream);
+
+/*
+ * Stage 2 -- per-query top-k ("Sparse attention: NSA and DSA": each query keeps
+ * the 2048 highest-scoring tokens; "[SGLang] NSA", section "Fused Top-K
+ * Transform", top-k over variable-length rows).
+ *
+ * Row t of topk_idx receives the n = min(k, vis[t]) positions s < vis[t] with
+ * the largest logits[t*ld + s]; equal scores go to the lower position, -0.0
+ * equals +0.0.  The n positions are written in ascending order at [0, n) and
+ * the rest of the row is -1.  Exact: the set equals that of a full sort.
+ * No full sort is done (radix select with shared-memory histograms).
+ *   logits   [dev] float [T, ld_logits] (only s < vis[t] is read)
+ *   topk_idx [dev] int32 [T, k]
+ *   ws       [dev] workspace of dsa_topk_workspace_bytes() bytes, 16-B aligned
+ */
+dsa_status dsa_topk(const dsa_decode_desc* desc, const float* logits, int64_t ld_logits,
+                    int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream);
+
+size_t dsa_topk_workspace_bytes(const dsa_decode_desc* desc, int64_t ld_logits);
+
+/*
+ * Stage 3 -- sparse MLA split partials ("Deepseek Details", section "DSA",
+ * stage 2: each block of the selected tokens runs an online softmax and writes
+ * Mid_O[batch, head, block, dim] and Mid_O_LogExpSum[batch, head, block];
+ * absorbed MLA as in "[SGLang] NSA", section "forward_decode").
+ *
+ * Query row t reads positions [0, n) of topk_idx row t, n = min(k, vis[t]);
+ * entries there that are < 0 or >= vis[t] are skipped.  Positions are cut into
+ * num_splits blocks of C = 64 * ceil(ceil(k / num_splits) / 64) positions;
+ * block b covers [b*C, (b+1)*C) clipped to n.  For block b and head h:
+ *   x_s   = sm_scale * q[t,h,:] . kv[row(s),:]            (576 dims)
+ *   Mid_O[t,h,b,:]  = sum_s softmax_b(x)_s * kv[row(s), 0:512]
+ *   Mid_LSE[t,h,b]  = log(sum_s exp(x_s))                  (natural log)
+ * An empty block writes Mid_O = 0 and Mid_LSE = -inf.  QK^T and PV run on
+ * tcgen05 tensor cores in bf16 with fp32 accumulation; softmax in fp32.
+ *   q        [dev] bf16 [T, H, 576] (q_nope 512 then q_rope 64), 16-B aligned
+ *   kv       [dev] bf16 [num_pages*64, 576] latent cache, 16-B aligned
+ *   topk_idx [dev] int32 [T, k] logical positions
+ *   num_splits 1 .. ceil(k/64), or 0 for dsa_num_splits_auto()
+ *   mid_o    [dev] float [T, H, num_splits, 512]
+ *   mid_lse  [dev] float [T, H, num_splits]
+ * With num_splits == 1, mid_o already is the final output.
+ */
+dsa_status dsa_sparse_mla_decode_split(const dsa_decode_desc* desc, const uint16_t* q,
+                                       const uint16_t* kv, const int32_t* topk_idx,
+                                       int32_t num_splits, float sm_scale, float* mid_o,
+                                       float* mid_lse, void* stream);
+
+/*
+ * Stage 4 -- cross-split merge ("Deepseek Details", section "DSA", stage 3:
+ * an online-softmax merge of the blocks' Mid_O and Mid_O_LogExpSum).
+ * For each of the num_rows = T*H rows, with L = max_b mid_lse[b]:
+ *   out = sum_b exp(mid_lse[b] - L) * mid_o[b] / sum_b exp(mid_lse[b] - L)
+ *   out_lse = L + log(sum_b exp(mid_lse[b] - L))
+ * Blocks with mid_lse = -inf are skipped; a row with none gives out = 0,
+ * out_lse = -inf.
+ *   mid_o [dev] float [num_rows, num_splits, 512]; mid_lse [dev] [num_rows, num_splits]
+ *   out   [dev] float [num_rows, 512]; out_lse [dev] float [num_rows] or NULL
+ */
+dsa_status dsa_merge(int32_t num_rows, int32_t num_splits, const float* mid_o,
+                     const float* mid_lse, float* out, float* out_lse, void* stream);
+
+/*
+ * The whole decode layer, stages 1-4 on one stream.
+ * If topk_in is non-NULL, stages 1-2 are skipped and the layer attends the
+ * given selection (the layer reuses another layer's top-k: "Multi-layer
+ * Indexer" abstract, and "Sparse attention: NSA and DSA", section "New demands
+ * on inference engines", reusing selections).  Otherwise the indexer and top-k
+ * run and, if topk_out is non-NULL, the selection is also written there.
+ * Requests whose every query sees <= k tokens select all of them, so their
+ * indexer scan is skipped (the short-context dense fallback of the same page).
+ *   out [dev] float [T, H, 512]
+ *   ws  [dev] workspace of dsa_workspace_bytes(desc, max_seqlen, num_splits)
+ * Other arguments as in the stage calls; max_seqlen bounds every seqlens[r].
+ */
+dsa_status dsa_decode_fused(const dsa_decode_desc* desc,
+                            const uint8_t* q_fp8, const float* q_scale, const float* w,
+                            const uint8_t* k_fp8, const float* k_scale,
+                            const uint16_t* q, const uint16_t* kv,
+                            const int32_t* topk_in, int32_t* topk_out,
+                            float sm_scale, int32_t num_splits, int32_t max_seqlen,
+                            float* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dsa_decode_fused with per-stage timing: stage_events[0..4] (cudaEvent_t
+ * handles passed as void*, any of them NULL) are recorded on `stream` before
+ * stage 1, after stage 1 (indexer), after stage 2 (top-k), after stage 3
+ * (sparse MLA) and after stage 4 (merge).  With stage_events == NULL this is
+ * dsa_decode_fused.  When topk_in is given, events 1 and 2 mark the same point.
+ */
+dsa_status dsa_decode_fused_timed(const dsa_decode_desc* desc,
+                                  const uint8_t* q_fp8, const float* q_scale, const float* w,
+                                  const uint8_t* k_fp8, const float* k_scale,
+                                  const uint16_t* q, const uint16_t* kv,
+                                  const int32_t* topk_in, int32_t* topk_out,
+                                  float sm_scale, int32_t num_splits, int32_t max_seqlen,
+                                  float* out, void* ws, size_t ws_bytes, void* stream,
+                                  void* const* stage_events);
+
+/* Workspace bytes dsa_decode_fused needs (num_splits 0 = auto). */
+size_t dsa_workspace_bytes(const dsa_decode_desc* desc, int32_t max_seqlen,
+                           int32_t num_splits);
+
+/* The split count the library picks when 0 is passed: enough CTAs to cover the
+ * GPU's SMs at one CTA per SM, at most ceil(k/64). */
+int32_t dsa_num_splits_auto(const dsa_decode_desc* desc);
+
+/* Human-readable name of a status code (static storage). */
+const char* dsa_status_str(dsa_status status);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device: DSA_OK, DSA_ERR_DEVICE_CHECK or DSA_ERR_TIMEOUT (or
+ * DSA_ERR_CUDA if the synchronisation itself failed). */
+dsa_status dsa_get_device_error(void* stream);
+
+/* Library version string. */
+const char* dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H_ */

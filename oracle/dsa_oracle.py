@@ -48,7 +48,7 @@ V_DIM = 512
 __all__ = [
     "PAGE_SIZE", "INDEX_HEADS", "INDEX_DIM", "LATENT_DIM", "V_DIM",
     "e4m3_table", "decode_e4m3", "decode_bf16", "visible_lengths",
-    "physical_rows", "indexer_logits", "indexer_logits_at", "topk",
+    "physical_rows", "indexer_logits", "indexer_logits_at", "topk", "attend",
     "selection_count", "split_bounds", "sparse_mla", "sparse_mla_split",
     "merge", "decode_layer", "pair_flops_mla", "pair_flops_indexer",
     "token_bytes_latent", "token_bytes_index", "decode_bytes",
@@ -219,6 +219,12 @@ def _attend(qh, rows_lat, sm_scale):
     l = p.sum(axis=1, keepdims=True)
     o = (p @ rows_lat[:, :V_DIM]) / l
     return o, (m + np.log(l))[:, 0]
+
+
+def attend(q_bits_t, lat_bits, sm_scale):
+    """Attention of one query row (bf16 bits [H, 576]) over the given latent
+    rows (bf16 bits [n, 576]): the per-query step of ``sparse_mla``."""
+    return _attend(decode_bf16(q_bits_t), decode_bf16(lat_bits).reshape(-1, LATENT_DIM), sm_scale)
 
 
 def _selected_rows(idx_row, n_pos, vis_t, page_table_row):

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI (no GPU needed: no call here reaches a kernel).
+
+The library is built with nvcc (it cross-compiles sm_103a without a GPU);
+these tests check that it loads, exports every function include/dsa.h declares,
+and rejects bad arguments on the host before anything is launched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from deepseek_sparse_attention_lightning_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return api.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def _fake_desc(**over):
+    d = dict(batch=2, q_per_req=1, num_heads=128, topk=2048, page_size=64, max_pages=4,
+             num_pages=8, seqlens=0x10000, page_table=0x20000)
+    d.update(over)
+    return api.DecodeDesc(**d)
+
+
+FAKE = 0x7f0000000000      # a 256-byte aligned, never dereferenced "device" pointer
+
+
+def test_header_declares_the_hot_path_calls():
+    names = _declared_functions()
+    for n in ["dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_decode_split", "dsa_merge",
+              "dsa_decode_fused", "dsa_workspace_bytes", "dsa_get_device_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in _declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(L):
+    assert api.dsa_status_str(0) == "DSA_OK"
+    assert api.dsa_status_str(5) == "DSA_ERR_DEVICE_CHECK"
+    assert api.dsa_status_str(6) == "DSA_ERR_TIMEOUT"
+    assert "sm_103a" in api.dsa_version()
+
+
+def test_descriptor_validation(L):
+    call = lambda d: L.dsa_indexer_logits(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, None)
+    assert L.dsa_indexer_logits(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, None) == 1
+    assert call(ctypes.byref(_fake_desc(batch=0))) == 1
+    assert call(ctypes.byref(_fake_desc(seqlens=None))) == 1
+    assert call(ctypes.byref(_fake_desc(page_table=0x20002))) == 1          # misaligned
+    assert call(ctypes.byref(_fake_desc(num_heads=100))) == 2
+    assert call(ctypes.byref(_fake_desc(num_heads=256))) == 2
+    assert call(ctypes.byref(_fake_desc(page_size=32))) == 2
+    assert call(ctypes.byref(_fake_desc(topk=4096))) == 2
+    assert call(ctypes.byref(_fake_desc(q_per_req=5))) == 2
+    assert call(ctypes.byref(_fake_desc(batch=2000))) == 2
+    # logits leading dimension shorter than the page table covers
+    assert L.dsa_indexer_logits(ctypes.byref(_fake_desc()), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                128, None) == 1
+    assert L.dsa_indexer_logits(ctypes.byref(_fake_desc()), FAKE + 1, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                256, None) == 1
+
+
+def test_workspace_checks(L):
+    d = ctypes.byref(_fake_desc())
+    assert L.dsa_topk(d, FAKE, 256, FAKE, FAKE, 16, None) == 3
+    assert L.dsa_topk(d, FAKE, 256, FAKE, None, 1 << 30, None) == 3
+    need = L.dsa_topk_workspace_bytes(d, 256)
+    assert need > 0
+    n1 = L.dsa_workspace_bytes(d, 256, 1)
+    n2 = L.dsa_workspace_bytes(d, 256, 4)
+    assert 0 < n1 < n2
+    assert L.dsa_workspace_bytes(d, 0, 1) == 0
+    assert L.dsa_decode_fused(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 0.07, 1, 256,
+                              FAKE, FAKE, n1 - 1, None) == 3
+    # max_seqlen beyond what the page table can hold
+    assert L.dsa_decode_fused(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 0.07, 1, 257,
+                              FAKE, FAKE, n1, None) == 1
+    # bad scale / split count
+    assert L.dsa_decode_fused(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, -1.0, 1, 256,
+                              FAKE, FAKE, n1, None) == 1
+    assert L.dsa_sparse_mla_decode_split(d, FAKE, FAKE, FAKE, 33, 0.07, FAKE, FAKE, None) == 1
+
+
+def test_merge_validation(L):
+    assert L.dsa_merge(-1, 2, FAKE, FAKE, FAKE, None, None) == 1
+    assert L.dsa_merge(4, 0, FAKE, FAKE, FAKE, None, None) == 1
+    assert L.dsa_merge(4, 33, FAKE, FAKE, FAKE, None, None) == 2
+    assert L.dsa_merge(4, 2, FAKE + 4, FAKE, FAKE, None, None) == 1
+    assert L.dsa_merge(0, 2, FAKE, FAKE, FAKE, None, None) == 0
+
+
+def test_package_import_does_not_load_and_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import importlib
+    import deepseek_sparse_attention_lightning_gb300 as pkg
+    importlib.reload(pkg)
+    monkeypatch.setattr(api, "_lib", None)
+    monkeypatch.setattr(api, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        api.lib()

@@ -1,0 +1,375 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerances (from the stated targets):
+  * indexer scores: |gpu - oracle| <= 1e-3 * E, E = sum of |terms| of the score;
+  * top-k: bit-exact as a set (and, by the ABI, as a sorted list) when both
+    sides select from the same fp32 score tensor;
+  * attention (Mid_O, Mid_LSE, merged output): |gpu - oracle| <= 2e-2 + 1e-2 |oracle|
+    given identical indices.
+Small cases span several tiles and a ragged tail; the workload-sized cases at
+the bottom check sampled outputs in the launch configuration the benchmark
+times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from deepseek_sparse_attention_lightning_gb300 import api
+from deepseek_sparse_attention_lightning_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+IDX_REL = 1e-3
+ATT_ATOL, ATT_RTOL = 2e-2, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from deepseek_sparse_attention_lightning_gb300 import build
+    build.build()
+    api.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+def _assert_no_device_error():
+    code = api.dsa_get_device_error()
+    assert code == 0, api.STATUS_NAMES.get(code, code)
+
+
+def _gpu_wl(base, seqlens=None, **kw):
+    wl = W.make_workload(W.small_spec(base, **kw), seqlens=seqlens)
+    return wl, wl.to("cuda")
+
+
+def _assert_close_att(got, want, what):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    both_inf = np.isneginf(got) & np.isneginf(want)
+    g, w = np.where(both_inf, 0.0, got), np.where(both_inf, 0.0, want)
+    bad = ~(np.abs(g - w) <= ATT_ATOL + ATT_RTOL * np.abs(w))
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside tolerance; " \
+                          f"max err {np.nanmax(np.abs(g - w))}"
+
+
+# ---------------------------------------------------------------- indexer
+
+INDEXER_CASES = [
+    dict(base="long_varlen", batch=3, q_per_req=1, seqlens=[130, 700, 257], paged=True, seed=21),
+    dict(base="mtp_32k", batch=2, q_per_req=2, seqlens=[300, 901], paged=True, seed=22),
+    dict(base="mtp_32k", batch=2, q_per_req=3, seqlens=[200, 450], paged=True, seed=23),
+    dict(base="mtp_32k", batch=2, q_per_req=4, seqlens=[129, 384], paged=True, seed=24),
+    dict(base="tiny_4k", batch=1, q_per_req=1, seqlens=[4096], paged=False, seed=0),
+    dict(base="long_varlen", batch=5, q_per_req=1, seqlens=[1, 64, 65, 127, 1000], paged=True, seed=25),
+]
+
+
+@pytest.mark.parametrize("case", INDEXER_CASES, ids=lambda c: f"{c['base']}-nq{c['q_per_req']}")
+def test_indexer_matches_oracle(case):
+    case = dict(case)
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    wl, g = _gpu_wl(base, seqlens=seqlens, heavy="none", **case)
+    logits = api.run_indexer(g).cpu().numpy()
+    _assert_no_device_error()
+    a = W.host_arrays(wl)
+    I, E = O.indexer_logits(a["q_fp8"], a["q_scale"], a["w"], a["k_fp8"], a["k_scale"],
+                            a["page_table"], a["seqlens"], a["q_per_req"])
+    vis = O.visible_lengths(a["seqlens"], a["q_per_req"])
+    nq = a["q_per_req"]
+    for t, n in enumerate(vis):
+        err = np.abs(logits[t, :n].astype(np.float64) - I[t, :n])
+        assert (err <= IDX_REL * E[t, :n] + 1e-30).all(), f"row {t}: max rel {np.max(err / (E[t, :n] + 1e-30))}"
+        S = int(a["seqlens"][t // nq])
+        tail_end = min(((S + 127) // 128) * 128, logits.shape[1])
+        assert np.isneginf(logits[t, n:tail_end]).all()
+
+
+def test_indexer_head_permutation_invariance_on_gpu():
+    wl, g = _gpu_wl("mtp_32k", batch=2, q_per_req=2, seqlens=[500, 700], heavy="none", seed=31)
+    l1 = api.run_indexer(g)
+    perm = torch.randperm(64, generator=torch.Generator().manual_seed(0)).cuda()
+    g.q_fp8 = g.q_fp8[:, perm].contiguous()
+    g.w = g.w[:, perm].contiguous()
+    l2 = api.run_indexer(g)
+    vis = O.visible_lengths(wl.seqlens.numpy(), 2)
+    for t, n in enumerate(vis):
+        a, b = l1[t, :n].cpu().numpy(), l2[t, :n].cpu().numpy()
+        assert np.allclose(a, b, rtol=1e-5, atol=1e-4 * np.abs(a).max())
+
+
+# ---------------------------------------------------------------- top-k
+
+def _topk_desc(vis_rows, ld, k, nq=1):
+    """A descriptor whose rows see exactly ``vis_rows`` tokens (nq = 1)."""
+    B = len(vis_rows)
+    seqlens = torch.tensor(vis_rows, dtype=torch.int32, device="cuda")
+    max_pages = ld // 64
+    table = torch.zeros((B, max_pages), dtype=torch.int32, device="cuda")
+    desc = api.make_desc(seqlens, table, nq, 128, k, max_pages)
+    return desc, (seqlens, table)
+
+
+def _gpu_topk(scores_np, vis_rows, k):
+    T, ld = scores_np.shape
+    desc, keep = _topk_desc(vis_rows, ld, k)
+    logits = torch.from_numpy(np.ascontiguousarray(scores_np, dtype=np.float32)).cuda()
+    ws = torch.empty(api.dsa_topk_workspace_bytes(desc, ld), dtype=torch.uint8, device="cuda")
+    out = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    api.dsa_topk(desc, logits, out, ws, ld)
+    res = out.cpu().numpy()
+    _assert_no_device_error()
+    return res
+
+
+TOPK_CASES = {
+    # name: (rows, ld, k, generator)
+    "gauss_k2048": (4, 20480, 2048, lambda r, n: r.standard_normal(n)),
+    "ties_k64": (3, 3072, 64, lambda r, n: np.round(r.standard_normal(n) * 4) / 4),
+    "ties_k2048": (3, 9216, 2048, lambda r, n: np.round(r.standard_normal(n) * 2) / 2),
+    "all_equal": (2, 8192, 100, lambda r, n: np.zeros(n)),
+    "signed_zero": (2, 4096, 300, lambda r, n: np.where(r.random(n) < 0.5, -0.0, 0.0)),
+    "heavy_tail": (2, 65536, 2048, lambda r, n: r.standard_normal(n) ** 3),
+    "k1": (2, 4096, 1, lambda r, n: r.standard_normal(n)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TOPK_CASES))
+def test_topk_bit_exact(name):
+    rows, ld, k, gen = TOPK_CASES[name]
+    rng = np.random.default_rng(abs(hash(name)) % 2 ** 31)
+    scores = np.stack([gen(rng, ld) for _ in range(rows)]).astype(np.float32)
+    vis = [ld - 7 * i for i in range(rows)]
+    got = _gpu_topk(scores, vis, k)
+    want = O.topk(scores, np.array(vis), k)
+    assert np.array_equal(got, want)
+
+
+def test_topk_short_rows_select_everything():
+    rng = np.random.default_rng(1)
+    scores = rng.standard_normal((4, 4096)).astype(np.float32)
+    vis = [1, 2047, 2048, 2049]
+    got = _gpu_topk(scores, vis, 2048)
+    want = O.topk(scores, np.array(vis), 2048)
+    assert np.array_equal(got, want)
+    assert got[0, 0] == 0 and (got[0, 1:] == -1).all()
+
+
+def test_topk_long_rows():
+    rng = np.random.default_rng(2)
+    ld = 196608
+    scores = rng.standard_normal((3, ld)).astype(np.float32)
+    vis = [ld, 131072, 100000]
+    got = _gpu_topk(scores, vis, 2048)
+    assert np.array_equal(got, O.topk(scores, np.array(vis), 2048))
+
+
+# ---------------------------------------------------------------- sparse MLA
+
+def _oracle_indices(wl, k=None):
+    a = W.host_arrays(wl)
+    I, _ = O.indexer_logits(a["q_fp8"], a["q_scale"], a["w"], a["k_fp8"], a["k_scale"],
+                            a["page_table"], a["seqlens"], a["q_per_req"], with_bound=False)
+    vis = O.visible_lengths(a["seqlens"], a["q_per_req"])
+    return a, O.topk(I.astype(np.float32), vis, a["topk"] if k is None else k)
+
+
+MLA_CASES = [
+    dict(base="mtp_32k", batch=2, q_per_req=2, num_heads=128, topk=2048, seqlens=[2600, 3100], seed=41),
+    dict(base="tiny_4k", batch=1, q_per_req=1, num_heads=16, topk=2048, seqlens=[4096], seed=0),
+    dict(base="short_dense", batch=3, q_per_req=1, num_heads=128, topk=2048, seqlens=[700, 1500, 63], seed=42),
+    dict(base="long_varlen", batch=2, q_per_req=1, num_heads=64, topk=256, seqlens=[1000, 333], seed=43),
+    dict(base="mtp_32k", batch=1, q_per_req=2, num_heads=48, topk=200, seqlens=[2], seed=44),
+]
+
+
+@pytest.mark.parametrize("splits", [1, 3, 0])
+@pytest.mark.parametrize("case", MLA_CASES, ids=lambda c: f"{c['base']}-H{c['num_heads']}-k{c['topk']}")
+def test_sparse_mla_split_and_merge_match_oracle(case, splits):
+    case = dict(case)
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    wl, g = _gpu_wl(base, seqlens=seqlens, heavy="none", **case)
+    a, idx = _oracle_indices(wl)
+    idx_gpu = torch.from_numpy(idx.astype(np.int32)).cuda()
+    mid_o, mid_lse = api.run_sparse_mla_split(g, idx_gpu, num_splits=splits)
+    S = mid_o.shape[2]
+    out, lse = api.run_merge(mid_o, mid_lse)
+    _assert_no_device_error()
+    mo, ml = O.sparse_mla_split(a["q"], a["kv"], idx, a["page_table"], a["seqlens"],
+                                a["q_per_req"], a["sm_scale"], S)
+    _assert_close_att(mid_o.cpu().numpy(), mo, "Mid_O")
+    _assert_close_att(mid_lse.cpu().numpy(), ml, "Mid_LSE")
+    o, l = O.sparse_mla(a["q"], a["kv"], idx, a["page_table"], a["seqlens"], a["q_per_req"],
+                        a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "O")
+    _assert_close_att(lse.cpu().numpy(), l, "LSE")
+
+
+def test_sparse_mla_skips_padding_and_many_empty_splits():
+    wl, g = _gpu_wl("long_varlen", batch=2, q_per_req=1, num_heads=128, topk=2048,
+                    seqlens=[100, 70], heavy="none", seed=45)
+    a = W.host_arrays(wl)
+    idx = np.full((2, 2048), -1, dtype=np.int64)
+    idx[0, :100] = np.random.default_rng(0).permutation(100)
+    idx[1, :70] = np.arange(70)
+    idx[1, 10] = -1                                     # a hole inside the valid prefix
+    mid_o, mid_lse = api.run_sparse_mla_split(g, torch.from_numpy(idx.astype(np.int32)).cuda(), 32)
+    out, lse = api.run_merge(mid_o, mid_lse)
+    _assert_no_device_error()
+    assert torch.isneginf(mid_lse[:, :, 2:]).all()      # splits past the selection are empty
+    o, l = O.sparse_mla(a["q"], a["kv"], idx, a["page_table"], a["seqlens"], 1, a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "O")
+    _assert_close_att(lse.cpu().numpy(), l, "LSE")
+
+
+# ---------------------------------------------------------------- fused layer
+
+FUSED_CASES = [
+    dict(base="mtp_32k", batch=3, q_per_req=2, num_heads=128, topk=2048, seqlens=[5000, 2100, 9000],
+         heavy="frac:0.01", seed=51),
+    dict(base="long_varlen", batch=2, q_per_req=1, num_heads=128, topk=2048, seqlens=[20000, 12345],
+         heavy="runs:0.005:8", seed=52),
+    dict(base="short_dense", batch=4, q_per_req=1, num_heads=128, topk=2048, seqlens=[512, 2048, 1999, 3000],
+         heavy="none", seed=53),
+    dict(base="tiny_4k", batch=1, q_per_req=1, num_heads=16, topk=2048, seqlens=[4096], heavy="count:64", seed=0),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: c["base"])
+def test_fused_decode_layer(case):
+    case = dict(case)
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    wl, g = _gpu_wl(base, seqlens=seqlens, **case)
+    T, k = wl.spec.num_tokens, wl.spec.topk
+    sel = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    out = api.run_decode(g, topk_out=sel)
+    logits = api.run_indexer(g)
+    _assert_no_device_error()
+    a = W.host_arrays(wl)
+    vis = O.visible_lengths(a["seqlens"], a["q_per_req"])
+    sel_np = sel.cpu().numpy()
+    # (1) the fused selection is exactly the top-k of the kernel's fp32 scores
+    lg = logits.cpu().numpy()
+    assert np.array_equal(sel_np, O.topk(lg, vis, k))
+    # (2) every selected token is a true top-k token up to the score tolerance
+    I, E = O.indexer_logits(a["q_fp8"], a["q_scale"], a["w"], a["k_fp8"], a["k_scale"],
+                            a["page_table"], a["seqlens"], a["q_per_req"])
+    for t, n in enumerate(vis):
+        if n <= k:
+            continue
+        kth = np.sort(I[t, :n])[::-1][k - 1]
+        chosen = sel_np[t][sel_np[t] >= 0]
+        assert (I[t, chosen] >= kth - 2 * IDX_REL * E[t, chosen]).all()
+    # (3) the output is the attention over the selected tokens
+    o, _ = O.sparse_mla(a["q"], a["kv"], sel_np, a["page_table"], a["seqlens"], a["q_per_req"],
+                        a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "O")
+
+
+def test_fused_reuses_given_selection_on_second_stream():
+    # Multi-layer-indexer schedule: layer 2 attends layer 1's selection while
+    # layer 2's own indexer + top-k run on another stream.
+    wl, g = _gpu_wl("mli_195k", batch=2, q_per_req=1, num_heads=128, topk=2048,
+                    seqlens=[6000, 9000], seed=61)
+    T, k = wl.spec.num_tokens, wl.spec.topk
+    sel1 = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    sel2 = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    out1 = api.run_decode(g, layer=0, topk_out=sel1)
+    side = torch.cuda.Stream()
+    ws2 = api.alloc_workspace(g)
+    ev = torch.cuda.Event()
+    ev.record()
+    side.wait_event(ev)
+    out2 = api.run_decode(g, layer=1, topk_in=sel1)           # attention of layer 2 (main)
+    with torch.cuda.stream(side):
+        logits2 = api.run_indexer(g, layer=1, stream=side)     # indexer of layer 2 (side)
+        api.dsa_topk(api.workload_desc(g), logits2, sel2,
+                     torch.empty(api.dsa_topk_workspace_bytes(api.workload_desc(g), logits2.shape[1]),
+                                 dtype=torch.uint8, device="cuda"), stream=side)
+    torch.cuda.synchronize()
+    _assert_no_device_error()
+    a2 = W.host_arrays(wl, layer=1)
+    s1 = sel1.cpu().numpy()
+    o2, _ = O.sparse_mla(a2["q"], a2["kv"], s1, a2["page_table"], a2["seqlens"], 1, a2["sm_scale"])
+    _assert_close_att(out2.cpu().numpy(), o2, "layer-2 output on layer-1 selection")
+    vis = O.visible_lengths(a2["seqlens"], 1)
+    assert np.array_equal(sel2.cpu().numpy(), O.topk(logits2.cpu().numpy(), vis, k))
+    # adjacent layers select overlapping sets (the premise of the schedule)
+    s2 = sel2.cpu().numpy()
+    overlap = np.mean([len(np.intersect1d(s1[t], s2[t])) / k for t in range(T)])
+    assert overlap > 0.2
+
+
+# ---------------------------------------------------------------- errors
+
+def test_device_check_flags_bad_page_id():
+    wl, g = _gpu_wl("long_varlen", batch=2, q_per_req=1, num_heads=128, topk=2048,
+                    seqlens=[3000, 700], heavy="none", seed=71)
+    g.page_table[0, 3] = wl.num_pages + 5               # outside the cache
+    logits = api.run_indexer(g)
+    assert api.dsa_get_device_error() == 5               # DSA_ERR_DEVICE_CHECK
+    assert api.dsa_get_device_error() == 0               # read-and-clear
+    row = logits[0].cpu().numpy()
+    assert np.isneginf(row[3 * 64:4 * 64]).all()         # the bad page's tokens are masked
+    assert np.isfinite(row[:3 * 64]).all()
+
+
+def test_host_errors_are_returned_before_launch():
+    wl, g = _gpu_wl("long_varlen", batch=1, q_per_req=1, num_heads=128, topk=2048,
+                    seqlens=[300], heavy="none", seed=72)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(api.DSAError) as e:
+        api.run_decode(g, ws=ws)
+    assert e.value.status == 3                           # DSA_ERR_WORKSPACE
+    d = api.workload_desc(g)
+    d.num_heads = 100
+    with pytest.raises(api.DSAError) as e:
+        api.dsa_sparse_mla_decode_split(d, g.q, g.kv, torch.zeros((1, 2048), dtype=torch.int32, device="cuda"),
+                                        1, 0.1, torch.empty((1, 100, 1, 512), device="cuda"),
+                                        torch.empty((1, 100, 1), device="cuda"))
+    assert e.value.status == 2                           # DSA_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- workload sizes
+
+def _sampled_checks(wl, g, sel, out, logits, rows_to_check, n_pos=4096):
+    """Oracle checks on sampled outputs of a workload-sized run."""
+    nq, k = wl.spec.q_per_req, wl.spec.topk
+    seqlens = wl.seqlens.cpu().numpy()
+    table = wl.page_table.cpu().numpy()
+    vis = O.visible_lengths(seqlens, nq)
+    sel_np = sel.cpu().numpy()
+    lg = logits.cpu().numpy()
+    # top-k: exact against the oracle on the kernel's scores, every row
+    assert np.array_equal(sel_np, O.topk(lg, vis, k))
+    rng = np.random.default_rng(0)
+    for t in rows_to_check:
+        r, n = t // nq, int(vis[t])
+        pos = np.unique(np.concatenate([rng.integers(0, n, size=min(n_pos, n)),
+                                        sel_np[t][sel_np[t] >= 0]]))
+        rows = torch.from_numpy(O.physical_rows(table[r], pos)).cuda()
+        k8 = wl.k_fp8[rows].cpu().numpy()
+        ks = wl.k_scale[rows].cpu().numpy()
+        I, E = O.indexer_logits_at(wl.q_fp8[t].cpu().numpy(), float(wl.q_scale[t]),
+                                   wl.w[t].cpu().numpy(), k8, ks, np.arange(len(pos)))
+        assert (np.abs(lg[t, pos] - I) <= IDX_REL * E).all()
+        chosen = sel_np[t][sel_np[t] >= 0]
+        lat = wl.kv[torch.from_numpy(O.physical_rows(table[r], chosen)).cuda()]
+        o, _ = O.attend(W.bf16_bits(wl.q[t]), W.bf16_bits(lat), wl.spec.sm_scale)
+        _assert_close_att(out[t].cpu().numpy(), o, f"row {t}")
+
+
+@pytest.mark.parametrize("name", ["long_128k", "mtp_32k", "short_dense", "tiny_4k"])
+def test_workload_sized_sampled(name):
+    wl = W.make_workload(name, device="cuda")
+    T, k = wl.spec.num_tokens, wl.spec.topk
+    sel = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    out = api.run_decode(wl, topk_out=sel)
+    logits = api.run_indexer(wl)
+    _assert_no_device_error()
+    check = sorted({0, T // 2, T - 1})
+    _sampled_checks(wl, wl, sel, out, logits, check)
+    del wl
+    torch.cuda.empty_cache()
