@@ -104,7 +104,7 @@ TopkWs topk_ws_layout(int T, int64_t ld) {
 
 struct FusedWs {
   int64_t ld;
-  size_t logits, hist, counters, cand, topk, mid_o, mid_lse, total;
+  size_t logits, hist, counters, cand, topk, rows, mid_o, mid_lse, total;
 };
 
 FusedWs fused_ws_layout(const dsa_decode_desc* d, int32_t max_seqlen, int splits) {
@@ -116,7 +116,8 @@ FusedWs fused_ws_layout(const dsa_decode_desc* d, int32_t max_seqlen, int splits
   w.counters = w.hist + size_t(T) * kHistBins * 4;
   w.cand = align256(w.counters + size_t(T) * kCounterWords * 4);
   w.topk = align256(w.cand + size_t(T) * size_t(w.ld) * 8);
-  w.mid_o = align256(w.topk + size_t(T) * size_t(d->topk) * 4);
+  w.rows = align256(w.topk + size_t(T) * size_t(d->topk) * 4);
+  w.mid_o = align256(w.rows + size_t(T) * size_t(d->topk) * 4);
   const size_t mo = splits > 1 ? size_t(T) * d->num_heads * splits * dsa::kVDim * 4 : 0;
   w.mid_lse = align256(w.mid_o + mo);
   w.total = align256(w.mid_lse + size_t(T) * d->num_heads * splits * 4);
@@ -144,12 +145,16 @@ const char* dsa_version(void) { return "dsa-gb300 0.1 (sm_103a)"; }
 
 int32_t dsa_num_splits_auto(const dsa_decode_desc* d) {
   if (!d || d->batch < 1 || d->q_per_req < 1 || d->topk < 1) return 1;
+  // As many CTA pairs per query row as fill the SMs, then the fewest splits
+  // that keep the same number of 64-key tiles per split (no empty splits).
   const int T = rows_of(d);
   const int sms = dsa::device_sm_count();
+  const int tiles = max_splits(d);
   int s = sms / (2 * T);
   if (s < 1) s = 1;
-  if (s > max_splits(d)) s = max_splits(d);
-  return s;
+  if (s > tiles) s = tiles;
+  const int per = (tiles + s - 1) / s;
+  return (tiles + per - 1) / per;
 }
 
 dsa_status dsa_indexer_logits(const dsa_decode_desc* d, const uint8_t* q_fp8, const float* q_scale,
@@ -159,7 +164,7 @@ dsa_status dsa_indexer_logits(const dsa_decode_desc* d, const uint8_t* q_fp8, co
   if (st != DSA_OK) return st;
   if (!q_fp8 || !q_scale || !w || !k_fp8 || !k_scale || !logits) return DSA_ERR_INVALID_ARG;
   if (!aligned(q_fp8, 16) || !aligned(k_fp8, 16) || !aligned(logits, 16) || !aligned(q_scale, 4) ||
-      !aligned(w, 4) || !aligned(k_scale, 4))
+      !aligned(w, 4) || !aligned(k_scale, 16))
     return DSA_ERR_INVALID_ARG;
   if (ld < static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE || ld % 4 != 0)
     return DSA_ERR_INVALID_ARG;
@@ -262,7 +267,7 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
     return DSA_ERR_INVALID_ARG;
   if (!topk_in && (!q_fp8 || !q_scale || !w || !k_fp8 || !k_scale || !aligned(q_fp8, 16) ||
                    !aligned(k_fp8, 16) || !aligned(q_scale, 4) || !aligned(w, 4) ||
-                   !aligned(k_scale, 4)))
+                   !aligned(k_scale, 16)))
     return DSA_ERR_INVALID_ARG;
   if ((topk_in && !aligned(topk_in, 4)) || (topk_out && !aligned(topk_out, 4)))
     return DSA_ERR_INVALID_ARG;
@@ -301,7 +306,8 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
     ta.hist = ia.hist; ta.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
     ta.cand = reinterpret_cast<uint2*>(base + lay.cand);
     ta.batch = d->batch; ta.nq = d->q_per_req; ta.k = d->topk; ta.hist_ready = 1;
-    e = dsa::launch_topk(ta, s);
+    ta.rows = reinterpret_cast<int32_t*>(base + lay.rows);
+    ta.page_table = d->page_table; ta.max_pages = d->max_pages; ta.num_pages = d->num_pages;    e = dsa::launch_topk(ta, s);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     idx = sel;
   } else if (!mark(0) || !mark(1)) {
@@ -310,6 +316,7 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
   if (!mark(2)) return DSA_ERR_CUDA;
   dsa::MlaLaunch ma{};
   ma.q = q; ma.kv = kv; ma.topk_idx = idx; ma.seqlens = d->seqlens; ma.page_table = d->page_table;
+  ma.rows = topk_in ? nullptr : reinterpret_cast<const int32_t*>(base + lay.rows);
   ma.mid_o = splits > 1 ? reinterpret_cast<float*>(base + lay.mid_o) : out;
   ma.mid_lse = reinterpret_cast<float*>(base + lay.mid_lse);
   ma.batch = d->batch; ma.nq = d->q_per_req; ma.heads = d->num_heads; ma.k = d->topk;

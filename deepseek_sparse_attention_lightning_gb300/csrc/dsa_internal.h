@@ -44,12 +44,18 @@ struct TopkLaunch {
   uint2* cand;          // [T][ld]
   int batch, nq, k;
   int hist_ready;       // 1: hist already holds the row histograms
+  // Optional fused index -> cache-row transform: rows[t][i] = the cache row
+  // of out[t][i] (-1 where out is -1).
+  int32_t* rows;        // [T][k] or nullptr
+  const int32_t* page_table;
+  int max_pages, num_pages;
 };
 
 struct MlaLaunch {
   const uint16_t* q;
   const uint16_t* kv;
   const int32_t* topk_idx;
+  const int32_t* rows;  // optional: cache rows of topk_idx (from the fused top-k)
   const int32_t* seqlens;
   const int32_t* page_table;
   float* mid_o;

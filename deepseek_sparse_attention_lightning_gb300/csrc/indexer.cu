@@ -14,13 +14,20 @@
 // key scale with no cross-thread reduction, writes the fp32 logit and counts it
 // in a shared-memory histogram of the top 11 key bits (the first top-k pass).
 //
-// Warp roles (256 threads, one persistent CTA per SM):
-//   warp 0   TMA producer: one 8 KB box per page into an 8-stage ring, and the
-//            request's FP8 queries (double-buffered) when the request changes;
-//   warp 1   MMA issuer (one thread) and TMEM owner;
-//   warps 4-7 epilogue (one thread per TMEM lane / token).
-// Keys are streamed exactly once per request; every query token of the
-// request is served by the same key tile (N = 64 * n_q).
+// Warp roles (384 threads, one persistent CTA per SM):
+//   warp 0, lane 0  TMA producer: one 8 KB box per page into an 8-stage ring,
+//            and the request's FP8 queries (double-buffered) when the request
+//            changes.  It issues nothing else, because every TMA instruction
+//            costs ~100 cycles to issue: two per 16 KB tile keep a SM's ring
+//            full at HBM speed.
+//   warps 1, 2  MMA issuers (one thread each, alternate tiles); warp 1 owns
+//            TMEM;
+//   warps 4-7, 8-11  two epilogue groups taking alternate tiles (one thread
+//            per TMEM lane / token), each with its own accumulator buffer; each
+//            thread loads its token's key scale three of its tiles ahead.
+// The page ids of the CTA's tile range are fetched once, by all threads, into
+// shared memory.  Keys are streamed exactly once per request; every query
+// token of the request is served by the same key tile (N = 64 * n_q).
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
 
@@ -31,34 +38,41 @@ namespace {
 
 constexpr int kTile = 128;                      // tokens per MMA tile (M)
 constexpr int kStageBytes = kTile * kIndexDim;  // 16 KB of FP8 keys
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
+constexpr int kEpiGroups = 2;   // warps 4-7 take even tiles, warps 8-11 odd tiles
 constexpr int kMaxBatch = 1024;
+constexpr int kPageWin = 1024;  // page ids cached in shared memory (512 tiles)
+constexpr int kScaleAhead = 3;  // epilogue scale prefetch distance (own tiles)
 
 template <int NQ>
 struct Cfg {
   static constexpr int kN = 64 * NQ;
-  static constexpr int kStages = NQ >= 3 ? 6 : 8;
+  static constexpr int kStages = NQ == 4 ? 5 : (NQ == 3 ? 6 : 8);
   static constexpr int kQBytes = kN * kIndexDim;
   static constexpr int kTmemCols = (2 * kN <= 128) ? 128 : ((2 * kN <= 256) ? 256 : 512);
   static constexpr int kOffStages = 0;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffHist = kOffQ + 2 * kQBytes;
-  static constexpr int kOffW = kOffHist + NQ * kHistBins * 4;
-  static constexpr int kOffPrefix = kOffW + kN * 4;
+  static constexpr int kOffW = kOffHist + kEpiGroups * NQ * kHistBins * 4;
+  static constexpr int kOffPages = kOffW + kEpiGroups * kN * 4;
+  static constexpr int kOffPrefix = kOffPages + kPageWin * 4;
   static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 4) * 4;
   static constexpr int kOffBar = kOffScratch + 64 * 4;
   static constexpr int kNumBars = 2 * kStages + 8;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffTmemSlot + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kOffBar % 8 == 0, "barrier alignment");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Exclusive prefix sum over the 256 threads of the block (one value each).
-__device__ __forceinline__ int block_excl_scan_256(int v, int* scratch, int* total) {
+// Exclusive prefix sum over the kThreads threads of the block (one value each).
+__device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) {
+  constexpr int kWarps = kThreads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -69,18 +83,41 @@ __device__ __forceinline__ int block_excl_scan_256(int v, int* scratch, int* tot
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < 8 ? scratch[lane] : 0;
+    int w = lane < kWarps ? scratch[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
+    for (int o = 1; o < 32; o <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    if (lane < 8) scratch[8 + lane] = w;
+    if (lane < kWarps) scratch[32 + lane] = w;
   }
   __syncthreads();
-  const int warp_off = warp ? scratch[8 + warp - 1] : 0;
-  *total = scratch[15];
+  const int warp_off = warp ? scratch[32 + warp - 1] : 0;
+  *total = scratch[32 + kWarps - 1];
   return warp_off + x - v;
+}
+
+// Request owning flattened tile g (prefix[r] <= g < prefix[r+1]).
+__device__ __forceinline__ int find_request(const int* prefix, int B, int g) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Page id of page `which` (0/1) of flattened tile g, or -1 if it lies outside
+// the cache.  The tile's second page, past the request's last page, repeats
+// the first.
+__device__ __forceinline__ int tile_page(const IndexerLaunch& p, const int* prefix, int r, int g,
+                                         int which) {
+  const int S = p.seqlens[r];
+  const int npg = (S + kPage - 1) / kPage;
+  int lp = 2 * (g - prefix[r]) + which;
+  if (lp >= npg) lp = lp - 1;
+  const int pg = p.page_table[static_cast<long long>(r) * p.max_pages + lp];
+  return (pg >= 0 && pg < p.num_pages) ? pg : -1;
 }
 
 template <int NQ>
@@ -95,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* scratch = reinterpret_cast<int*>(smem + C::kOffScratch);
   uint32_t* shist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
   float* wbuf = reinterpret_cast<float*>(smem + C::kOffW);
+  int* pages = reinterpret_cast<int*>(smem + C::kOffPages);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
   const uint32_t bar0 = sbase + C::kOffBar;
 #define KV_FULL(s) (bar0 + 8u * (s))
@@ -110,10 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Tiles per request (requests whose every query selects all tokens are
   // skipped when asked), then their prefix sums.
   {
-    int cnt[4], sum = 0;
+    int cnt[3], sum = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = threadIdx.x * 4 + e;
+    for (int e = 0; e < 3; ++e) {
+      const int r = threadIdx.x * 3 + e;
       int c = 0;
       if (r < B) {
         const int S = p.seqlens[r];
@@ -123,16 +161,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       sum += c;
     }
     int total;
-    int run = block_excl_scan_256(sum, scratch, &total);
+    int run = block_excl_scan(sum, scratch, &total);
     if (threadIdx.x == 0) prefix[0] = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = threadIdx.x * 4 + e;
+    for (int e = 0; e < 3; ++e) {
+      const int r = threadIdx.x * 3 + e;
       run += cnt[e];
       if (r < B) prefix[r + 1] = run;
     }
   }
-  for (int i = threadIdx.x; i < NQ * kHistBins; i += kThreads) shist[i] = 0u;
+  for (int i = threadIdx.x; i < kEpiGroups * NQ * kHistBins; i += kThreads) shist[i] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(KV_FULL(s), 1);
@@ -140,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(Q_FULL(b), 1);
-      mbar_init(Q_EMPTY(b), 1);
+      mbar_init(Q_EMPTY(b), 2);   // one commit per MMA issuer
       mbar_init(ACC_FULL(b), 1);
       mbar_init(ACC_EMPTY(b), 128);
     }
@@ -159,6 +197,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g0 = static_cast<int>((static_cast<long long>(blockIdx.x) * total) / G);
   const int g1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / G);
 
+  // Page ids of the first kPageWin / 2 tiles of the range, fetched by all
+  // threads at once.
+  {
+    const int n = min(2 * (g1 - g0), kPageWin);
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const int g = g0 + (i >> 1);
+      pages[i] = tile_page(p, prefix, find_request(prefix, B, g), g, i & 1);
+    }
+  }
+  __syncthreads();
+  auto page_of = [&](int r, int g, int which) -> int {
+    const int i = 2 * (g - g0) + which;
+    return i < kPageWin ? pages[i] : tile_page(p, prefix, r, g, which);
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && g0 < g1) {
@@ -169,9 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int r = 0, cur = -1, seg = -1;
       uint32_t it = 0;
       bool ok = true;
-      for (int g = g0; g < g1; ++g) {
+      for (int g = g0; g < g1; ++g, ++it) {
         while (prefix[r + 1] <= g) ++r;
-        const int j = g - prefix[r];
         if (r != cur) {
           cur = r;
           ++seg;
@@ -185,20 +237,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int S = p.seqlens[r];
-        const int npg = (S + kPage - 1) / kPage;
-        const int* row = p.page_table + static_cast<long long>(r) * p.max_pages;
-        const int pg0 = row[2 * j];
-        const int pg1 = (2 * j + 1 < npg) ? row[2 * j + 1] : pg0;
-        // An out-of-range page id reads past the cache end (TMA fills zeros);
-        // the epilogue reports it and masks the tokens.
-        const int y0 = (pg0 >= 0 && pg0 < p.num_pages) ? pg0 * kPage : p.num_pages * kPage;
-        const int y1 = (pg1 >= 0 && pg1 < p.num_pages) ? pg1 * kPage : p.num_pages * kPage;
+        // An out-of-range page id (-1 here) is reported and read past the
+        // cache end (TMA fills zeros); the epilogue masks its tokens.
+        const int pg0 = page_of(r, g, 0), pg1 = page_of(r, g, 1);
+        if (pg0 < 0 || pg1 < 0) raise_error(kErrCheck);
+        const int y0 = pg0 >= 0 ? pg0 * kPage : p.num_pages * kPage;
+        const int y1 = pg1 >= 0 ? pg1 * kPage : p.num_pages * kPage;
         const uint32_t dst = sbase + C::kOffStages + st * kStageBytes;
         mbar_expect_tx(KV_FULL(st), kStageBytes);
         tma_load_2d(dst, &tmap_k, 0, y0, KV_FULL(st), pol_k);
         tma_load_2d(dst + kPage * kIndexDim, &tmap_k, 0, y1, KV_FULL(st), pol_k);
-        ++it;
       }
       if (!ok) raise_error(kErrTimeout);
       // No copy may still be in flight when the CTA exits.
@@ -211,20 +259,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (seg >= 1) mbar_wait(Q_FULL((seg - 1) & 1), ((seg - 1) >> 1) & 1);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads: warp 1 takes the even tiles (accumulator 0),
+    // warp 2 the odd ones (accumulator 1); one thread alone could not issue
+    // a tile's MMAs and commits as fast as HBM delivers the tiles.  Both walk
+    // every tile to keep the request (query buffer) count in step.
+    const uint32_t mi = static_cast<uint32_t>(warp - 1);
     if (lane == 0 && g0 < g1) {
       constexpr uint32_t idesc = make_idesc(0, 0, 0, 0, C::kN, 128);
       int r = 0, cur = -1, seg = -1;
-      uint32_t it = 0;
-      bool ok = true;
+      bool q_ready = false, ok = true;
+      int last = -1;
       for (int g = g0; g < g1; ++g) {
         while (prefix[r + 1] <= g) ++r;
         if (r != cur) {
           if (seg >= 0) tc_commit(Q_EMPTY(seg & 1));
           cur = r;
           ++seg;
+          q_ready = false;
+        }
+        const uint32_t it = static_cast<uint32_t>(g - g0);
+        if ((it & 1) != mi) continue;
+        if (!q_ready) {
           if (!mbar_wait(Q_FULL(seg & 1), (seg >> 1) & 1)) { ok = false; break; }
+          q_ready = true;
         }
         const uint32_t st = it % C::kStages;
         if (!mbar_wait(KV_FULL(st), (it / C::kStages) & 1)) { ok = false; break; }
@@ -241,68 +300,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(KV_EMPTY(st));
         tc_commit(ACC_FULL(ab));
-        ++it;
+        last = static_cast<int>(it);
       }
       if (seg >= 0) tc_commit(Q_EMPTY(seg & 1));
       if (!ok) raise_error(kErrTimeout);
-      if (it > 0) mbar_wait(ACC_FULL((it - 1) & 1), ((it - 1) >> 1) & 1);
+      if (last >= 0) mbar_wait(ACC_FULL(last & 1), (last >> 1) & 1);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int q4 = warp - kEpiWarp0;       // TMEM lane quarter
+    // Group gi handles the tiles it = gi, gi + 2, ... (accumulator gi), with
+    // its own histogram and weight buffer, so two tiles are in flight.
+    const int gi = (warp - kEpiWarp0) / 4;
+    const int q4 = warp & 3;               // TMEM lane quarter of this warp
     const int row = q4 * 32 + lane;        // token within the tile
-    const int tid = threadIdx.x - kEpiWarp0 * 32;
+    const int tid = (warp - kEpiWarp0 - 4 * gi) * 32 + lane;
+    const uint32_t bar_id = 1 + gi;
+    uint32_t* ghist = shist + gi * NQ * kHistBins;
+    float* gw = wbuf + gi * C::kN;
     const float ninf = __int_as_float(0xff800000);
+    // Key scale of this thread's token in tile g (0 if the page is invalid).
+    int rs = 0;
+    auto scale_of = [&](int g) -> float {
+      if (g >= g1) return 0.f;
+      while (prefix[rs + 1] <= g) ++rs;
+      const int pg = page_of(rs, g, row >> 6);
+      return pg >= 0 ? __ldg(p.k_scale + static_cast<long long>(pg) * kPage + (row & (kPage - 1)))
+                     : 0.f;
+    };
+    float sk0 = scale_of(g0 + gi), sk1 = scale_of(g0 + gi + kEpiGroups),
+          sk2 = scale_of(g0 + gi + 2 * kEpiGroups);
+    static_assert(kScaleAhead == 3, "three scale registers");
     int r = 0, cur = -1, S = 0;
-    uint32_t it = 0;
     bool ok = true;
     auto flush_hist = [&](int req) {
-      named_bar_sync(1, 128);
-#pragma unroll
+      named_bar_sync(bar_id, 128);
       for (int i = 0; i < NQ; ++i) {
         uint32_t* gh = p.hist + static_cast<long long>(req * NQ + i) * kHistBins;
         for (int b = tid; b < kHistBins; b += 128) {
-          const uint32_t v = shist[i * kHistBins + b];
+          const uint32_t v = ghist[i * kHistBins + b];
           if (v) {
             atomicAdd(gh + b, v);
-            shist[i * kHistBins + b] = 0u;
+            ghist[i * kHistBins + b] = 0u;
           }
         }
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(bar_id, 128);
     };
-    for (int g = g0; g < g1; ++g) {
+    for (int g = g0 + gi; g < g1; g += kEpiGroups) {
+      const uint32_t it = static_cast<uint32_t>(g - g0);
       while (prefix[r + 1] <= g) ++r;
       if (r != cur) {
         if (cur >= 0 && p.hist) flush_hist(cur);
-        named_bar_sync(1, 128);
+        named_bar_sync(bar_id, 128);
         cur = r;
         S = p.seqlens[r];
         for (int e = tid; e < C::kN; e += 128) {
           const int t = r * NQ + e / kIndexHeads;
-          wbuf[e] = p.w[static_cast<long long>(t) * kIndexHeads + (e % kIndexHeads)] * p.q_scale[t];
+          gw[e] = p.w[static_cast<long long>(t) * kIndexHeads + (e % kIndexHeads)] * p.q_scale[t];
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(bar_id, 128);
       }
       const int s = (g - prefix[r]) * kTile + row;
-      bool tok_ok = s < S;
-      float sk = 0.f;
-      if (tok_ok) {
-        const int pg = p.page_table[static_cast<long long>(r) * p.max_pages + (s >> 6)];
-        if (pg < 0 || pg >= p.num_pages) {
-          raise_error(kErrCheck);
-          tok_ok = false;
-        } else {
-          sk = __ldg(p.k_scale + static_cast<long long>(pg) * kPage + (s & (kPage - 1)));
-        }
-      }
+      const float sk = sk0;
+      const bool tok_ok = s < S && page_of(r, g, row >> 6) >= 0;
+      sk0 = sk1;
+      sk1 = sk2;
+      sk2 = scale_of(g + kScaleAhead * kEpiGroups);
       const uint32_t ab = it & 1;
       if (!mbar_wait(ACC_FULL(ab), (it >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tl = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + ab * C::kN;
-      float outv[NQ];
-#pragma unroll
+#pragma unroll 1
       for (int i = 0; i < NQ; ++i) {
         uint32_t acc[64];
         tmem_ld64(tl + i * 64, acc);
@@ -310,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(ACC_EMPTY(ab));
         }
-        const float4* w4 = reinterpret_cast<const float4*>(wbuf + i * kIndexHeads);
+        const float4* w4 = reinterpret_cast<const float4*>(gw + i * kIndexHeads);
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
@@ -320,19 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           s0 = fmaf(ww.z, fmaxf(__uint_as_float(acc[4 * jj + 2]), 0.f), s0);
           s1 = fmaf(ww.w, fmaxf(__uint_as_float(acc[4 * jj + 3]), 0.f), s1);
         }
-        outv[i] = (s0 + s1) * sk;
-      }
-      if (s < p.ld) {
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
+        if (s < p.ld) {
           const int vis = S - (NQ - 1 - i);
           const bool live = tok_ok && s < vis;
-          const float v = live ? outv[i] : ninf;
+          const float v = live ? (s0 + s1) * sk : ninf;
           p.logits[static_cast<long long>(r * NQ + i) * p.ld + s] = v;
-          if (p.hist && live) atomicAdd(&shist[i * kHistBins + (float_key(v) >> kHistShift)], 1u);
+          if (p.hist && live) atomicAdd(&ghist[i * kHistBins + (float_key(v) >> kHistShift)], 1u);
         }
       }
-      ++it;
     }
     if (!ok) raise_error(kErrTimeout);
     if (cur >= 0 && p.hist) flush_hist(cur);

@@ -2,9 +2,10 @@
 // Details", section "DSA", stage 3: the blocks' Mid_O and Mid_O_LogExpSum are
 // combined into the final output).
 //
-// One warp per (query, head) row: the lanes hold the splits' log-sum-exps,
-// reduce their maximum L and the weights exp(lse_b - L) by shuffles, then
-// stream the splits' 512-float partial outputs with 16-byte loads.
+// One thread per 4 output values of one (query, head) row: it reads the row's
+// split log-sum-exps (a broadcast within the row's 128 threads), forms the
+// weights exp(lse_b - L) / sum, and streams its 16 bytes of every split's
+// partial output with the loads of several splits in flight.
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
 
@@ -13,46 +14,57 @@ DSA_DEFINE_ERROR_WORD(merge)
 namespace dsa {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kThreads = 256;
+constexpr int kVec = kVDim / 4;   // float4s per row
 
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kThreads)
     merge_kernel(int rows, int splits, const float* __restrict__ mid_o,
                  const float* __restrict__ mid_lse, float* __restrict__ out,
                  float* __restrict__ out_lse) {
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const long long gid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+  const int row = static_cast<int>(gid / kVec);
+  const int c4 = static_cast<int>(gid % kVec);
   if (row >= rows) return;
   const float ninf = __int_as_float(0xff800000);
-  float lse = lane < splits ? __ldg(mid_lse + static_cast<long long>(row) * splits + lane) : ninf;
-  float m = lse;
+  const float* lse = mid_lse + static_cast<long long>(row) * splits;
+  float m = ninf;
+  for (int b = 0; b < splits; ++b) m = fmaxf(m, __ldg(lse + b));
+  const float4* src = reinterpret_cast<const float4*>(mid_o) +
+                      static_cast<long long>(row) * splits * kVec + c4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float tot = 0.f;
+  if (m > ninf) {
+    // Batches of 8 splits: all loads of a batch are in flight together (an
+    // empty split holds zeros and gets weight 0).
+    for (int b0 = 0; b0 < splits; b0 += 8) {
+      float4 v[8];
+      float wv[8];
 #pragma unroll
-  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const bool empty = !(m > ninf);
-  float wgt = (!empty && lse > ninf) ? __expf(lse - m) : 0.f;
-  float tot = wgt;
+      for (int u = 0; u < 8; ++u) {
+        const int b = b0 + u;
+        if (b < splits) {
+          const float l = __ldg(lse + b);
+          wv[u] = l > ninf ? __expf(l - m) : 0.f;
+          v[u] = __ldg(src + static_cast<long long>(b) * kVec);
+        } else {
+          wv[u] = 0.f;
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
 #pragma unroll
-  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  float4 acc[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* src = reinterpret_cast<const float4*>(mid_o + static_cast<long long>(row) * splits * kVDim);
-  for (int b = 0; b < splits; ++b) {
-    const float wb = __shfl_sync(0xffffffffu, wgt, b) * inv;
-    if (wb == 0.f) continue;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 v = __ldg(src + b * (kVDim / 4) + q * 32 + lane);
-      acc[q].x = fmaf(wb, v.x, acc[q].x);
-      acc[q].y = fmaf(wb, v.y, acc[q].y);
-      acc[q].z = fmaf(wb, v.z, acc[q].z);
-      acc[q].w = fmaf(wb, v.w, acc[q].w);
+      for (int u = 0; u < 8; ++u) {
+        tot += wv[u];
+        acc.x = fmaf(wv[u], v[u].x, acc.x);
+        acc.y = fmaf(wv[u], v[u].y, acc.y);
+        acc.z = fmaf(wv[u], v[u].z, acc.z);
+        acc.w = fmaf(wv[u], v[u].w, acc.w);
+      }
     }
   }
-  float4* dst = reinterpret_cast<float4*>(out + static_cast<long long>(row) * kVDim);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) dst[q * 32 + lane] = acc[q];
-  if (out_lse && lane == 0) out_lse[row] = tot > 0.f ? m + __logf(tot) : ninf;
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  reinterpret_cast<float4*>(out)[static_cast<long long>(row) * kVec + c4] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (out_lse && c4 == 0) out_lse[row] = tot > 0.f ? m + __logf(tot) : ninf;
 }
 
 }  // namespace
@@ -60,8 +72,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 cudaError_t launch_merge(int rows, int splits, const float* mid_o, const float* mid_lse,
                          float* out, float* out_lse, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  const int grid = (rows + kWarps - 1) / kWarps;
-  merge_kernel<<<grid, kWarps * 32, 0, stream>>>(rows, splits, mid_o, mid_lse, out, out_lse);
+  const long long threads = static_cast<long long>(rows) * kVec;
+  const int grid = static_cast<int>((threads + kThreads - 1) / kThreads);
+  merge_kernel<<<grid, kThreads, 0, stream>>>(rows, splits, mid_o, mid_lse, out, out_lse);
   return cudaGetLastError();
 }
 

@@ -29,9 +29,12 @@
 // P to TMEM, and P V (4 MMAs, N = 256, V read MN-major from the same smem
 // stage) accumulates into O.
 //
-// Warp roles (256 threads): warp 0 gathers rows with TMA tile::gather4
-// (logical index -> page table -> cache row, fused here), warp 1 issues the
-// MMAs and owns TMEM, warps 4-7 run the softmax and the epilogue.
+// Warp roles (256 threads): warps 0, 2, 3 resolve every selected position to
+// its cache row (logical index -> page table -> row, fused here) and gather
+// the rows with 16-byte cp.async copies written straight into the swizzled
+// stage layout (a row-granular gather; TMA tile::gather4 was measured to be
+// issue-bound at ~100 cycles per 4 rows); warp 1 issues the MMAs and owns
+// TMEM; warps 4-7 run the softmax and the epilogue.
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
 
@@ -49,9 +52,10 @@ constexpr int kQSmemAtoms = (kLatentDim - kQTmemDims) / 64;  // 4
 constexpr int kQAtomBytes = 128 * 128;                   // 128 heads x 64 dims bf16
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kOffQ + kQSmemAtoms * kQAtomBytes;
-constexpr int kOffRows = kOffStage + 2 * kStageBytes;
-constexpr int kOffMask = kOffRows + 2 * kBN * 4;
-constexpr int kOffBar = kOffMask + 2 * 8;
+constexpr int kMaxPos = 2048;                            // positions of one split (<= k)
+constexpr int kOffRows = kOffStage + 2 * kStageBytes;    // cache row of every position
+constexpr int kOffMask = kOffRows + kMaxPos * 4;         // validity bits, 32 per word
+constexpr int kOffBar = kOffMask + (kMaxPos / 32) * 4;
 constexpr int kNumBars = 10;
 constexpr int kOffSlot = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;
@@ -59,6 +63,8 @@ constexpr int kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 256;
 constexpr int kSoftWarp0 = 4;
+constexpr int kLoaderWarps = 3;                            // warps 0, 2, 3
+constexpr int kRowChunks = kLatentDim * 2 / 16;            // 72 chunks of 16 B per row
 constexpr float kRescaleLog2 = 8.0f;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -67,8 +73,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                      const __grid_constant__ CUtensorMap tmap_kv, const MlaLaunch p) {
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const MlaLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   const int split = blockIdx.x >> 1, half = blockIdx.x & 1, t = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -100,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sbase = smem_u32(smem);
   int* rows_s = reinterpret_cast<int*>(smem + kOffRows);
-  unsigned long long* mask_s = reinterpret_cast<unsigned long long*>(smem + kOffMask);
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(smem + kOffMask);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
   const uint32_t bar0 = sbase + kOffBar;
   const uint32_t Q_FULL = bar0, Q_TMEM = bar0 + 8, S_FULL = bar0 + 16, S_FREE = bar0 + 24,
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(P_FULL, 128);
     mbar_init(PV_DONE, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(KV_FULL(s), 1);
+      mbar_init(KV_FULL(s), kLoaderWarps * 32);   // one cp.async arrive per loader thread
       mbar_init(KV_EMPTY(s), 1);
     }
     fence_mbar_init();
@@ -129,8 +134,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ loaders
+    // Three warps (96 threads) gather the selected latent rows with 16-byte
+    // cp.async copies into the 128B-swizzled stage layout; each thread's
+    // copies arrive on the stage's full barrier when they land.
+    const int lw = warp == 0 ? 0 : warp - 1;           // loader warp 0..2
+    const int ltid = lw * 32 + lane;
     const int* ptab = p.page_table + static_cast<long long>(r) * p.max_pages;
     const int* idx_row = p.topk_idx + static_cast<long long>(t) * k;
     int safe_row = 0;
@@ -138,72 +148,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pg0 = ptab[0];
       if (pg0 >= 0 && pg0 < p.num_pages) safe_row = pg0 * kPage;
     }
-    const uint64_t pol = policy_evict_last();
-    if (lane == 0) {
+    if (ltid == 0) {
       prefetch_tmap(&tmap_q);
-      prefetch_tmap(&tmap_kv);
       mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
       for (int a = 0; a < kQSmemAtoms; ++a)
         tma_load_2d(sbase + kOffQ + a * kQAtomBytes, &tmap_q, kQTmemDims + 64 * a, t * H, Q_FULL,
-                    pol);
+                    policy_evict_last());
     }
-    int issued = 0;
+    // Resolve every position of the split first (logical index -> page table
+    // -> cache row), 8 x 32 positions per batch so the loads overlap; the
+    // three warps take alternate batches.
+    const int npos = ntiles * kBN;
+    if (p.rows) {
+      // The fused top-k already translated positions to cache rows.
+      const int* rrow = p.rows + static_cast<long long>(t) * k;
+      for (int b0 = lw * 256; b0 < npos; b0 += kLoaderWarps * 256) {
+        int rv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int pos = start + b0 + 32 * u + lane;
+          rv[u] = (b0 + 32 * u < npos && pos < end) ? __ldg(rrow + pos) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = b0 + 32 * u;
+          if (i >= npos) break;
+          const bool valid = rv[u] >= 0 && rv[u] < p.num_pages * kPage;
+          rows_s[i + lane] = valid ? rv[u] : safe_row;
+          const uint32_t m = __ballot_sync(0xffffffffu, valid);
+          if (lane == 0) mask_s[i >> 5] = m;
+        }
+      }
+    }
+    for (int b0 = lw * 256; b0 < npos && !p.rows; b0 += kLoaderWarps * 256) {
+      int idx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int pos = start + b0 + 32 * u + lane;
+        idx[u] = (b0 + 32 * u < npos && pos < end) ? __ldg(idx_row + pos) : -1;
+      }
+      int pg[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) pg[u] = (idx[u] >= 0 && idx[u] < vis) ? __ldg(ptab + (idx[u] >> 6)) : -1;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = b0 + 32 * u;
+        if (i >= npos) break;
+        const int pos = start + i + lane;
+        if (pos < end && idx[u] >= vis) raise_error(kErrCheck);
+        bool valid = idx[u] >= 0 && idx[u] < vis;
+        if (valid && (pg[u] < 0 || pg[u] >= p.num_pages)) {
+          raise_error(kErrCheck);
+          valid = false;
+        }
+        rows_s[i + lane] = valid ? pg[u] * kPage + (idx[u] & (kPage - 1)) : safe_row;
+        const uint32_t m = __ballot_sync(0xffffffffu, valid);
+        if (lane == 0) mask_s[i >> 5] = m;
+      }
+    }
+    named_bar_sync(1, kLoaderWarps * 32);   // rows_s / mask_s complete
+    const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
     for (int it = 0; it < ntiles; ++it) {
       const int st = it & 1;
-      if (it >= 2) {
-        int ok = 0;
-        if (lane == 0) ok = mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          if (lane == 0) raise_error(kErrTimeout);
-          break;
-        }
+      if (it >= 2 && !mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1)) {
+        raise_error(kErrTimeout);
+        break;
       }
-      const int base = start + it * kBN;
-      uint32_t m[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = lane + 32 * e;
-        const int pos = base + j;
-        const int idx = pos < end ? __ldg(idx_row + pos) : -1;
-        bool valid = idx >= 0 && idx < vis;
-        if (pos < end && idx >= vis) raise_error(kErrCheck);
-        int row = safe_row;
-        if (valid) {
-          const int pg = __ldg(ptab + (idx >> 6));
-          if (pg < 0 || pg >= p.num_pages) {
-            raise_error(kErrCheck);
-            valid = false;
-          } else {
-            row = pg * kPage + (idx & (kPage - 1));
-          }
-        }
-        rows_s[st * kBN + j] = row;
-        m[e] = __ballot_sync(0xffffffffu, valid);
+      // 64 rows x 72 chunks of 16 B; chunk ch of row rr goes to atom ch / 8,
+      // slot (ch % 8) ^ (rr % 8) of the row's 128-byte line (128B swizzle).
+      const uint32_t dst = sbase + kOffStage + st * kStageBytes;
+      const int* rows = rows_s + it * kBN;
+      for (int c = ltid; c < kBN * kRowChunks; c += kLoaderWarps * 32) {
+        const int rr = c / kRowChunks, ch = c - rr * kRowChunks;
+        cp_async_16(dst + (ch >> 3) * kAtomBytes + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4),
+                    kvb + static_cast<long long>(rows[rr]) * (kLatentDim * 2) + ch * 16);
       }
-      __syncwarp();
-      if (lane == 0) {
-        mask_s[st] = static_cast<unsigned long long>(m[0]) |
-                     (static_cast<unsigned long long>(m[1]) << 32);
-        mbar_expect_tx(KV_FULL(st), kStageBytes);
-        const uint32_t dst = sbase + kOffStage + st * kStageBytes;
-        for (int g = 0; g < kBN / 4; ++g) {
-          const int* rr = rows_s + st * kBN + 4 * g;
-          const int r0 = rr[0], r1 = rr[1], r2 = rr[2], r3 = rr[3];
-#pragma unroll
-          for (int a = 0; a < kAtoms; ++a)
-            tma_gather4(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r0, r1, r2, r3,
-                        KV_FULL(st), pol);
-        }
-      }
-      __syncwarp();
-      ++issued;
+      cp_async_arrive_noinc(KV_FULL(st));
     }
-    if (lane == 0) {
-      // No copy may still be in flight when the CTA exits.
-      for (int u = issued - 1; u >= 0 && u >= issued - 2; --u) mbar_wait(KV_FULL(u & 1), (u >> 1) & 1);
-      mbar_wait(Q_FULL, 0);
-    }
+    // No copy may still be in flight when the CTA exits.
+    cp_async_wait_all();
+    if (ltid == 0) mbar_wait(Q_FULL, 0);
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -229,6 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < ntiles && ok; ++it) {
         const int st = it & 1;
         if (!mbar_wait(KV_FULL(st), (it >> 1) & 1)) { ok = false; break; }
+        // The tile was written by cp.async (generic proxy); make it visible to
+        // the tensor core's (async proxy) reads.
+        fence_proxy_async_smem();
         if (it >= 1 && !mbar_wait(S_FREE, (it - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t stage = sbase + kOffStage + st * kStageBytes;
@@ -262,18 +289,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + (static_cast<long long>(t) * H + (live ? h : 0)) * kLatentDim);
-#pragma unroll 1
+      // Loads of chunk c+1 are in flight while chunk c is stored.
+      uint4 cur[8], nxt[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) cur[u] = live ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
       for (int c = 0; c < kQTmemDims / 64; ++c) {
+        if (c + 1 < kQTmemDims / 64) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            nxt[u] = live ? __ldg(src + (c + 1) * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
+        }
         uint32_t rr[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint4 x = live ? __ldg(src + c * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
-          rr[4 * u + 0] = x.x;
-          rr[4 * u + 1] = x.y;
-          rr[4 * u + 2] = x.z;
-          rr[4 * u + 3] = x.w;
+          rr[4 * u + 0] = cur[u].x;
+          rr[4 * u + 1] = cur[u].y;
+          rr[4 * u + 2] = cur[u].z;
+          rr[4 * u + 3] = cur[u].w;
         }
         tmem_st32(tmem + lanebase + kColQ + 32 * c, rr);
+        if (c + 1 < kQTmemDims / 64) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) cur[u] = nxt[u];
+        }
       }
       tc_fence_before();
       mbar_arrive(Q_TMEM);
@@ -289,7 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64(tmem + lanebase + kColS, sr);
       tc_fence_before();
       mbar_arrive(S_FREE);
-      const unsigned long long msk = mask_s[st];
+      const unsigned long long msk = static_cast<unsigned long long>(mask_s[2 * it]) |
+                                     (static_cast<unsigned long long>(mask_s[2 * it + 1]) << 32);
       float x[64];
       float tmax = ninf;
 #pragma unroll
@@ -368,20 +408,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
-  CUtensorMap tq, tkv;
+  CUtensorMap tq;
   const uint64_t qrows = static_cast<uint64_t>(a.batch) * a.nq * a.heads;
-  const uint64_t rows = static_cast<uint64_t>(a.num_pages) * kPage;
   if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kLatentDim, qrows,
                       kLatentDim * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kLatentDim, rows,
-                      kLatentDim * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.num_splits, a.batch * a.nq);
-  sparse_mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tkv, a);
+  sparse_mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, a);
   return cudaGetLastError();
 }
 

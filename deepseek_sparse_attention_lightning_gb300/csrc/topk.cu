@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kSelMax = 2048;                         // positions above b* per chunk < k
+constexpr int kPairMax = 1024;                        // sub-candidates ranked pairwise (fit in ssel)
 constexpr int kOffHist = 0;                           // 2048 x u32
 constexpr int kOffSel = kOffHist + kHistBins * 4;     // 2048 x i32
 constexpr int kOffCand = kOffSel + kSelMax * 4;       // kTopkChunk x uint2
@@ -34,6 +35,16 @@ constexpr int kBitmapWords = kSmemBytes / 4;
 
 __device__ __forceinline__ int visible(const int32_t* seqlens, int t, int nq) {
   return seqlens[t / nq] - (nq - 1 - t % nq);
+}
+
+// Cache row of logical position s of request r (-1 if its page id is bad).
+__device__ __forceinline__ int phys_row(const TopkLaunch& p, int r, int s) {
+  const int pg = p.page_table[static_cast<long long>(r) * p.max_pages + (s >> 6)];
+  if (pg < 0 || pg >= p.num_pages) {
+    raise_error(kErrCheck);
+    return -1;
+  }
+  return pg * kPage + (s & (kPage - 1));
 }
 
 // Exclusive scan of one value per thread over a 512-thread block.
@@ -127,17 +138,26 @@ __global__ void __launch_bounds__(kThreads)
   uint2* scand = reinterpret_cast<uint2*>(smem + kOffCand);
   __shared__ uint32_t scratch[40];
   __shared__ int res[2];
-  __shared__ int s_info[8];   // nsel, ncand, base, cbase, last, emit
+  __shared__ int s_info[8];   // nsel, ncand, base, cbase, last, emit, sub count
 
   const int t = blockIdx.y;
   const int k = p.k;
   const int vis = visible(p.seqlens, t, p.nq);
   int32_t* out_row = p.out + static_cast<long long>(t) * k;
 
+  const int req = t / p.nq;
   if (vis <= k) {
     // Every visible token is selected (the short-context case).
-    if (blockIdx.x == 0)
-      for (int i = threadIdx.x; i < k; i += kThreads) out_row[i] = i < vis ? i : -1;
+    if (blockIdx.x == 0) {
+      int32_t* rows_row = p.rows ? p.rows + static_cast<long long>(t) * k : nullptr;
+      for (int i = threadIdx.x; i < k; i += kThreads) {
+        out_row[i] = i < vis ? i : -1;
+        if (rows_row) {
+          const int row = i < vis ? phys_row(p, req, i) : -1;
+          rows_row[i] = row;
+        }
+      }
+    }
     return;
   }
   const int nch = (vis + kTopkChunk - 1) / kTopkChunk;
@@ -145,14 +165,28 @@ __global__ void __launch_bounds__(kThreads)
   uint32_t* counters = p.counters + static_cast<long long>(t) * kCounterWords;
   uint2* cand_row = p.cand + static_cast<long long>(t) * p.ld;
 
+  // ---- this CTA's chunk of the row: all of a thread's scores are loaded
+  //      first (one latency), then the row histogram.
+  const float* row = p.logits + static_cast<long long>(t) * p.ld;
+  const int lo = blockIdx.x * kTopkChunk;
+  const int hi = min(vis, lo + kTopkChunk);
+  constexpr int kIters = kTopkChunk / (4 * kThreads);
+  float x[kIters][4];
+#pragma unroll
+  for (int q = 0; q < kIters; ++q) {
+    const int s = lo + q * 4 * kThreads + 4 * static_cast<int>(threadIdx.x);
+    if (s + 3 < hi) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(row + s));
+      x[q][0] = v.x; x[q][1] = v.y; x[q][2] = v.z; x[q][3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[q][e] = s + e < hi ? __ldcg(row + s + e) : 0.f;
+    }
+  }
   // ---- threshold bin b*: the count of scores in bins above it is < k and
   //      reaches k with it.
   const uint32_t* gh = p.hist + static_cast<long long>(t) * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = __ldcg(gh + i);
-  if (threadIdx.x == 0) {
-    s_info[0] = 0;
-    s_info[1] = 0;
-  }
   __syncthreads();
   find_crossing(sh, static_cast<uint32_t>(k), true, res, scratch);
   const int bstar = res[0];
@@ -160,38 +194,57 @@ __global__ void __launch_bounds__(kThreads)
     if (threadIdx.x == 0) raise_error(kErrCheck);
     return;
   }
-
-  // ---- scan this CTA's chunk of the row
-  const float* row = p.logits + static_cast<long long>(t) * p.ld;
-  const int lo = blockIdx.x * kTopkChunk;
-  const int hi = min(vis, lo + kTopkChunk);
-  const int vend = lo + ((hi - lo) & ~3);
   const uint32_t ub = static_cast<uint32_t>(bstar);
-  auto visit = [&](int s, float x) {
-    const uint32_t key = float_key(x);
-    const uint32_t bin = key >> kHistShift;
-    if (bin > ub) {
-      const int pos = atomicAdd(&s_info[0], 1);
-      if (pos < kSelMax) ssel[pos] = s;
-    } else if (bin == ub) {
-      const int pos = atomicAdd(&s_info[1], 1);
-      scand[pos] = make_uint2(key, static_cast<uint32_t>(s));
+  // Classify the thread's scores, then place them with one block scan of the
+  // packed (candidates << 16 | selected) counts.
+  uint32_t above = 0, inbin = 0;
+#pragma unroll
+  for (int q = 0; q < kIters; ++q) {
+    const int s = lo + q * 4 * kThreads + 4 * static_cast<int>(threadIdx.x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t bin = float_key(x[q][e]) >> kHistShift;
+      const uint32_t bit = 1u << (4 * q + e);
+      if (s + e < hi) {
+        if (bin > ub) above |= bit;
+        else if (bin == ub) inbin |= bit;
+      }
     }
-  };
-  for (int s = lo + 4 * threadIdx.x; s < vend; s += 4 * kThreads) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + s));
-    visit(s, v.x);
-    visit(s + 1, v.y);
-    visit(s + 2, v.z);
-    visit(s + 3, v.w);
   }
-  for (int s = vend + threadIdx.x; s < hi; s += kThreads) visit(s, __ldcg(row + s));
+  const uint32_t mine = (static_cast<uint32_t>(__popc(inbin)) << 16) | __popc(above);
+  const uint32_t off = block_excl_scan_512(mine, scratch);
+  if (threadIdx.x == kThreads - 1) {
+    s_info[0] = static_cast<int>((off + mine) & 0xFFFFu);
+    s_info[1] = static_cast<int>((off + mine) >> 16);
+  }
+  {
+    int oa = static_cast<int>(off & 0xFFFFu), oc = static_cast<int>(off >> 16);
+#pragma unroll
+    for (int q = 0; q < kIters; ++q) {
+      const int s = lo + q * 4 * kThreads + 4 * static_cast<int>(threadIdx.x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t bit = 1u << (4 * q + e);
+        if (above & bit) {
+          if (oa < kSelMax) ssel[oa] = s + e;
+          ++oa;
+        } else if (inbin & bit) {
+          scand[oc++] = make_uint2(float_key(x[q][e]), static_cast<uint32_t>(s + e));
+        }
+      }
+    }
+  }
   __syncthreads();
   const int nsel = s_info[0], ncand = s_info[1];
   if (threadIdx.x == 0) {
     if (nsel > kSelMax) raise_error(kErrCheck);
-    s_info[2] = nsel ? static_cast<int>(atomicAdd(counters + 0, static_cast<uint32_t>(nsel))) : 0;
-    s_info[3] = ncand ? static_cast<int>(atomicAdd(counters + 1, static_cast<uint32_t>(ncand))) : 0;
+    // One 64-bit atomic reserves room in both lists: (candidates, selected).
+    const unsigned long long add =
+        (static_cast<unsigned long long>(ncand) << 32) | static_cast<unsigned long long>(nsel);
+    const unsigned long long old =
+        atomicAdd(reinterpret_cast<unsigned long long*>(counters), add);
+    s_info[2] = static_cast<int>(old & 0xFFFFFFFFull);
+    s_info[3] = static_cast<int>(old >> 32);
   }
   __syncthreads();
   {
@@ -201,17 +254,20 @@ __global__ void __launch_bounds__(kThreads)
       if (base + i < k) out_row[base + i] = ssel[i];
     for (int i = threadIdx.x; i < ncand; i += kThreads) cand_row[cbase + i] = scand[i];
   }
-  __threadfence();
+  // The barrier orders the block's writes before thread 0's release fence;
+  // the last CTA's acquire fence then sees every CTA's writes.
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     const uint32_t ticket = atomicAdd(counters + 2, 1u);
-    s_info[4] = (ticket == static_cast<uint32_t>(nch - 1)) ? 1 : 0;
+    const bool last = ticket == static_cast<uint32_t>(nch - 1);
+    if (last) __threadfence();
+    s_info[4] = last ? 1 : 0;
   }
   __syncthreads();
   if (!s_info[4]) return;
 
   // ---- last CTA of the row: resolve the candidates of bin b*.
-  __threadfence();
   const int nabove = static_cast<int>(__ldcg(counters + 0));
   const int nc = static_cast<int>(__ldcg(counters + 1));
   const uint32_t need = static_cast<uint32_t>(k - nabove);
@@ -229,6 +285,7 @@ __global__ void __launch_bounds__(kThreads)
   const int kshift[2] = {10, 0};
   const int kwidth[2] = {11, 10};
   bool ok = need >= 1;
+  bool pairwise = false;
   for (int lvl = 0; lvl < 2 && ok; ++lvl) {
     const int sh_ = kshift[lvl];
     const uint32_t dm = (1u << kwidth[lvl]) - 1u;
@@ -247,42 +304,86 @@ __global__ void __launch_bounds__(kThreads)
     kprefix |= d << sh_;
     kmask |= dm << sh_;
     __syncthreads();
-  }
-  const uint32_t kstar = kprefix;
-  // Exact ties at the threshold key: keep the need_l lowest positions.
-  uint32_t istar = 0xFFFFFFFFu;
-  if (ok && need_l < cnt_eq) {
-    uint32_t iprefix = 0, imask = 0, need_i = need_l;
-    const int ishift[3] = {20, 10, 0};
-    const int iwidth[3] = {11, 10, 10};
-    for (int lvl = 0; lvl < 3 && ok; ++lvl) {
-      const int sh_ = ishift[lvl];
-      const uint32_t dm = (1u << iwidth[lvl]) - 1u;
-      for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
-      __syncthreads();
-      for (int e = threadIdx.x; e < nc; e += kThreads) {
-        const uint2 c = cp[e];
-        if (c.x == kstar && (c.y & imask) == iprefix) atomicAdd(&sh[(c.y >> sh_) & dm], 1u);
-      }
-      __syncthreads();
-      find_crossing(sh, need_i, false, res, scratch);
-      if (res[0] < 0) { ok = false; break; }
-      need_i -= static_cast<uint32_t>(res[1]);
-      iprefix |= static_cast<uint32_t>(res[0]) << sh_;
-      imask |= dm << sh_;
-      __syncthreads();
+    // Few candidates left in the crossing digit: rank them pairwise instead
+    // of further radix levels.
+    if (lvl == 0 && cnt_eq <= static_cast<uint32_t>(kPairMax)) {
+      pairwise = true;
+      break;
     }
-    istar = iprefix;
   }
   if (!ok) {
     if (threadIdx.x == 0) raise_error(kErrCheck);
     return;
   }
-  for (int e = threadIdx.x; e < nc; e += kThreads) {
-    const uint2 c = cp[e];
-    if (c.x > kstar || (c.x == kstar && c.y <= istar)) {
-      const int pos = atomicAdd(&s_info[5], 1);
-      if (nabove + pos < k) out_row[nabove + pos] = static_cast<int>(c.y);
+  if (pairwise) {
+    // Candidates whose digit is above the crossing one are in; of those with
+    // the crossing digit (m <= kPairMax), the need_l best by (key desc,
+    // position asc) are in.
+    uint2* sub = reinterpret_cast<uint2*>(ssel);
+    if (threadIdx.x == 0) s_info[6] = 0;
+    __syncthreads();
+    const uint32_t hi_digits = kprefix >> 10;
+    for (int e = threadIdx.x; e < nc; e += kThreads) {
+      const uint2 c = cp[e];
+      const uint32_t cd = c.x >> 10;
+      if (cd > hi_digits) {
+        const int pos = atomicAdd(&s_info[5], 1);
+        if (nabove + pos < k) out_row[nabove + pos] = static_cast<int>(c.y);
+      } else if (cd == hi_digits) {
+        sub[atomicAdd(&s_info[6], 1)] = c;
+      }
+    }
+    __syncthreads();
+    const int m = s_info[6];
+    for (int i = threadIdx.x; i < m; i += kThreads) {
+      const uint2 ci = sub[i];
+      uint32_t rank = 0;
+      for (int j2 = 0; j2 < m; ++j2) {
+        const uint2 cj = sub[j2];
+        rank += (cj.x > ci.x || (cj.x == ci.x && cj.y < ci.y)) ? 1u : 0u;
+      }
+      if (rank < need_l) {
+        const int pos = atomicAdd(&s_info[5], 1);
+        if (nabove + pos < k) out_row[nabove + pos] = static_cast<int>(ci.y);
+      }
+    }
+  } else {
+    const uint32_t kstar = kprefix;
+    // Exact ties at the threshold key: keep the need_l lowest positions.
+    uint32_t istar = 0xFFFFFFFFu;
+    if (need_l < cnt_eq) {
+      uint32_t iprefix = 0, imask = 0, need_i = need_l;
+      const int ishift[3] = {20, 10, 0};
+      const int iwidth[3] = {11, 10, 10};
+      for (int lvl = 0; lvl < 3 && ok; ++lvl) {
+        const int sh_ = ishift[lvl];
+        const uint32_t dm = (1u << iwidth[lvl]) - 1u;
+        for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
+        __syncthreads();
+        for (int e = threadIdx.x; e < nc; e += kThreads) {
+          const uint2 c = cp[e];
+          if (c.x == kstar && (c.y & imask) == iprefix) atomicAdd(&sh[(c.y >> sh_) & dm], 1u);
+        }
+        __syncthreads();
+        find_crossing(sh, need_i, false, res, scratch);
+        if (res[0] < 0) { ok = false; break; }
+        need_i -= static_cast<uint32_t>(res[1]);
+        iprefix |= static_cast<uint32_t>(res[0]) << sh_;
+        imask |= dm << sh_;
+        __syncthreads();
+      }
+      istar = iprefix;
+    }
+    if (!ok) {
+      if (threadIdx.x == 0) raise_error(kErrCheck);
+      return;
+    }
+    for (int e = threadIdx.x; e < nc; e += kThreads) {
+      const uint2 c = cp[e];
+      if (c.x > kstar || (c.x == kstar && c.y <= istar)) {
+        const int pos = atomicAdd(&s_info[5], 1);
+        if (nabove + pos < k) out_row[nabove + pos] = static_cast<int>(c.y);
+      }
     }
   }
   __threadfence_block();
@@ -291,27 +392,37 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---- rewrite the row in ascending position order through a bitmap.
   const int nwords = (vis + 31) >> 5;
-  if (nwords > kBitmapWords) return;
-  uint32_t* bm = reinterpret_cast<uint32_t*>(smem);
-  for (int i = threadIdx.x; i < nwords; i += kThreads) bm[i] = 0u;
-  __syncthreads();
-  for (int i = threadIdx.x; i < k; i += kThreads) {
-    const int s = __ldcg(out_row + i);
-    if (s >= 0 && s < vis) atomicOr(&bm[s >> 5], 1u << (s & 31));
+  if (nwords <= kBitmapWords) {
+    uint32_t* bm = reinterpret_cast<uint32_t*>(smem);
+    for (int i = threadIdx.x; i < nwords; i += kThreads) bm[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < k; i += kThreads) {
+      const int s = __ldcg(out_row + i);
+      if (s >= 0 && s < vis) atomicOr(&bm[s >> 5], 1u << (s & 31));
+    }
+    __syncthreads();
+    const int per = (nwords + kThreads - 1) / kThreads;
+    const int w0 = min(nwords, threadIdx.x * per), w1 = min(nwords, w0 + per);
+    uint32_t cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
+    uint32_t pos = block_excl_scan_512(cnt, scratch);
+    for (int w = w0; w < w1; ++w) {
+      uint32_t bits = bm[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (pos < static_cast<uint32_t>(k)) out_row[pos] = w * 32 + b;
+        ++pos;
+      }
+    }
   }
-  __syncthreads();
-  const int per = (nwords + kThreads - 1) / kThreads;
-  const int w0 = min(nwords, threadIdx.x * per), w1 = min(nwords, w0 + per);
-  uint32_t cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
-  uint32_t off = block_excl_scan_512(cnt, scratch);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bits = bm[w];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1;
-      if (off < static_cast<uint32_t>(k)) out_row[off] = w * 32 + b;
-      ++off;
+  if (p.rows) {
+    // Fused index -> cache-row transform of the final selection.
+    __syncthreads();
+    int32_t* rows_row = p.rows + static_cast<long long>(t) * k;
+    for (int i = threadIdx.x; i < k; i += kThreads) {
+      const int s = __ldcg(out_row + i);
+      rows_row[i] = (s >= 0 && s < vis) ? phys_row(p, req, s) : -1;
     }
   }
 }

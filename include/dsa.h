@@ -112,7 +112,7 @@ typedef struct dsa_decode_desc {
  *   q_scale [dev] float [T]           per query token, > 0
  *   w       [dev] float [T, 64]       per-head weights
  *   k_fp8   [dev] uint8 [num_pages*64, 128] FP8 E4M3 index-key cache, 16-B aligned
- *   k_scale [dev] float [num_pages*64] per cached token, > 0
+ *   k_scale [dev] float [num_pages*64] per cached token, > 0, 16-B aligned
  *   logits  [dev] float [T, ld_logits]; ld_logits >= max_pages*64, multiple of 4
  */
 dsa_status dsa_indexer_logits(const dsa_decode_desc* desc, const uint8_t* q_fp8,
