@@ -41,6 +41,8 @@ _SIGS = {
     "dsa_topk": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_int64, c_void_p, c_void_p,
                            c_size_t, c_void_p]),
     "dsa_topk_workspace_bytes": (c_size_t, [ctypes.POINTER(DecodeDesc), c_int64]),
+    "dsa_topk_noalloc": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_int64, c_void_p,
+                                   c_void_p]),
     "dsa_sparse_mla_decode_split": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p,
                                               c_void_p, c_int32, c_float, c_void_p, c_void_p,
                                               c_void_p]),
@@ -148,6 +150,15 @@ def dsa_topk(desc, logits, topk_idx, ws, ld=None, stream=None):
     _check(lib().dsa_topk(ctypes.byref(desc), _ptr(logits, torch.float32, "logits"), ld,
                           _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(ws, torch.uint8, "ws"),
                           ws.numel(), _stream(stream)), "dsa_topk")
+
+
+def dsa_topk_noalloc(desc, logits, topk_idx, ld=None, stream=None):
+    """dsa_topk with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/dsa.h)."""
+    ld = int(logits.shape[-1]) if ld is None else int(ld)
+    _check(lib().dsa_topk_noalloc(ctypes.byref(desc), _ptr(logits, torch.float32, "logits"), ld,
+                                  _ptr(topk_idx, torch.int32, "topk_idx"), _stream(stream)),
+           "dsa_topk_noalloc")
 
 
 def dsa_sparse_mla_decode_split(desc, q, kv, topk_idx, num_splits, sm_scale, mid_o, mid_lse,

@@ -16,6 +16,9 @@
 //           key bits and, for exact ties, a radix select over the position,
 //           then rewrites the row in ascending position order through a
 //           shared-memory bitmap.
+#include <mutex>
+
+#include "dsa.h"
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
 
@@ -445,4 +448,83 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Top-k without a caller-provided workspace (dsa_topk_noalloc).
+//
+// For callers that cannot allocate device memory at the point where they run
+// the selection, the histogram, counters and candidate lists live in one
+// statically sized device array.  Every GPU that loads the library reserves
+// it (kNoAllocScratchBytes) until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxRows = 64;                 // query rows T
+constexpr long long kNoAllocMaxScores = 1ll << 21;  // T * ld_logits
+constexpr size_t kNoAllocHistBytes = size_t(kNoAllocMaxRows) * kHistBins * 4;
+constexpr size_t kNoAllocCounterOff = kNoAllocHistBytes;
+constexpr size_t kNoAllocCandOff =
+    (kNoAllocCounterOff + size_t(kNoAllocMaxRows) * kCounterWords * 4 + 255) & ~size_t(255);
+constexpr size_t kNoAllocScratchBytes = kNoAllocCandOff + size_t(kNoAllocMaxScores) * 8;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device (looked up once
+// per device; the host-side symbol is not a device address).
+void* noalloc_scratch(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
 }  // namespace dsa
+
+extern "C" dsa_status dsa_topk_noalloc(const dsa_decode_desc* d, const float* logits,
+                                       int64_t ld, int32_t* topk_idx, void* stream) {
+  using namespace dsa;
+  if (!d || d->batch < 1 || d->q_per_req < 1 || d->num_heads < 1 || d->topk < 1 ||
+      d->max_pages < 1 || d->num_pages < 1 || !d->seqlens || !d->page_table)
+    return DSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(d->seqlens) & 3) || (reinterpret_cast<uintptr_t>(d->page_table) & 3))
+    return DSA_ERR_INVALID_ARG;
+  if (d->batch > DSA_MAX_BATCH || d->q_per_req > DSA_MAX_Q_PER_REQ || d->topk > DSA_MAX_TOPK ||
+      d->page_size != DSA_PAGE_SIZE)
+    return DSA_ERR_UNSUPPORTED;
+  if (!logits || !topk_idx || (reinterpret_cast<uintptr_t>(logits) & 15) ||
+      (reinterpret_cast<uintptr_t>(topk_idx) & 3))
+    return DSA_ERR_INVALID_ARG;
+  if (ld < static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE || ld % 4 != 0)
+    return DSA_ERR_INVALID_ARG;
+  const int T = d->batch * d->q_per_req;
+  if (T > kNoAllocMaxRows || static_cast<long long>(T) * ld > kNoAllocMaxScores)
+    return DSA_ERR_UNSUPPORTED;   // beyond the fixed scratch: use dsa_topk with a workspace
+  cudaError_t e;
+  uint8_t* base = static_cast<uint8_t*>(noalloc_scratch(&e));
+  if (!base) return DSA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The previous call's histogram and counters are still there: clear them.
+  e = cudaMemsetAsync(base, 0, kNoAllocCandOff, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  TopkLaunch a{};
+  a.seqlens = d->seqlens; a.logits = logits; a.ld = ld; a.out = topk_idx;
+  a.hist = reinterpret_cast<uint32_t*>(base);
+  a.counters = reinterpret_cast<uint32_t*>(base + kNoAllocCounterOff);
+  a.cand = reinterpret_cast<uint2*>(base + kNoAllocCandOff);
+  a.batch = d->batch; a.nq = d->q_per_req; a.k = d->topk; a.hist_ready = 0;
+  return launch_topk(a, s) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}

@@ -140,6 +140,30 @@ dsa_status dsa_topk(const dsa_decode_desc* desc, const float* logits, int64_t ld
 size_t dsa_topk_workspace_bytes(const dsa_decode_desc* desc, int64_t ld_logits);
 
 /*
+ * dsa_topk without a workspace argument.  (A library convenience; the pages
+ * have no counterpart.)
+ *
+ * For callers that cannot allocate device memory where they run the
+ * selection: an inference-engine plugin or step function that executes after
+ * the engine has reserved all of the device's memory for its caches, or a
+ * host runtime without a device allocator of its own, where a cudaMalloc
+ * would fail or stall the device.  The histogram, counters and candidate
+ * lists then live in a file-scope device array of fixed size (about 16.5 MB)
+ * that every GPU loading this library reserves until the process exits.  No
+ * call allocates or frees memory.
+ *   Limits: T = batch * q_per_req <= 64 and T * ld_logits <= 2^21 scores;
+ *   larger batches return DSA_ERR_UNSUPPORTED (use dsa_topk with a workspace).
+ *   The first call on a device looks up the array's device address (once per
+ *   device); make that first call before capturing the stream into a graph.
+ *   All calls on a device share the one array: each call clears the parts
+ *   that must start at zero, and calls that may run at the same time on the
+ *   GPU (different streams, no ordering between them) race on it.
+ * Arguments and results are those of dsa_topk.
+ */
+dsa_status dsa_topk_noalloc(const dsa_decode_desc* desc, const float* logits, int64_t ld_logits,
+                            int32_t* topk_idx, void* stream);
+
+/*
  * Stage 3 -- sparse MLA split partials ("Deepseek Details", section "DSA",
  * stage 2: each block of the selected tokens runs an online softmax and writes
  * Mid_O[batch, head, block, dim] and Mid_O_LogExpSum[batch, head, block];
