@@ -42,14 +42,21 @@ constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiGroups = 2;   // warps 4-7 take even tiles, warps 8-11 odd tiles
 constexpr int kMaxBatch = 1024;
-constexpr int kPageWin = 1024;  // page ids cached in shared memory (512 tiles)
+constexpr int kPageWin = 512;   // page ids cached in shared memory (256 tiles)
 constexpr int kScaleAhead = 3;  // epilogue scale prefetch distance (own tiles)
+constexpr int kSmemLimit = 232448;
 
 template <int NQ>
 struct Cfg {
   static constexpr int kN = 64 * NQ;
-  static constexpr int kStages = NQ == 4 ? 5 : (NQ == 3 ? 6 : 8);
   static constexpr int kQBytes = kN * kIndexDim;
+  // Everything but the key ring; the ring then takes what shared memory is
+  // left (up to 12 stages): the ring's bytes in flight set the bandwidth.
+  static constexpr int kFixed = 2 * kQBytes + kEpiGroups * NQ * kHistBins * 4 +
+                                kEpiGroups * kN * 4 + kPageWin * 4 + (1024 + 4) * 4 + 64 * 4 +
+                                (2 * 12 + 8) * 8 + 16 + 1024;
+  static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
   static constexpr int kTmemCols = (2 * kN <= 128) ? 128 : ((2 * kN <= 256) ? 256 : 512);
   static constexpr int kOffStages = 0;
   static constexpr int kOffQ = kStages * kStageBytes;
