@@ -307,7 +307,9 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
     ta.cand = reinterpret_cast<uint2*>(base + lay.cand);
     ta.batch = d->batch; ta.nq = d->q_per_req; ta.k = d->topk; ta.hist_ready = 1;
     ta.rows = reinterpret_cast<int32_t*>(base + lay.rows);
-    ta.page_table = d->page_table; ta.max_pages = d->max_pages; ta.num_pages = d->num_pages;    e = dsa::launch_topk(ta, s);
+    ta.page_table = d->page_table; ta.max_pages = d->max_pages; ta.num_pages = d->num_pages;
+    ta.pdl = 1;   // overlaps its launch with the indexer's last CTAs
+    e = dsa::launch_topk(ta, s);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     idx = sel;
   } else if (!mark(0) || !mark(1)) {
@@ -322,10 +324,13 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
   ma.batch = d->batch; ma.nq = d->q_per_req; ma.heads = d->num_heads; ma.k = d->topk;
   ma.max_pages = d->max_pages; ma.num_pages = d->num_pages; ma.num_splits = splits;
   ma.sm_scale = sm_scale;
+  // After the fused top-k, the attention CTAs start (and fetch their queries)
+  // while the top-k finishes; they wait for it before reading its rows.
+  ma.pdl = topk_in ? 0 : 1;
   cudaError_t e = dsa::launch_sparse_mla(ma, s);
   if (e != cudaSuccess || !mark(3)) return DSA_ERR_CUDA;
   if (splits > 1) {
-    e = dsa::launch_merge(T * d->num_heads, splits, ma.mid_o, ma.mid_lse, out, nullptr, s);
+    e = dsa::launch_merge(T * d->num_heads, splits, ma.mid_o, ma.mid_lse, out, nullptr, s, true);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
   }
   if (!mark(4)) return DSA_ERR_CUDA;

@@ -49,6 +49,7 @@ struct TopkLaunch {
   int32_t* rows;        // [T][k] or nullptr
   const int32_t* page_table;
   int max_pages, num_pages;
+  int pdl;              // 1: launched as a programmatic dependent of the indexer
 };
 
 struct MlaLaunch {
@@ -62,13 +63,33 @@ struct MlaLaunch {
   float* mid_lse;
   int batch, nq, heads, k, max_pages, num_pages, num_splits;
   float sm_scale;
+  int pdl;              // 1: launched as a programmatic dependent of the top-k
 };
 
 cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s);
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t s);
 cudaError_t launch_merge(int rows, int splits, const float* mid_o, const float* mid_lse,
-                         float* out, float* out_lse, cudaStream_t s);
+                         float* out, float* out_lse, cudaStream_t s, bool pdl = false);
+
+// Launches `kern` on `s`; with `pdl` as a programmatic dependent of the
+// previous kernel of the stream (the kernel then calls grid_dep_wait before it
+// reads anything that kernel wrote).
+template <typename... Exp, typename... Act>
+cudaError_t launch_kernel(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool pdl, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Act&&>(args)...);
+}
 
 // Each translation unit keeps its own device error word; these read and clear
 // them (synchronous).  Return 0 or a dsa_status code.

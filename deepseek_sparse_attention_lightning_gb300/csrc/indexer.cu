@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  grid_dep_launch();   // the top-k may be scheduled as this kernel's CTAs retire
   auto page_of = [&](int r, int g, int which) -> int {
     const int i = 2 * (g - g0) + which;
     return i < kPageWin ? pages[i] : tile_page(p, prefix, r, g, which);

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kThreads)
     merge_kernel(int rows, int splits, const float* __restrict__ mid_o,
                  const float* __restrict__ mid_lse, float* __restrict__ out,
                  float* __restrict__ out_lse) {
+  grid_dep_wait();   // Mid_O / Mid_LSE may come from the kernel before
+  grid_dep_launch();
   const long long gid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   const int row = static_cast<int>(gid / kVec);
   const int c4 = static_cast<int>(gid % kVec);
@@ -70,12 +72,12 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 cudaError_t launch_merge(int rows, int splits, const float* mid_o, const float* mid_lse,
-                         float* out, float* out_lse, cudaStream_t stream) {
+                         float* out, float* out_lse, cudaStream_t stream, bool pdl) {
   if (rows <= 0) return cudaSuccess;
   const long long threads = static_cast<long long>(rows) * kVec;
   const int grid = static_cast<int>((threads + kThreads - 1) / kThreads);
-  merge_kernel<<<grid, kThreads, 0, stream>>>(rows, splits, mid_o, mid_lse, out, out_lse);
-  return cudaGetLastError();
+  return launch_kernel(merge_kernel, dim3(grid), dim3(kThreads), 0, stream, pdl, rows, splits,
+                       mid_o, mid_lse, out, out_lse);
 }
 
 }  // namespace dsa

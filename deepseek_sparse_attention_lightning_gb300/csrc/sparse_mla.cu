@@ -19,7 +19,11 @@
 //   [320,352)  P   bf16 probabilities (2 per column), the A operand of P V
 //   [352,512)  Q   q dims [0, 320) as bf16 pairs, the A operand of Q K^T
 // Shared memory: q dims [320, 576) (64 KB, 128B-swizzled) and two stages of
-// 64 gathered latent rows (9 atoms of 64 dims, 72 KB each).
+// 64 gathered latent rows (9 atoms of 64 dims, 72 KB each).  Before the
+// second stage holds keys it holds q dims [0, 256), brought by TMA for the
+// softmax threads to move into TMEM (q dims [256, 320) they load
+// themselves): the SM's load/store path delivers only ~20 GB/s of scattered
+// 16-byte loads, the copy engine several times that.
 //
 // Per tile: S = Q K^T is 20 TMEM-A MMAs (dims 0..319) + 16 smem-A MMAs (dims
 // 320..575), M = 128, N = 64, K = 16 (kind::f16, bf16 in, fp32 out).  The
@@ -31,10 +35,12 @@
 //
 // Warp roles (256 threads): warps 0, 2, 3 resolve every selected position to
 // its cache row (logical index -> page table -> row, fused here) and gather
-// the rows with 16-byte cp.async copies written straight into the swizzled
-// stage layout (a row-granular gather; TMA tile::gather4 was measured to be
-// issue-bound at ~100 cycles per 4 rows); warp 1 issues the MMAs and owns
-// TMEM; warps 4-7 run the softmax and the epilogue.
+// the rows with TMA tile::gather4 copies (4 rows x 64 dims each, written in
+// the 128B-swizzled stage layout by the copy engine); all 96 loader threads
+// issue, because one gather4 costs its issuing thread ~170 cycles while the
+// SM's copy engine accepts many at once (one issuer: ~0.8 TB/s over the GPU,
+// 128 issuers: ~4.7 TB/s, on 1152-byte rows).  Warp 1 issues the MMAs and
+// owns TMEM; warps 4-7 run the softmax and the epilogue.
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
 
@@ -56,7 +62,8 @@ constexpr int kMaxPos = 2048;                            // positions of one spl
 constexpr int kOffRows = kOffStage + 2 * kStageBytes;    // cache row of every position
 constexpr int kOffMask = kOffRows + kMaxPos * 4;         // validity bits, 32 per word
 constexpr int kOffBar = kOffMask + (kMaxPos / 32) * 4;
-constexpr int kNumBars = 10;
+constexpr int kNumBars = 11;
+constexpr int kQStageAtoms = 4;                            // q dims [0, 256) via stage 1
 constexpr int kOffSlot = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;
 constexpr int kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
@@ -64,7 +71,9 @@ constexpr int kTmemCols = 512;
 constexpr int kThreads = 256;
 constexpr int kSoftWarp0 = 4;
 constexpr int kLoaderWarps = 3;                            // warps 0, 2, 3
-constexpr int kRowChunks = kLatentDim * 2 / 16;            // 72 chunks of 16 B per row
+constexpr int kGathers = (kBN / 4) * kAtoms;               // 144 gather4 copies per tile
+constexpr int kORowPitch = 256 * 4 + 16;                   // staged Mid_O row (epilogue)
+static_assert(128 * kORowPitch <= 2 * kStageBytes, "Mid_O staging fits in the key stages");
 constexpr float kRescaleLog2 = 8.0f;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -73,7 +82,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q, const MlaLaunch p) {
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                      const __grid_constant__ CUtensorMap tmap_kv, const MlaLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   const int split = blockIdx.x >> 1, half = blockIdx.x & 1, t = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
   const uint32_t bar0 = sbase + kOffBar;
   const uint32_t Q_FULL = bar0, Q_TMEM = bar0 + 8, S_FULL = bar0 + 16, S_FREE = bar0 + 24,
-                 P_FULL = bar0 + 32, PV_DONE = bar0 + 40;
+                 P_FULL = bar0 + 32, PV_DONE = bar0 + 40, Q_STAGE = bar0 + 80;
 #define KV_FULL(s) (bar0 + 48u + 8u * (s))
 #define KV_EMPTY(s) (bar0 + 64u + 8u * (s))
 
@@ -120,8 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(S_FREE, 128);
     mbar_init(P_FULL, 128);
     mbar_init(PV_DONE, 1);
+    mbar_init(Q_STAGE, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(KV_FULL(s), kLoaderWarps * 32);   // one cp.async arrive per loader thread
+      mbar_init(KV_FULL(s), kLoaderWarps * 32);   // one expect-tx arrive per loader thread
       mbar_init(KV_EMPTY(s), 1);
     }
     fence_mbar_init();
@@ -133,16 +144,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();
 
   if (warp == 0 || warp == 2 || warp == 3) {
     // ------------------------------------------------------------ loaders
-    // Three warps (96 threads) gather the selected latent rows with 16-byte
-    // cp.async copies into the 128B-swizzled stage layout; each thread's
-    // copies arrive on the stage's full barrier when they land.
+    // Three warps (96 threads) gather the selected latent rows with TMA
+    // gather4 copies into the 128B-swizzled stage layout; each thread
+    // announces its own bytes on the stage's full barrier, then issues.
     const int lw = warp == 0 ? 0 : warp - 1;           // loader warp 0..2
     const int ltid = lw * 32 + lane;
     const int* ptab = p.page_table + static_cast<long long>(r) * p.max_pages;
     const int* idx_row = p.topk_idx + static_cast<long long>(t) * k;
+    // The selected positions come from the kernel before (the top-k when
+    // launched as its dependent); the queries, page table and cache do not.
+    grid_dep_wait();
     int safe_row = 0;
     {
       const int pg0 = ptab[0];
@@ -150,10 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ltid == 0) {
       prefetch_tmap(&tmap_q);
+      prefetch_tmap(&tmap_kv);
       mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
       for (int a = 0; a < kQSmemAtoms; ++a)
         tma_load_2d(sbase + kOffQ + a * kQAtomBytes, &tmap_q, kQTmemDims + 64 * a, t * H, Q_FULL,
                     policy_evict_last());
+      mbar_expect_tx(Q_STAGE, kQStageAtoms * kQAtomBytes);
+      for (int a = 0; a < kQStageAtoms; ++a)
+        tma_load_2d(sbase + kOffStage + kStageBytes + a * kQAtomBytes, &tmap_q, 64 * a, t * H,
+                    Q_STAGE, policy_evict_last());
     }
     // Resolve every position of the split first (logical index -> page table
     // -> cache row), 8 x 32 positions per batch so the loads overlap; the
@@ -207,27 +227,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     named_bar_sync(1, kLoaderWarps * 32);   // rows_s / mask_s complete
-    const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
+    const uint64_t pol_kv = policy_evict_last();   // the sibling half reads the same rows
+    int issued = 0;
     for (int it = 0; it < ntiles; ++it) {
       const int st = it & 1;
       if (it >= 2 && !mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1)) {
         raise_error(kErrTimeout);
         break;
       }
-      // 64 rows x 72 chunks of 16 B; chunk ch of row rr goes to atom ch / 8,
-      // slot (ch % 8) ^ (rr % 8) of the row's 128-byte line (128B swizzle).
+      // Stage 1 holds q dims [0, 256) until the softmax threads moved them.
+      if (it == 1 && !mbar_wait(Q_TMEM, 0)) {
+        raise_error(kErrTimeout);
+        break;
+      }
+      // Copy c = 9 g + a brings rows 4g..4g+3 of the tile, dims [64a, 64a+64),
+      // to atom a at byte 512 g (the copy engine applies the 128B swizzle).
       const uint32_t dst = sbase + kOffStage + st * kStageBytes;
       const int* rows = rows_s + it * kBN;
-      for (int c = ltid; c < kBN * kRowChunks; c += kLoaderWarps * 32) {
-        const int rr = c / kRowChunks, ch = c - rr * kRowChunks;
-        cp_async_16(dst + (ch >> 3) * kAtomBytes + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4),
-                    kvb + static_cast<long long>(rows[rr]) * (kLatentDim * 2) + ch * 16);
+      const int mine = (kGathers - ltid + kLoaderWarps * 32 - 1) / (kLoaderWarps * 32);
+      mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(mine) * 4u * 128u);
+      for (int c = ltid; c < kGathers; c += kLoaderWarps * 32) {
+        const int g = c / kAtoms, a = c - g * kAtoms;
+        const int* r4 = rows + 4 * g;
+        tma_gather4(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r4[0], r4[1], r4[2], r4[3],
+                    KV_FULL(st), pol_kv);
       }
-      cp_async_arrive_noinc(KV_FULL(st));
+      issued = it + 1;
     }
-    // No copy may still be in flight when the CTA exits.
-    cp_async_wait_all();
-    if (ltid == 0) mbar_wait(Q_FULL, 0);
+    // No copy may still be in flight when the CTA exits: the last phase of
+    // each stage completes only once every loader's bytes have landed.
+    if (ltid == 0) {
+      for (int u = issued - 1; u >= 0 && u >= issued - 2; --u) mbar_wait(KV_FULL(u & 1), (u >> 1) & 1);
+      mbar_wait(Q_FULL, 0);
+      mbar_wait(Q_STAGE, 0);
+    }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -253,9 +286,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < ntiles && ok; ++it) {
         const int st = it & 1;
         if (!mbar_wait(KV_FULL(st), (it >> 1) & 1)) { ok = false; break; }
-        // The tile was written by cp.async (generic proxy); make it visible to
-        // the tensor core's (async proxy) reads.
-        fence_proxy_async_smem();
         if (it >= 1 && !mbar_wait(S_FREE, (it - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t stage = sbase + kOffStage + st * kStageBytes;
@@ -285,35 +315,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = q4 * 32 + lane;
     const uint32_t lanebase = static_cast<uint32_t>(q4 * 32) << 16;
     const bool live = h < H;
-    // q dims [0, 320) -> TMEM columns [kColQ, kColQ + 160)
+    // q dims [0, 320) -> TMEM columns [kColQ, kColQ + 160): dims [0, 256)
+    // from the TMA copy in stage 1 (row h of each 128B-swizzled atom), dims
+    // [256, 320) loaded here.
     {
       const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<long long>(t) * H + (live ? h : 0)) * kLatentDim);
-      // Loads of chunk c+1 are in flight while chunk c is stored.
-      uint4 cur[8], nxt[8];
+          p.q + (static_cast<long long>(t) * H + (live ? h : 0)) * kLatentDim) +
+          kQStageAtoms * 8;
+      uint4 qv[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) cur[u] = live ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int c = 0; c < kQTmemDims / 64; ++c) {
-        if (c + 1 < kQTmemDims / 64) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            nxt[u] = live ? __ldg(src + (c + 1) * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
-        }
+      for (int u = 0; u < 8; ++u) qv[u] = live ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+      bool qok = mbar_wait(Q_STAGE, 0);
+      const uint8_t* qs = smem + kOffStage + kStageBytes + h * 128;
+#pragma unroll 1
+      for (int c = 0; c < kQStageAtoms; ++c) {
         uint32_t rr[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          rr[4 * u + 0] = cur[u].x;
-          rr[4 * u + 1] = cur[u].y;
-          rr[4 * u + 2] = cur[u].z;
-          rr[4 * u + 3] = cur[u].w;
+          const uint4 v = *reinterpret_cast<const uint4*>(qs + c * kQAtomBytes + ((u ^ (h & 7)) << 4));
+          rr[4 * u + 0] = v.x;
+          rr[4 * u + 1] = v.y;
+          rr[4 * u + 2] = v.z;
+          rr[4 * u + 3] = v.w;
         }
         tmem_st32(tmem + lanebase + kColQ + 32 * c, rr);
-        if (c + 1 < kQTmemDims / 64) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) cur[u] = nxt[u];
-        }
       }
+      uint32_t rr[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        rr[4 * u + 0] = qv[u].x;
+        rr[4 * u + 1] = qv[u].y;
+        rr[4 * u + 2] = qv[u].z;
+        rr[4 * u + 3] = qv[u].w;
+      }
+      tmem_st32(tmem + lanebase + kColQ + 32 * kQStageAtoms, rr);
+      if (!qok) raise_error(kErrTimeout);
       tc_fence_before();
       mbar_arrive(Q_TMEM);
     }
@@ -377,20 +413,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) raise_error(kErrTimeout);
     if (ok) ok = mbar_wait(PV_DONE, (ntiles - 1) & 1);
     tc_fence_after();
-    // epilogue: O / l -> Mid_O, log-sum-exp -> Mid_LSE
+    // epilogue: O / l -> Mid_O, log-sum-exp -> Mid_LSE.  Each thread owns
+    // one head's 1 KB row of Mid_O; it stages the row in shared memory (the
+    // key stages are idle once the last P V is done) and writes it with one
+    // bulk copy, instead of 64 scattered 16-byte stores per thread.
     const float inv = (ok && lrun > 0.f) ? 1.f / lrun : 0.f;
-    float* dst = out_base + static_cast<long long>(live ? h : 0) * S * kVDim;
+    // Row pitch 1040 B: eight consecutive threads' 16-byte stores hit
+    // distinct banks.
+    const uint32_t orow = sbase + kOffStage + static_cast<uint32_t>(h) * kORowPitch;
+    uint8_t* orow_p = smem + kOffStage + h * kORowPitch;
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       uint32_t o[32];
       tmem_ld32(tmem + lanebase + kColO + 32 * c, o);
-      if (live) {
-        float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+      float4* d4 = reinterpret_cast<float4*>(orow_p + 128 * c);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          d4[u] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
-                              __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
-      }
+      for (int u = 0; u < 8; ++u)
+        d4[u] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                            __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+    }
+    if (live) {
+      fence_proxy_async_smem();   // generic-proxy writes -> bulk-copy reads
+      bulk_store(out_base + static_cast<long long>(h) * S * kVDim, orow, 256 * 4);
+      bulk_commit();
+      bulk_wait_read_all();
     }
     if (live && half == 0)
       p.mid_lse[(static_cast<long long>(t) * H + h) * S + split] =
@@ -408,17 +454,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
-  CUtensorMap tq;
+  CUtensorMap tq, tkv;
   const uint64_t qrows = static_cast<uint64_t>(a.batch) * a.nq * a.heads;
   if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kLatentDim, qrows,
                       kLatentDim * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // One latent row per box row; gather4 takes four row coordinates per copy.
+  if (!encode_tmap_2d(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kLatentDim,
+                      static_cast<uint64_t>(a.num_pages) * kPage, kLatentDim * 2, 64, 1,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.num_splits, a.batch * a.nq);
-  sparse_mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, a);
-  return cudaGetLastError();
+  return launch_kernel(sparse_mla_kernel, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0,
+                       tq, tkv, a);
 }
 
 }  // namespace dsa

@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int res[2];
   __shared__ int s_info[8];   // nsel, ncand, base, cbase, last, emit, sub count
 
+  // Everything this kernel reads may come from the kernel before it.
+  grid_dep_wait();
+  grid_dep_launch();
   const int t = blockIdx.y;
   const int k = p.k;
   const int vis = visible(p.seqlens, t, p.nq);
@@ -444,8 +447,8 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  topk_select_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(topk_select_kernel, grid, dim3(kThreads), kSmemBytes, stream,
+                       a.pdl != 0 && a.hist_ready, a);
 }
 
 // ---------------------------------------------------------------------------
