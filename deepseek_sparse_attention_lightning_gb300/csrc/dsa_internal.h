@@ -17,7 +17,15 @@ constexpr int kPage = 64;
 constexpr int kHistBins = 2048;     // top 11 bits of the order-preserving score key
 constexpr int kHistShift = 21;
 constexpr int kTopkChunk = 8192;    // logits per CTA in the top-k passes
-constexpr int kCounterWords = 4;    // per query row: selected, candidates, ticket, spare
+constexpr int kTopkMaxChunks = 256; // chunks per row: rows of up to 2^21 scores
+
+// Top-k control words of one query row: [0] ticket, [1..3] spare,
+// [4 + c] candidate count of chunk c.
+__host__ __device__ constexpr int topk_ctl_words(int64_t ld) {
+  return 4 + static_cast<int>((ld + kTopkChunk - 1) / kTopkChunk);
+}
+// Selection bitmap words of one query row.
+__host__ __device__ constexpr int64_t topk_bitmap_words(int64_t ld) { return (ld + 31) / 32; }
 
 struct IndexerLaunch {
   const uint8_t* q_fp8;
@@ -40,15 +48,11 @@ struct TopkLaunch {
   int64_t ld;
   int32_t* out;         // [T][k]
   uint32_t* hist;       // [T][kHistBins], zeroed (or filled by the indexer)
-  uint32_t* counters;   // [T][kCounterWords], zeroed
-  uint2* cand;          // [T][ld]
+  uint32_t* counters;   // [T][topk_ctl_words(ld)], zeroed
+  uint2* cand;          // [T][ld]: chunk c's candidates at [c * kTopkChunk, ...)
+  uint32_t* bitmap;     // [T][topk_bitmap_words(ld)]: the selection, one bit per position
   int batch, nq, k;
   int hist_ready;       // 1: hist already holds the row histograms
-  // Optional fused index -> cache-row transform: rows[t][i] = the cache row
-  // of out[t][i] (-1 where out is -1).
-  int32_t* rows;        // [T][k] or nullptr
-  const int32_t* page_table;
-  int max_pages, num_pages;
   int pdl;              // 1: launched as a programmatic dependent of the indexer
 };
 
@@ -56,7 +60,6 @@ struct MlaLaunch {
   const uint16_t* q;
   const uint16_t* kv;
   const int32_t* topk_idx;
-  const int32_t* rows;  // optional: cache rows of topk_idx (from the fused top-k)
   const int32_t* seqlens;
   const int32_t* page_table;
   float* mid_o;

@@ -176,43 +176,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     Q_STAGE, policy_evict_last());
     }
     // Resolve every position of the split first (logical index -> page table
-    // -> cache row), 8 x 32 positions per batch so the loads overlap; the
-    // three warps take alternate batches.
+    // -> cache row).  Groups of 32 positions go round-robin to the three
+    // warps, 8 groups per batch so the loads overlap.
     const int npos = ntiles * kBN;
-    if (p.rows) {
-      // The fused top-k already translated positions to cache rows.
-      const int* rrow = p.rows + static_cast<long long>(t) * k;
-      for (int b0 = lw * 256; b0 < npos; b0 += kLoaderWarps * 256) {
-        int rv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int pos = start + b0 + 32 * u + lane;
-          rv[u] = (b0 + 32 * u < npos && pos < end) ? __ldg(rrow + pos) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = b0 + 32 * u;
-          if (i >= npos) break;
-          const bool valid = rv[u] >= 0 && rv[u] < p.num_pages * kPage;
-          rows_s[i + lane] = valid ? rv[u] : safe_row;
-          const uint32_t m = __ballot_sync(0xffffffffu, valid);
-          if (lane == 0) mask_s[i >> 5] = m;
-        }
-      }
-    }
-    for (int b0 = lw * 256; b0 < npos && !p.rows; b0 += kLoaderWarps * 256) {
+    for (int g0 = lw; 32 * g0 < npos; g0 += kLoaderWarps * 8) {
       int idx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int pos = start + b0 + 32 * u + lane;
-        idx[u] = (b0 + 32 * u < npos && pos < end) ? __ldg(idx_row + pos) : -1;
+        const int i = 32 * (g0 + kLoaderWarps * u);
+        const int pos = start + i + lane;
+        idx[u] = (i < npos && pos < end) ? __ldg(idx_row + pos) : -1;
       }
       int pg[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) pg[u] = (idx[u] >= 0 && idx[u] < vis) ? __ldg(ptab + (idx[u] >> 6)) : -1;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int i = b0 + 32 * u;
+        const int i = 32 * (g0 + kLoaderWarps * u);
         if (i >= npos) break;
         const int pos = start + i + lane;
         if (pos < end && idx[u] >= vis) raise_error(kErrCheck);

@@ -8,14 +8,17 @@
 // Scores are compared through an order-preserving 32-bit key (-0 == +0).
 //   pass 1  histogram of the top 11 key bits per row (fused into the indexer
 //           epilogue on the fused path, else topk_hist_kernel);
-//   pass 2  topk_select_kernel, many CTAs per row: finds the bin b* where the
-//           count from the top crosses k, writes every position above b*
-//           straight to the output and appends the positions in b* to a
-//           candidate list; the last CTA of the row (ticket counter) resolves
-//           the candidates with two more radix levels over the remaining 21
-//           key bits and, for exact ties, a radix select over the position,
-//           then rewrites the row in ascending position order through a
-//           shared-memory bitmap.
+//   pass 2  topk_select_kernel, one CTA per 8192 positions of a row: finds the
+//           bin b* where the count from the top crosses k, marks every
+//           position above b* in the row's selection bitmap (one bit per
+//           position, written without atomics: each thread owns 16
+//           consecutive positions) and stores the positions in b* as
+//           candidates in its chunk's own slice of the candidate list; the
+//           last CTA of the row (ticket counter) resolves the candidates with
+//           more radix levels over the remaining 21 key bits and, for exact
+//           ties, a radix select over the position, sets the winners' bits,
+//           and writes the row in ascending position order by a scan of the
+//           bitmap.
 #include <mutex>
 
 #include "dsa.h"
@@ -28,26 +31,34 @@ namespace dsa {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kSelMax = 2048;                         // positions above b* per chunk < k
-constexpr int kPairMax = 1024;                        // sub-candidates ranked pairwise (fit in ssel)
+constexpr int kPer = kTopkChunk / kThreads;           // consecutive positions per thread
+constexpr int kPairMax = 1024;                        // sub-candidates ranked pairwise
 constexpr int kOffHist = 0;                           // 2048 x u32
-constexpr int kOffSel = kOffHist + kHistBins * 4;     // 2048 x i32
-constexpr int kOffCand = kOffSel + kSelMax * 4;       // kTopkChunk x uint2
-constexpr int kSmemBytes = kOffCand + kTopkChunk * 8; // 80 KB, reused as the bitmap
-constexpr int kBitmapWords = kSmemBytes / 4;
+constexpr int kOffCand = kOffHist + kHistBins * 4;    // kTopkChunk x uint2
+constexpr int kOffSub = kOffCand + kTopkChunk * 8;    // kPairMax x uint2
+constexpr int kSmemBytes = kOffSub + kPairMax * 8;    // 80 KB
+static_assert(kPer == 16, "a thread pair fills one 32-bit bitmap word");
 
 __device__ __forceinline__ int visible(const int32_t* seqlens, int t, int nq) {
   return seqlens[t / nq] - (nq - 1 - t % nq);
 }
 
-// Cache row of logical position s of request r (-1 if its page id is bad).
-__device__ __forceinline__ int phys_row(const TopkLaunch& p, int r, int s) {
-  const int pg = p.page_table[static_cast<long long>(r) * p.max_pages + (s >> 6)];
-  if (pg < 0 || pg >= p.num_pages) {
-    raise_error(kErrCheck);
-    return -1;
+// Index of the n-th (0-based) set bit of m (m has more than n set bits).
+__device__ __forceinline__ int nth_set_bit(uint32_t m, int n) {
+  int pos = 0;
+#pragma unroll
+  for (int width = 16; width > 0; width >>= 1) {
+    const uint32_t low = m & ((1u << width) - 1u);
+    const int c = __popc(low);
+    if (n >= c) {
+      n -= c;
+      m >>= width;
+      pos += width;
+    } else {
+      m = low;
+    }
   }
-  return pg * kPage + (s & (kPage - 1));
+  return pos;
 }
 
 // Exclusive scan of one value per thread over a 512-thread block.
@@ -137,11 +148,12 @@ __global__ void __launch_bounds__(kThreads)
     topk_select_kernel(const TopkLaunch p) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* sh = reinterpret_cast<uint32_t*>(smem + kOffHist);
-  int* ssel = reinterpret_cast<int*>(smem + kOffSel);
   uint2* scand = reinterpret_cast<uint2*>(smem + kOffCand);
+  uint2* sub = reinterpret_cast<uint2*>(smem + kOffSub);
   __shared__ uint32_t scratch[40];
   __shared__ int res[2];
-  __shared__ int s_info[8];   // nsel, ncand, base, cbase, last, emit, sub count
+  __shared__ int s_info[4];   // candidates of this CTA, last flag, winners, sub count
+  __shared__ int s_pref[kTopkMaxChunks + 1];
 
   // Everything this kernel reads may come from the kernel before it.
   grid_dep_wait();
@@ -149,142 +161,152 @@ __global__ void __launch_bounds__(kThreads)
   const int t = blockIdx.y;
   const int k = p.k;
   const int vis = visible(p.seqlens, t, p.nq);
+  const int lane = threadIdx.x & 31;
   int32_t* out_row = p.out + static_cast<long long>(t) * k;
 
-  const int req = t / p.nq;
   if (vis <= k) {
     // Every visible token is selected (the short-context case).
-    if (blockIdx.x == 0) {
-      int32_t* rows_row = p.rows ? p.rows + static_cast<long long>(t) * k : nullptr;
-      for (int i = threadIdx.x; i < k; i += kThreads) {
-        out_row[i] = i < vis ? i : -1;
-        if (rows_row) {
-          const int row = i < vis ? phys_row(p, req, i) : -1;
-          rows_row[i] = row;
-        }
-      }
-    }
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i < k; i += kThreads) out_row[i] = i < vis ? i : -1;
     return;
   }
   const int nch = (vis + kTopkChunk - 1) / kTopkChunk;
-  if (static_cast<int>(blockIdx.x) >= nch) return;
-  uint32_t* counters = p.counters + static_cast<long long>(t) * kCounterWords;
+  const int x = blockIdx.x;
+  if (x >= nch) return;
+  uint32_t* ctl = p.counters + static_cast<long long>(t) * topk_ctl_words(p.ld);
   uint2* cand_row = p.cand + static_cast<long long>(t) * p.ld;
+  uint32_t* bm_row = p.bitmap + static_cast<long long>(t) * topk_bitmap_words(p.ld);
 
-  // ---- this CTA's chunk of the row: all of a thread's scores are loaded
-  //      first (one latency), then the row histogram.
+  // ---- this CTA's chunk: 16 consecutive scores per thread (through L1: a
+  //      warp's four 16-byte loads share their cache lines), loaded before
+  //      the row histogram (one latency for both).
   const float* row = p.logits + static_cast<long long>(t) * p.ld;
-  const int lo = blockIdx.x * kTopkChunk;
+  const int lo = x * kTopkChunk;
   const int hi = min(vis, lo + kTopkChunk);
-  constexpr int kIters = kTopkChunk / (4 * kThreads);
-  float x[kIters][4];
+  const int s0 = lo + kPer * static_cast<int>(threadIdx.x);
+  float v[kPer];
+  if (s0 + kPer <= hi) {
 #pragma unroll
-  for (int q = 0; q < kIters; ++q) {
-    const int s = lo + q * 4 * kThreads + 4 * static_cast<int>(threadIdx.x);
-    if (s + 3 < hi) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(row + s));
-      x[q][0] = v.x; x[q][1] = v.y; x[q][2] = v.z; x[q][3] = v.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[q][e] = s + e < hi ? __ldcg(row + s + e) : 0.f;
+    for (int q = 0; q < kPer / 4; ++q) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + s0) + q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
     }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) v[j] = s0 + j < hi ? __ldg(row + s0 + j) : 0.f;
   }
-  // ---- threshold bin b*: the count of scores in bins above it is < k and
-  //      reaches k with it.
   const uint32_t* gh = p.hist + static_cast<long long>(t) * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = __ldcg(gh + i);
+  if (threadIdx.x == 0) s_info[0] = 0;
   __syncthreads();
+  // ---- threshold bin b*: the count of scores in bins above it (nabove) is
+  //      < k and reaches k with it.
   find_crossing(sh, static_cast<uint32_t>(k), true, res, scratch);
   const int bstar = res[0];
+  const int nabove = res[1];
   if (bstar < 0) {  // histogram inconsistent with the row
     if (threadIdx.x == 0) raise_error(kErrCheck);
     return;
   }
   const uint32_t ub = static_cast<uint32_t>(bstar);
-  // Classify the thread's scores, then place them with one block scan of the
-  // packed (candidates << 16 | selected) counts.
   uint32_t above = 0, inbin = 0;
 #pragma unroll
-  for (int q = 0; q < kIters; ++q) {
-    const int s = lo + q * 4 * kThreads + 4 * static_cast<int>(threadIdx.x);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t bin = float_key(x[q][e]) >> kHistShift;
-      const uint32_t bit = 1u << (4 * q + e);
-      if (s + e < hi) {
-        if (bin > ub) above |= bit;
-        else if (bin == ub) inbin |= bit;
-      }
+  for (int j = 0; j < kPer; ++j) {
+    if (s0 + j < hi) {
+      const uint32_t bin = float_key(v[j]) >> kHistShift;
+      if (bin > ub) above |= 1u << j;
+      else if (bin == ub) inbin |= 1u << j;
     }
   }
-  const uint32_t mine = (static_cast<uint32_t>(__popc(inbin)) << 16) | __popc(above);
-  const uint32_t off = block_excl_scan_512(mine, scratch);
-  if (threadIdx.x == kThreads - 1) {
-    s_info[0] = static_cast<int>((off + mine) & 0xFFFFu);
-    s_info[1] = static_cast<int>((off + mine) >> 16);
-  }
-  {
-    int oa = static_cast<int>(off & 0xFFFFu), oc = static_cast<int>(off >> 16);
+  // Positions above b* -> the bitmap: threads 2w and 2w+1 fill word w of the
+  // chunk (every word of [lo, hi) is written, so the bitmap needs no clear).
+  const uint32_t upper = __shfl_down_sync(0xffffffffu, above, 1);
+  if ((threadIdx.x & 1) == 0 && s0 < hi) bm_row[s0 >> 5] = above | (upper << 16);
+  // Positions in b* -> this chunk's slice of the candidate list.
+  const int mine = __popc(inbin);
+  int incl = mine;
 #pragma unroll
-    for (int q = 0; q < kIters; ++q) {
-      const int s = lo + q * 4 * kThreads + 4 * static_cast<int>(threadIdx.x);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t bit = 1u << (4 * q + e);
-        if (above & bit) {
-          if (oa < kSelMax) ssel[oa] = s + e;
-          ++oa;
-        } else if (inbin & bit) {
-          scand[oc++] = make_uint2(float_key(x[q][e]), static_cast<uint32_t>(s + e));
-        }
-      }
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  __syncthreads();
-  const int nsel = s_info[0], ncand = s_info[1];
-  if (threadIdx.x == 0) {
-    if (nsel > kSelMax) raise_error(kErrCheck);
-    // One 64-bit atomic reserves room in both lists: (candidates, selected).
-    const unsigned long long add =
-        (static_cast<unsigned long long>(ncand) << 32) | static_cast<unsigned long long>(nsel);
-    const unsigned long long old =
-        atomicAdd(reinterpret_cast<unsigned long long*>(counters), add);
-    s_info[2] = static_cast<int>(old & 0xFFFFFFFFull);
-    s_info[3] = static_cast<int>(old >> 32);
-  }
-  __syncthreads();
+  int wbase = 0;
+  if (lane == 31) wbase = atomicAdd(&s_info[0], incl);
+  wbase = __shfl_sync(0xffffffffu, wbase, 31);
   {
-    const int base = s_info[2], cbase = s_info[3];
-    const int nw = min(nsel, kSelMax);
-    for (int i = threadIdx.x; i < nw; i += kThreads)
-      if (base + i < k) out_row[base + i] = ssel[i];
-    for (int i = threadIdx.x; i < ncand; i += kThreads) cand_row[cbase + i] = scand[i];
+    int pos = lo + wbase + incl - mine;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if ((inbin >> j) & 1u) cand_row[pos++] = make_uint2(float_key(v[j]), static_cast<uint32_t>(s0 + j));
   }
   // The barrier orders the block's writes before thread 0's release fence;
   // the last CTA's acquire fence then sees every CTA's writes.
   __syncthreads();
   if (threadIdx.x == 0) {
+    ctl[4 + x] = static_cast<uint32_t>(s_info[0]);
     __threadfence();
-    const uint32_t ticket = atomicAdd(counters + 2, 1u);
+    const uint32_t ticket = atomicAdd(ctl, 1u);
     const bool last = ticket == static_cast<uint32_t>(nch - 1);
     if (last) __threadfence();
-    s_info[4] = last ? 1 : 0;
+    s_info[1] = last ? 1 : 0;
   }
   __syncthreads();
-  if (!s_info[4]) return;
+  if (!s_info[1]) return;
 
-  // ---- last CTA of the row: resolve the candidates of bin b*.
-  const int nabove = static_cast<int>(__ldcg(counters + 0));
-  const int nc = static_cast<int>(__ldcg(counters + 1));
+  // ---- last CTA of the row: gather the candidates of bin b*.
+  {
+    const uint32_t c = threadIdx.x < static_cast<unsigned>(nch) ? __ldcg(ctl + 4 + threadIdx.x) : 0u;
+    const uint32_t e = block_excl_scan_512(c, scratch);
+    if (threadIdx.x <= static_cast<unsigned>(nch)) s_pref[threadIdx.x] = static_cast<int>(e);
+  }
+  if (threadIdx.x == 0) { s_info[2] = 0; s_info[3] = 0; }
+  __syncthreads();
+  const int nc = s_pref[nch];
+  if (static_cast<uint32_t>(nc) != sh[ub]) {   // candidates disagree with the histogram
+    if (threadIdx.x == 0) raise_error(kErrCheck);
+    return;
+  }
+  // Candidate e lives in chunk c (s_pref[c] <= e < s_pref[c + 1]).
+  auto chunk_of = [&](int e) -> int {
+    int a = 0, b = nch - 1;
+    while (a < b) {
+      const int m = (a + b + 1) >> 1;
+      if (s_pref[m] <= e) a = m; else b = m - 1;
+    }
+    return a;
+  };
+  const bool in_smem = nc <= kTopkChunk;
+  auto cget = [&](int e) -> uint2 {
+    if (in_smem) return scand[e];
+    const int c = chunk_of(e);
+    return __ldcg(cand_row + static_cast<long long>(c) * kTopkChunk + (e - s_pref[c]));
+  };
+  if (in_smem) {
+    // Four loads in flight per thread, then their four stores.
+    for (int e0 = threadIdx.x; e0 < nc; e0 += 4 * kThreads) {
+      uint2 cv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kThreads;
+        if (e < nc) {
+          const int c = chunk_of(e);
+          cv[u] = __ldcg(cand_row + static_cast<long long>(c) * kTopkChunk + (e - s_pref[c]));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (e0 + u * kThreads < nc) scand[e0 + u * kThreads] = cv[u];
+    }
+    __syncthreads();
+  }
+  // A winner's bit goes into the bitmap (the CTAs that wrote it are done).
+  auto take = [&](uint32_t s) {
+    atomicOr(bm_row + (s >> 5), 1u << (s & 31));
+    atomicAdd(&s_info[2], 1);
+  };
+
+  // ---- resolve: the need best candidates by (key desc, position asc).
   const uint32_t need = static_cast<uint32_t>(k - nabove);
-  const uint2* cp = cand_row;
-  if (nc <= kTopkChunk) {
-    for (int i = threadIdx.x; i < nc; i += kThreads) scand[i] = __ldcg(cand_row + i);
-    cp = scand;
-  }
-  if (threadIdx.x == 0) s_info[5] = 0;
-  __syncthreads();
-
   uint32_t kprefix = ub << kHistShift, kmask = 0xFFFFFFFFu << kHistShift;
   uint32_t need_l = need;
   uint32_t cnt_eq = 0;
@@ -298,7 +320,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
     __syncthreads();
     for (int e = threadIdx.x; e < nc; e += kThreads) {
-      const uint32_t key = cp[e].x;
+      const uint32_t key = cget(e).x;
       if ((key & kmask) == kprefix) atomicAdd(&sh[(key >> sh_) & dm], 1u);
     }
     __syncthreads();
@@ -325,22 +347,15 @@ __global__ void __launch_bounds__(kThreads)
     // Candidates whose digit is above the crossing one are in; of those with
     // the crossing digit (m <= kPairMax), the need_l best by (key desc,
     // position asc) are in.
-    uint2* sub = reinterpret_cast<uint2*>(ssel);
-    if (threadIdx.x == 0) s_info[6] = 0;
-    __syncthreads();
     const uint32_t hi_digits = kprefix >> 10;
     for (int e = threadIdx.x; e < nc; e += kThreads) {
-      const uint2 c = cp[e];
+      const uint2 c = cget(e);
       const uint32_t cd = c.x >> 10;
-      if (cd > hi_digits) {
-        const int pos = atomicAdd(&s_info[5], 1);
-        if (nabove + pos < k) out_row[nabove + pos] = static_cast<int>(c.y);
-      } else if (cd == hi_digits) {
-        sub[atomicAdd(&s_info[6], 1)] = c;
-      }
+      if (cd > hi_digits) take(c.y);
+      else if (cd == hi_digits) sub[atomicAdd(&s_info[3], 1)] = c;
     }
     __syncthreads();
-    const int m = s_info[6];
+    const int m = s_info[3];
     for (int i = threadIdx.x; i < m; i += kThreads) {
       const uint2 ci = sub[i];
       uint32_t rank = 0;
@@ -348,10 +363,7 @@ __global__ void __launch_bounds__(kThreads)
         const uint2 cj = sub[j2];
         rank += (cj.x > ci.x || (cj.x == ci.x && cj.y < ci.y)) ? 1u : 0u;
       }
-      if (rank < need_l) {
-        const int pos = atomicAdd(&s_info[5], 1);
-        if (nabove + pos < k) out_row[nabove + pos] = static_cast<int>(ci.y);
-      }
+      if (rank < need_l) take(ci.y);
     }
   } else {
     const uint32_t kstar = kprefix;
@@ -367,7 +379,7 @@ __global__ void __launch_bounds__(kThreads)
         for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
         __syncthreads();
         for (int e = threadIdx.x; e < nc; e += kThreads) {
-          const uint2 c = cp[e];
+          const uint2 c = cget(e);
           if (c.x == kstar && (c.y & imask) == iprefix) atomicAdd(&sh[(c.y >> sh_) & dm], 1u);
         }
         __syncthreads();
@@ -385,51 +397,50 @@ __global__ void __launch_bounds__(kThreads)
       return;
     }
     for (int e = threadIdx.x; e < nc; e += kThreads) {
-      const uint2 c = cp[e];
-      if (c.x > kstar || (c.x == kstar && c.y <= istar)) {
-        const int pos = atomicAdd(&s_info[5], 1);
-        if (nabove + pos < k) out_row[nabove + pos] = static_cast<int>(c.y);
-      }
+      const uint2 c = cget(e);
+      if (c.x > kstar || (c.x == kstar && c.y <= istar)) take(c.y);
     }
   }
-  __threadfence_block();
+  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0 && nabove + s_info[5] != k) raise_error(kErrCheck);
+  if (threadIdx.x == 0 && nabove + s_info[2] != k) raise_error(kErrCheck);
 
-  // ---- rewrite the row in ascending position order through a bitmap.
+  // ---- the row in ascending position order from the bitmap, staged in
+  //      shared memory (the candidate buffer) in slices of 8192 words with
+  //      their exclusive bit-count prefix.  Output j is then found by a
+  //      binary search over the prefix, so every thread writes about k / 512
+  //      outputs however the selected bits cluster.
   const int nwords = (vis + 31) >> 5;
-  if (nwords <= kBitmapWords) {
-    uint32_t* bm = reinterpret_cast<uint32_t*>(smem);
-    for (int i = threadIdx.x; i < nwords; i += kThreads) bm[i] = 0u;
+  uint32_t* sbm = reinterpret_cast<uint32_t*>(smem + kOffCand);
+  constexpr int kSlice = kTopkChunk;       // words: bitmap + prefix = the 64 KB buffer
+  uint32_t* spre = sbm + kSlice;
+  uint32_t base = 0;
+  for (int c0 = 0; c0 < nwords; c0 += kSlice) {
+    const int cn = min(kSlice, nwords - c0);
+    __syncthreads();   // the previous slice (or the candidates) is no longer read
+    for (int i = threadIdx.x; i < cn; i += kThreads) sbm[i] = __ldcg(bm_row + c0 + i);
     __syncthreads();
-    for (int i = threadIdx.x; i < k; i += kThreads) {
-      const int s = __ldcg(out_row + i);
-      if (s >= 0 && s < vis) atomicOr(&bm[s >> 5], 1u << (s & 31));
-    }
-    __syncthreads();
-    const int per = (nwords + kThreads - 1) / kThreads;
-    const int w0 = min(nwords, threadIdx.x * per), w1 = min(nwords, w0 + per);
+    const int per = (cn + kThreads - 1) / kThreads;
+    const int w0 = min(cn, static_cast<int>(threadIdx.x) * per), w1 = min(cn, w0 + per);
     uint32_t cnt = 0;
-    for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
-    uint32_t pos = block_excl_scan_512(cnt, scratch);
+    for (int w = w0; w < w1; ++w) cnt += __popc(sbm[w]);
+    uint32_t run = block_excl_scan_512(cnt, scratch);
+    const uint32_t total = scratch[16 + 15];   // inclusive sum over the block
     for (int w = w0; w < w1; ++w) {
-      uint32_t bits = bm[w];
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (pos < static_cast<uint32_t>(k)) out_row[pos] = w * 32 + b;
-        ++pos;
-      }
+      spre[w] = run;
+      run += __popc(sbm[w]);
     }
-  }
-  if (p.rows) {
-    // Fused index -> cache-row transform of the final selection.
     __syncthreads();
-    int32_t* rows_row = p.rows + static_cast<long long>(t) * k;
-    for (int i = threadIdx.x; i < k; i += kThreads) {
-      const int s = __ldcg(out_row + i);
-      rows_row[i] = (s >= 0 && s < vis) ? phys_row(p, req, s) : -1;
+    for (uint32_t j = threadIdx.x; j < total; j += kThreads) {
+      int a = 0, b = cn - 1;   // the last word whose prefix is <= j holds output j
+      while (a < b) {
+        const int m = (a + b + 1) >> 1;
+        if (spre[m] <= j) a = m; else b = m - 1;
+      }
+      if (base + j < static_cast<uint32_t>(k))
+        out_row[base + j] = (c0 + a) * 32 + nth_set_bit(sbm[a], static_cast<int>(j - spre[a]));
     }
+    base += total;
   }
 }
 
@@ -438,6 +449,7 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   const int T = a.batch * a.nq;
   const int chunks = static_cast<int>((a.ld + kTopkChunk - 1) / kTopkChunk);
+  if (chunks > kTopkMaxChunks) return cudaErrorInvalidValue;
   dim3 grid(chunks > 0 ? chunks : 1, T);
   if (!a.hist_ready) {
     topk_hist_kernel<<<grid, kThreads, 0, stream>>>(a);
@@ -455,8 +467,8 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
 // Top-k without a caller-provided workspace (dsa_topk_noalloc).
 //
 // For callers that cannot allocate device memory at the point where they run
-// the selection, the histogram, counters and candidate lists live in one
-// statically sized device array.  Every GPU that loads the library reserves
+// the selection, the histogram, control words, candidate lists and selection
+// bitmap live in one statically sized device array.  Every GPU that loads the library reserves
 // it (kNoAllocScratchBytes) until the process exits.
 // ---------------------------------------------------------------------------
 namespace {
@@ -465,9 +477,16 @@ constexpr int kNoAllocMaxRows = 64;                 // query rows T
 constexpr long long kNoAllocMaxScores = 1ll << 21;  // T * ld_logits
 constexpr size_t kNoAllocHistBytes = size_t(kNoAllocMaxRows) * kHistBins * 4;
 constexpr size_t kNoAllocCounterOff = kNoAllocHistBytes;
+// Control words: 4 per row plus one per 8192-score chunk, over all rows at
+// most 4 T + T + 2^21 / 8192 words.
+constexpr size_t kNoAllocCounterWords =
+    size_t(kNoAllocMaxRows) * 5 + size_t(kNoAllocMaxScores) / kTopkChunk;
 constexpr size_t kNoAllocCandOff =
-    (kNoAllocCounterOff + size_t(kNoAllocMaxRows) * kCounterWords * 4 + 255) & ~size_t(255);
-constexpr size_t kNoAllocScratchBytes = kNoAllocCandOff + size_t(kNoAllocMaxScores) * 8;
+    (kNoAllocCounterOff + kNoAllocCounterWords * 4 + 255) & ~size_t(255);
+constexpr size_t kNoAllocBitmapOff = kNoAllocCandOff + size_t(kNoAllocMaxScores) * 8;
+// Bitmap: ceil(ld / 32) words per row, at most 2^21 / 32 + T words.
+constexpr size_t kNoAllocScratchBytes =
+    kNoAllocBitmapOff + (size_t(kNoAllocMaxScores) / 32 + kNoAllocMaxRows) * 4;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -528,6 +547,7 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_decode_desc* d, const float* lo
   a.hist = reinterpret_cast<uint32_t*>(base);
   a.counters = reinterpret_cast<uint32_t*>(base + kNoAllocCounterOff);
   a.cand = reinterpret_cast<uint2*>(base + kNoAllocCandOff);
+  a.bitmap = reinterpret_cast<uint32_t*>(base + kNoAllocBitmapOff);
   a.batch = d->batch; a.nq = d->q_per_req; a.k = d->topk; a.hist_ready = 0;
   return launch_topk(a, s) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

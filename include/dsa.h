@@ -148,7 +148,7 @@ size_t dsa_topk_workspace_bytes(const dsa_decode_desc* desc, int64_t ld_logits);
  * the engine has reserved all of the device's memory for its caches, or a
  * host runtime without a device allocator of its own, where a cudaMalloc
  * would fail or stall the device.  The histogram, counters and candidate
- * lists then live in a file-scope device array of fixed size (about 16.5 MB)
+ * lists then live in a file-scope device array of fixed size (about 16.8 MB)
  * that every GPU loading this library reserves until the process exits.  No
  * call allocates or frees memory.
  *   Limits: T = batch * q_per_req <= 64 and T * ld_logits <= 2^21 scores;
