@@ -15,16 +15,19 @@
 // in a shared-memory histogram of the top 11 key bits (the first top-k pass).
 //
 // Warp roles (384 threads, one persistent CTA per SM):
-//   warp 0, lane 0  TMA producer: one 8 KB box per page into an 8-stage ring,
-//            and the request's FP8 queries (double-buffered) when the request
-//            changes.  It issues nothing else, because every TMA instruction
-//            costs ~100 cycles to issue: two per 16 KB tile keep a SM's ring
-//            full at HBM speed.
+//   warp 0, lane 0  TMA producer: one 8 KB box per page into a ring of 5-12
+//            stages (as many as shared memory holds next to the fixed
+//            buffers), and the request's FP8 queries (double-buffered) when
+//            the request changes.  It issues nothing else: a TMA instruction
+//            costs its issuing thread ~100-170 cycles.
 //   warps 1, 2  MMA issuers (one thread each, alternate tiles); warp 1 owns
 //            TMEM;
 //   warps 4-7, 8-11  two epilogue groups taking alternate tiles (one thread
-//            per TMEM lane / token), each with its own accumulator buffer; each
-//            thread loads its token's key scale three of its tiles ahead.
+//            per TMEM lane / token); each thread loads its token's key scale
+//            three of its tiles ahead.
+// Accumulators: four TMEM buffers when they fit (n_q <= 2), else two, so the
+// MMAs of a tile do not wait for the epilogue of the tile two before it (with
+// two buffers that round trip, not HBM, set the pace).
 // The page ids of the CTA's tile range are fetched once, by all threads, into
 // shared memory.  Keys are streamed exactly once per request; every query
 // token of the request is served by the same key tile (N = 64 * n_q).
@@ -54,10 +57,14 @@ struct Cfg {
   // left (up to 12 stages): the ring's bytes in flight set the bandwidth.
   static constexpr int kFixed = 2 * kQBytes + kEpiGroups * NQ * kHistBins * 4 +
                                 kEpiGroups * kN * 4 + kPageWin * 4 + (1024 + 4) * 4 + 64 * 4 +
-                                (2 * 12 + 8) * 8 + 16 + 1024;
+                                (2 * 12 + 4 + 2 * 4) * 8 + 16 + 1024;
   static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
-  static constexpr int kTmemCols = (2 * kN <= 128) ? 128 : ((2 * kN <= 256) ? 256 : 512);
+  // Accumulator buffers: four when they fit in TMEM, so the MMA of a tile
+  // never waits for the epilogue of the tile two before it.
+  static constexpr int kAccBufs = (4 * kN <= 512) ? 4 : 2;
+  static constexpr int kTmemCols =
+      (kAccBufs * kN <= 128) ? 128 : ((kAccBufs * kN <= 256) ? 256 : 512);
   static constexpr int kOffStages = 0;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffHist = kOffQ + 2 * kQBytes;
@@ -66,7 +73,7 @@ struct Cfg {
   static constexpr int kOffPrefix = kOffPages + kPageWin * 4;
   static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 4) * 4;
   static constexpr int kOffBar = kOffScratch + 64 * 4;
-  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccBufs;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffTmemSlot + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory");
@@ -147,10 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define Q_FULL(b) (bar0 + 8u * (2 * C::kStages + (b)))
 #define Q_EMPTY(b) (bar0 + 8u * (2 * C::kStages + 2 + (b)))
 #define ACC_FULL(b) (bar0 + 8u * (2 * C::kStages + 4 + (b)))
-#define ACC_EMPTY(b) (bar0 + 8u * (2 * C::kStages + 6 + (b)))
+#define ACC_EMPTY(b) (bar0 + 8u * (2 * C::kStages + 4 + C::kAccBufs + (b)))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.batch;
+  if (threadIdx.x == 0) {   // descriptor fetches overlap the prologue's loads
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_q);
+  }
 
   // Tiles per request (requests whose every query selects all tokens are
   // skipped when asked), then their prefix sums.
@@ -186,6 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(Q_FULL(b), 1);
       mbar_init(Q_EMPTY(b), 2);   // one commit per MMA issuer
+    }
+    for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(ACC_FULL(b), 1);
       mbar_init(ACC_EMPTY(b), 128);
     }
@@ -223,8 +236,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && g0 < g1) {
-      prefetch_tmap(&tmap_k);
-      prefetch_tmap(&tmap_q);
       const uint64_t pol_k = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
       int r = 0, cur = -1, seg = -1;
@@ -295,8 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t st = it % C::kStages;
         if (!mbar_wait(KV_FULL(st), (it / C::kStages) & 1)) { ok = false; break; }
-        const uint32_t ab = it & 1;
-        if (it >= 2 && !mbar_wait(ACC_EMPTY(ab), ((it >> 1) - 1) & 1)) { ok = false; break; }
+        const uint32_t ab = it % C::kAccBufs;
+        if (it >= C::kAccBufs && !mbar_wait(ACC_EMPTY(ab), ((it / C::kAccBufs) - 1) & 1)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t a0 = sbase + C::kOffStages + st * kStageBytes;
         const uint32_t b0 = sbase + C::kOffQ + (seg & 1) * C::kQBytes;
@@ -312,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (seg >= 0) tc_commit(Q_EMPTY(seg & 1));
       if (!ok) raise_error(kErrTimeout);
-      if (last >= 0) mbar_wait(ACC_FULL(last & 1), (last >> 1) & 1);
+      if (last >= 0) mbar_wait(ACC_FULL(last % C::kAccBufs), (last / C::kAccBufs) & 1);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
@@ -375,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       sk0 = sk1;
       sk1 = sk2;
       sk2 = scale_of(g + kScaleAhead * kEpiGroups);
-      const uint32_t ab = it & 1;
-      if (!mbar_wait(ACC_FULL(ab), (it >> 1) & 1)) { ok = false; break; }
+      const uint32_t ab = it % C::kAccBufs;
+      if (!mbar_wait(ACC_FULL(ab), (it / C::kAccBufs) & 1)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tl = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + ab * C::kN;
 #pragma unroll 1
