@@ -78,19 +78,31 @@ cudaError_t launch_merge(int rows, int splits, const float* mid_o, const float* 
 // Launches `kern` on `s`; with `pdl` as a programmatic dependent of the
 // previous kernel of the stream (the kernel then calls grid_dep_wait before it
 // reads anything that kernel wrote).
+// `cluster_x` > 1 groups consecutive CTAs along x into clusters of that size.
 template <typename... Exp, typename... Act>
 cudaError_t launch_kernel(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem,
-                          cudaStream_t s, bool pdl, Act&&... args) {
+                          cudaStream_t s, bool pdl, int cluster_x, Act&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Act&&>(args)...);
 }
 

@@ -76,7 +76,7 @@ cudaError_t launch_merge(int rows, int splits, const float* mid_o, const float* 
   if (rows <= 0) return cudaSuccess;
   const long long threads = static_cast<long long>(rows) * kVec;
   const int grid = static_cast<int>((threads + kThreads - 1) / kThreads);
-  return launch_kernel(merge_kernel, dim3(grid), dim3(kThreads), 0, stream, pdl, rows, splits,
+  return launch_kernel(merge_kernel, dim3(grid), dim3(kThreads), 0, stream, pdl, 1, rows, splits,
                        mid_o, mid_lse, out, out_lse);
 }
 

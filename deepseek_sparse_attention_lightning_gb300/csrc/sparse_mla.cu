@@ -62,7 +62,7 @@ constexpr int kMaxPos = 2048;                            // positions of one spl
 constexpr int kOffRows = kOffStage + 2 * kStageBytes;    // cache row of every position
 constexpr int kOffMask = kOffRows + kMaxPos * 4;         // validity bits, 32 per word
 constexpr int kOffBar = kOffMask + (kMaxPos / 32) * 4;
-constexpr int kNumBars = 11;
+constexpr int kNumBars = 12;
 constexpr int kQStageAtoms = 4;                            // q dims [0, 256) via stage 1
 constexpr int kOffSlot = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;
@@ -119,7 +119,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
   const uint32_t bar0 = sbase + kOffBar;
   const uint32_t Q_FULL = bar0, Q_TMEM = bar0 + 8, S_FULL = bar0 + 16, S_FREE = bar0 + 24,
-                 P_FULL = bar0 + 32, PV_DONE = bar0 + 40, Q_STAGE = bar0 + 80;
+                 P_FULL = bar0 + 32, PV_DONE = bar0 + 40, Q_STAGE = bar0 + 80,
+                 Q_PEER = bar0 + 88;
+  // The two value halves of a split form a cluster: every key row and query
+  // box is fetched once and multicast to both CTAs.
+  const uint32_t crank = cluster_ctarank(), peer = crank ^ 1u;
+  constexpr uint16_t kBoth = 0x3;
 #define KV_FULL(s) (bar0 + 48u + 8u * (s))
 #define KV_EMPTY(s) (bar0 + 64u + 8u * (s))
 
@@ -131,9 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(P_FULL, 128);
     mbar_init(PV_DONE, 1);
     mbar_init(Q_STAGE, 1);
+    mbar_init(Q_PEER, 1);                         // the peer's softmax read its q staging
     for (int s = 0; s < 2; ++s) {
       mbar_init(KV_FULL(s), kLoaderWarps * 32);   // one expect-tx arrive per loader thread
-      mbar_init(KV_EMPTY(s), 1);
+      mbar_init(KV_EMPTY(s), 2);                  // both CTAs' MMAs done with the stage
     }
     fence_mbar_init();
   }
@@ -145,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   grid_dep_launch();
+  cluster_sync();   // both CTAs' barriers exist before any copy or arrive targets them
 
   if (warp == 0 || warp == 2 || warp == 3) {
     // ------------------------------------------------------------ loaders
@@ -155,26 +162,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ltid = lw * 32 + lane;
     const int* ptab = p.page_table + static_cast<long long>(r) * p.max_pages;
     const int* idx_row = p.topk_idx + static_cast<long long>(t) * k;
-    // The selected positions come from the kernel before (the top-k when
-    // launched as its dependent); the queries, page table and cache do not.
-    grid_dep_wait();
+    // Queries, page table and cache are inputs of the layer; only the
+    // selected positions come from the kernel before (the top-k when this
+    // grid is launched as its dependent), so the query copies start first.
+    if (ltid == 0) {
+      prefetch_tmap(&tmap_q);
+      prefetch_tmap(&tmap_kv);
+      mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
+      mbar_expect_tx(Q_STAGE, kQStageAtoms * kQAtomBytes);
+      const uint64_t pol_q = policy_evict_last();
+      for (int a = static_cast<int>(crank); a < kQSmemAtoms; a += 2)
+        tma_load_2d_mc(sbase + kOffQ + a * kQAtomBytes, &tmap_q, kQTmemDims + 64 * a, t * H, Q_FULL,
+                       kBoth, pol_q);
+      for (int a = static_cast<int>(crank); a < kQStageAtoms; a += 2)
+        tma_load_2d_mc(sbase + kOffStage + kStageBytes + a * kQAtomBytes, &tmap_q, 64 * a, t * H,
+                       Q_STAGE, kBoth, pol_q);
+    }
     int safe_row = 0;
     {
       const int pg0 = ptab[0];
       if (pg0 >= 0 && pg0 < p.num_pages) safe_row = pg0 * kPage;
     }
-    if (ltid == 0) {
-      prefetch_tmap(&tmap_q);
-      prefetch_tmap(&tmap_kv);
-      mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
-      for (int a = 0; a < kQSmemAtoms; ++a)
-        tma_load_2d(sbase + kOffQ + a * kQAtomBytes, &tmap_q, kQTmemDims + 64 * a, t * H, Q_FULL,
-                    policy_evict_last());
-      mbar_expect_tx(Q_STAGE, kQStageAtoms * kQAtomBytes);
-      for (int a = 0; a < kQStageAtoms; ++a)
-        tma_load_2d(sbase + kOffStage + kStageBytes + a * kQAtomBytes, &tmap_q, 64 * a, t * H,
-                    Q_STAGE, policy_evict_last());
-    }
+    grid_dep_wait();
     // Resolve every position of the split first (logical index -> page table
     // -> cache row).  Groups of 32 positions go round-robin to the three
     // warps, 8 groups per batch so the loads overlap.
@@ -215,31 +224,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         raise_error(kErrTimeout);
         break;
       }
-      // Stage 1 holds q dims [0, 256) until the softmax threads moved them.
-      if (it == 1 && !mbar_wait(Q_TMEM, 0)) {
+      // Stage 1 holds q dims [0, 256) until the softmax threads of both CTAs
+      // moved them (tile 1 lands in both).
+      if (it == 1 && !(mbar_wait(Q_TMEM, 0) && mbar_wait(Q_PEER, 0))) {
         raise_error(kErrTimeout);
         break;
       }
       // Copy c = 9 g + a brings rows 4g..4g+3 of the tile, dims [64a, 64a+64),
-      // to atom a at byte 512 g (the copy engine applies the 128B swizzle).
+      // to atom a at byte 512 g of both CTAs (the copy engine applies the 128B
+      // swizzle); this CTA issues the copies c = crank mod 2, 72 loaders one
+      // each.  Every loader announces 1/96 of the tile's bytes.
       const uint32_t dst = sbase + kOffStage + st * kStageBytes;
       const int* rows = rows_s + it * kBN;
-      const int mine = (kGathers - ltid + kLoaderWarps * 32 - 1) / (kLoaderWarps * 32);
-      mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(mine) * 4u * 128u);
-      for (int c = ltid; c < kGathers; c += kLoaderWarps * 32) {
+      mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(kStageBytes / (kLoaderWarps * 32)));
+      const int c = 2 * ltid + static_cast<int>(crank);
+      if (c < kGathers) {
         const int g = c / kAtoms, a = c - g * kAtoms;
         const int* r4 = rows + 4 * g;
-        tma_gather4(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r4[0], r4[1], r4[2], r4[3],
-                    KV_FULL(st), pol_kv);
+        tma_gather4_mc(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r4[0], r4[1], r4[2], r4[3],
+                       KV_FULL(st), kBoth, pol_kv);
       }
       issued = it + 1;
     }
     // No copy may still be in flight when the CTA exits: the last phase of
-    // each stage completes only once every loader's bytes have landed.
+    // each stage completes only once every byte (both CTAs' copies) landed.
+    // The peer's arrive on Q_PEER is consumed here too.
     if (ltid == 0) {
       for (int u = issued - 1; u >= 0 && u >= issued - 2; --u) mbar_wait(KV_FULL(u & 1), (u >> 1) & 1);
       mbar_wait(Q_FULL, 0);
       mbar_wait(Q_STAGE, 0);
+      mbar_wait(Q_PEER, 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -258,7 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kBN / 16; ++j)
           mma_f16_ts(tO, tP + 8 * j, smem_desc_sw128(stage + j * 2048, kAtomBytes, 1024), idesc_pv,
                      (i > 0 || j > 0) ? 1u : 0u);
-        tc_commit(KV_EMPTY(i & 1));
+        // The stage is reused by tile i + 2 (if any), whose copies land in
+        // both CTAs: both MMAs must be done with it.
+        if (i + 2 < ntiles) tc_commit_mc(KV_EMPTY(i & 1), kBoth);
         tc_commit(PV_DONE);
         ++pv_issued;
         return true;
@@ -332,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!qok) raise_error(kErrTimeout);
       tc_fence_before();
       mbar_arrive(Q_TMEM);
+      named_bar_sync(2, 128);   // this CTA's softmax threads all read stage 1
+      if (h == 0) mbar_arrive_remote(mapa_shared(Q_PEER, peer));
     }
     const float sc = p.sm_scale * 1.4426950408889634f;  // exp -> exp2
     float mrun = ninf, lrun = 0.f;
@@ -422,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.mid_lse[(static_cast<long long>(t) * H + h) * S + split] =
           (ok && lrun > 0.f) ? (mrun + log2f(lrun)) * 0.6931471805599453f : ninf;
   }
-  __syncthreads();
+  // Neither CTA leaves while the other may still signal or copy into it.
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -449,7 +468,7 @@ cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.num_splits, a.batch * a.nq);
   return launch_kernel(sparse_mla_kernel, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0,
-                       tq, tkv, a);
+                       2, tq, tkv, a);
 }
 
 }  // namespace dsa

@@ -460,7 +460,7 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   return launch_kernel(topk_select_kernel, grid, dim3(kThreads), kSmemBytes, stream,
-                       a.pdl != 0 && a.hist_ready, a);
+                       a.pdl != 0 && a.hist_ready, 1, a);
 }
 
 // ---------------------------------------------------------------------------
