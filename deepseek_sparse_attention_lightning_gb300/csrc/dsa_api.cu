@@ -3,6 +3,7 @@
 // encoding and the launch sequence of the decode layer.
 #include <cmath>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -10,6 +11,7 @@
 
 #include "dsa.h"
 #include "dsa_internal.h"
+#include "dsa_ptx.cuh"
 
 namespace dsa {
 
@@ -81,6 +83,14 @@ dsa_status check_desc(const dsa_decode_desc* d) {
 }
 
 int rows_of(const dsa_decode_desc* d) { return d->batch * d->q_per_req; }
+
+// Zero-fills n16 16-byte words; lets its dependent (the indexer) start at once.
+__global__ void ws_clear_kernel(uint4* p, long long n16) {
+  dsa::grid_dep_launch();
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += step)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
 
 int max_splits(const dsa_decode_desc* d) { return (d->topk + 63) / 64; }
 
@@ -296,15 +306,22 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
   const int32_t* idx = topk_in;
   if (!topk_in) {
     int32_t* sel = topk_out ? topk_out : reinterpret_cast<int32_t*>(base + lay.topk);
-    cudaError_t e = cudaMemsetAsync(base + lay.hist, 0, lay.cand - lay.hist, s);
-    if (e != cudaSuccess || !mark(0)) return DSA_ERR_CUDA;
+    // Histogram and control words start at zero: a small kernel clears them
+    // and the indexer runs as its dependent (prologue and key stream overlap
+    // the clear; only its first histogram flush waits for it).
+    if (!mark(0)) return DSA_ERR_CUDA;
+    const long long n16 = static_cast<long long>((lay.cand - lay.hist) / 16);
+    const int cgrid = static_cast<int>(std::min<long long>((n16 + 255) / 256, 148));
+    cudaError_t e = dsa::launch_kernel(ws_clear_kernel, dim3(cgrid), dim3(256), 0, s, false, 1,
+                                       reinterpret_cast<uint4*>(base + lay.hist), n16);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
     dsa::IndexerLaunch ia{};
     ia.q_fp8 = q_fp8; ia.q_scale = q_scale; ia.w = w; ia.k_fp8 = k_fp8; ia.k_scale = k_scale;
     ia.seqlens = d->seqlens; ia.page_table = d->page_table;
     ia.logits = reinterpret_cast<float*>(base + lay.logits); ia.ld = lay.ld;
     ia.hist = reinterpret_cast<uint32_t*>(base + lay.hist);
     ia.batch = d->batch; ia.nq = d->q_per_req; ia.max_pages = d->max_pages;
-    ia.num_pages = d->num_pages; ia.topk = d->topk; ia.skip_short = 1;
+    ia.num_pages = d->num_pages; ia.topk = d->topk; ia.skip_short = 1; ia.pdl = 1;
     e = dsa::launch_indexer(ia, s);
     if (e != cudaSuccess || !mark(1)) return DSA_ERR_CUDA;
     dsa::TopkLaunch ta{};

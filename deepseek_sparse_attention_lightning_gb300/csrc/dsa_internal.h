@@ -40,6 +40,7 @@ struct IndexerLaunch {
   uint32_t* hist;       // [T][kHistBins] or nullptr
   int batch, nq, max_pages, num_pages, topk;
   int skip_short;       // skip requests whose queries all see <= topk tokens
+  int pdl;              // 1: launched as a programmatic dependent of the workspace clear
 };
 
 struct TopkLaunch {

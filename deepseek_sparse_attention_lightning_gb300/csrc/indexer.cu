@@ -356,6 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int r = 0, cur = -1, S = 0;
     bool ok = true;
     auto flush_hist = [&](int req) {
+      // The histogram may be cleared by the kernel before (fused path): the
+      // first global atomic waits for it; everything earlier does not.
+      grid_dep_wait();
       named_bar_sync(bar_id, 128);
       for (int i = 0; i < NQ; ++i) {
         uint32_t* gh = p.hist + static_cast<long long>(req * NQ + i) * kHistBins;
@@ -452,8 +455,8 @@ cudaError_t launch_nq(const IndexerLaunch& a, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = device_sm_count();
-  indexer_kernel<NQ><<<grid, kThreads, C::kSmemBytes, stream>>>(tk, tq, a);
-  return cudaGetLastError();
+  return launch_kernel(indexer_kernel<NQ>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream,
+                       a.pdl != 0, 1, tk, tq, a);
 }
 
 }  // namespace
