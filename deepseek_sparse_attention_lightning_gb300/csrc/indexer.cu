@@ -15,11 +15,12 @@
 // in a shared-memory histogram of the top 11 key bits (the first top-k pass).
 //
 // Warp roles (384 threads, one persistent CTA per SM):
-//   warp 0, lane 0  TMA producer: one 8 KB box per page into a ring of 5-12
-//            stages (as many as shared memory holds next to the fixed
-//            buffers), and the request's FP8 queries (double-buffered) when
-//            the request changes.  It issues nothing else: a TMA instruction
-//            costs its issuing thread ~100-170 cycles.
+//   warp 0   TMA producer: one 8 KB box per page into a ring of 5-12 stages
+//            (as many as shared memory holds next to the fixed buffers),
+//            issued by 8 lanes for 4 tiles at a time, and the request's FP8
+//            queries (double-buffered) when the request changes.  It issues
+//            nothing else: a TMA instruction costs its issuing thread
+//            ~100-170 cycles.
 //   warps 1, 2  MMA issuers (one thread each, alternate tiles); warp 1 owns
 //            TMEM;
 //   warps 4-7, 8-11  two epilogue groups taking alternate tiles (one thread
@@ -47,6 +48,7 @@ constexpr int kEpiGroups = 2;   // warps 4-7 take even tiles, warps 8-11 odd til
 constexpr int kMaxBatch = 1024;
 constexpr int kPageWin = 512;   // page ids cached in shared memory (256 tiles)
 constexpr int kScaleAhead = 3;  // epilogue scale prefetch distance (own tiles)
+constexpr int kGroup = 4;       // tiles whose copies the producer warp issues together
 constexpr int kSmemLimit = 232448;
 
 template <int NQ>
@@ -235,47 +237,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && g0 < g1) {
+    // The whole warp issues, kGroup tiles at a time: lane 2u + w copies page
+    // w of tile u of the group, after lane 2u waited for the stage and armed
+    // its barrier (copies from several threads keep more requests in flight
+    // than one issuing thread).  The queries of a request that starts in the
+    // group go first, from lane 0.
+    if (g0 < g1) {
       const uint64_t pol_k = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      int r = 0, cur = -1, seg = -1;
-      uint32_t it = 0;
+      const int ntl = g1 - g0;
+      int r = 0, cur = -1, seg = -1;   // lane 0: request and query segment
+      int rl = 0;                      // this lane's request (its tiles only increase)
+      int done = 0;                    // tiles whose copies were all issued
       bool ok = true;
-      for (int g = g0; g < g1; ++g, ++it) {
-        while (prefix[r + 1] <= g) ++r;
-        if (r != cur) {
-          cur = r;
-          ++seg;
-          const int qb = seg & 1;
-          if (seg >= 2 && !mbar_wait(Q_EMPTY(qb), ((seg >> 1) - 1) & 1)) { ok = false; break; }
-          mbar_expect_tx(Q_FULL(qb), C::kQBytes);
-          tma_load_2d(sbase + C::kOffQ + qb * C::kQBytes, &tmap_q, 0, r * C::kN, Q_FULL(qb), pol_q);
+      for (int it0 = 0; it0 < ntl; it0 += kGroup) {
+        if (lane == 0) {
+          for (int u = 0; u < kGroup && it0 + u < ntl && ok; ++u) {
+            const int g = g0 + it0 + u;
+            while (prefix[r + 1] <= g) ++r;
+            if (r != cur) {
+              cur = r;
+              ++seg;
+              const int qb = seg & 1;
+              if (seg >= 2 && !mbar_wait(Q_EMPTY(qb), ((seg >> 1) - 1) & 1)) { ok = false; break; }
+              mbar_expect_tx(Q_FULL(qb), C::kQBytes);
+              tma_load_2d(sbase + C::kOffQ + qb * C::kQBytes, &tmap_q, 0, r * C::kN, Q_FULL(qb),
+                          pol_q);
+            }
+          }
         }
-        const uint32_t st = it % C::kStages;
-        if (it >= C::kStages && !mbar_wait(KV_EMPTY(st), ((it / C::kStages) - 1) & 1)) {
-          ok = false;
-          break;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int it = it0 + (lane >> 1);
+        const int which = lane & 1;
+        const bool act = lane < 2 * kGroup && it < ntl;
+        const uint32_t st = static_cast<uint32_t>(it) % C::kStages;
+        bool armed = true;
+        if (act && which == 0) {
+          if (it >= C::kStages) armed = mbar_wait(KV_EMPTY(st), ((it / C::kStages) - 1) & 1);
+          if (armed) mbar_expect_tx(KV_FULL(st), kStageBytes);
         }
-        // An out-of-range page id (-1 here) is reported and read past the
-        // cache end (TMA fills zeros); the epilogue masks its tokens.
-        const int pg0 = page_of(r, g, 0), pg1 = page_of(r, g, 1);
-        if (pg0 < 0 || pg1 < 0) raise_error(kErrCheck);
-        const int y0 = pg0 >= 0 ? pg0 * kPage : p.num_pages * kPage;
-        const int y1 = pg1 >= 0 ? pg1 * kPage : p.num_pages * kPage;
-        const uint32_t dst = sbase + C::kOffStages + st * kStageBytes;
-        mbar_expect_tx(KV_FULL(st), kStageBytes);
-        tma_load_2d(dst, &tmap_k, 0, y0, KV_FULL(st), pol_k);
-        tma_load_2d(dst + kPage * kIndexDim, &tmap_k, 0, y1, KV_FULL(st), pol_k);
+        armed = __shfl_sync(0xffffffffu, armed, lane & ~1);
+        if (__any_sync(0xffffffffu, act && !armed)) { ok = false; break; }
+        if (act) {
+          // An out-of-range page id (-1 here) is reported and read past the
+          // cache end (TMA fills zeros); the epilogue masks its tokens.
+          const int g = g0 + it;
+          while (prefix[rl + 1] <= g) ++rl;
+          const int pg = page_of(rl, g, which);
+          if (pg < 0) raise_error(kErrCheck);
+          const int y = pg >= 0 ? pg * kPage : p.num_pages * kPage;
+          tma_load_2d(sbase + C::kOffStages + st * kStageBytes + which * (kPage * kIndexDim), &tmap_k,
+                      0, y, KV_FULL(st), pol_k);
+        }
+        done = min(it0 + kGroup, ntl);
       }
-      if (!ok) raise_error(kErrTimeout);
-      // No copy may still be in flight when the CTA exits.
-      const uint32_t n = it < static_cast<uint32_t>(C::kStages) ? it : C::kStages;
-      for (uint32_t s = 0; s < n; ++s) {
-        const uint32_t u = it - 1 - ((it - 1 - s) % C::kStages);
-        mbar_wait(KV_FULL(s), (u / C::kStages) & 1);
+      if (lane == 0) {
+        if (!ok) raise_error(kErrTimeout);
+        // No copy may still be in flight when the CTA exits.
+        const uint32_t it = static_cast<uint32_t>(done);
+        const uint32_t n = it < static_cast<uint32_t>(C::kStages) ? it : C::kStages;
+        for (uint32_t s = 0; s < n; ++s) {
+          const uint32_t u = it - 1 - ((it - 1 - s) % C::kStages);
+          mbar_wait(KV_FULL(u % C::kStages), (u / C::kStages) & 1);
+        }
+        if (seg >= 0) mbar_wait(Q_FULL(seg & 1), (seg >> 1) & 1);
+        if (seg >= 1) mbar_wait(Q_FULL((seg - 1) & 1), ((seg - 1) >> 1) & 1);
       }
-      if (seg >= 0) mbar_wait(Q_FULL(seg & 1), (seg >> 1) & 1);
-      if (seg >= 1) mbar_wait(Q_FULL((seg - 1) & 1), ((seg - 1) >> 1) & 1);
     }
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
