@@ -59,8 +59,7 @@ int device_sm_count() {
 namespace {
 
 using dsa::kHistBins;
-using dsa::topk_bitmap_words;
-using dsa::topk_ctl_words;
+using dsa::kTopkCtlWords;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -101,22 +100,21 @@ int resolve_splits(const dsa_decode_desc* d, int32_t num_splits) {
 dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 struct TopkWs {
-  size_t hist, counters, cand, bitmap, total;
+  size_t hist, counters, cand, total;
 };
 
 TopkWs topk_ws_layout(int T, int64_t ld) {
   TopkWs w;
   w.hist = 0;
   w.counters = w.hist + size_t(T) * kHistBins * 4;
-  w.cand = align256(w.counters + size_t(T) * topk_ctl_words(ld) * 4);
-  w.bitmap = align256(w.cand + size_t(T) * size_t(ld) * 8);
-  w.total = align256(w.bitmap + size_t(T) * size_t(topk_bitmap_words(ld)) * 4);
+  w.cand = align256(w.counters + size_t(T) * kTopkCtlWords * 4);
+  w.total = align256(w.cand + size_t(T) * size_t(ld) * 8);
   return w;
 }
 
 struct FusedWs {
   int64_t ld;
-  size_t logits, hist, counters, cand, bitmap, topk, mid_o, mid_lse, total;
+  size_t logits, hist, counters, cand, topk, mid_o, mid_lse, total;
 };
 
 FusedWs fused_ws_layout(const dsa_decode_desc* d, int32_t max_seqlen, int splits) {
@@ -126,9 +124,8 @@ FusedWs fused_ws_layout(const dsa_decode_desc* d, int32_t max_seqlen, int splits
   w.logits = 0;
   w.hist = align256(w.logits + size_t(T) * size_t(w.ld) * 4);
   w.counters = w.hist + size_t(T) * kHistBins * 4;
-  w.cand = align256(w.counters + size_t(T) * topk_ctl_words(w.ld) * 4);
-  w.bitmap = align256(w.cand + size_t(T) * size_t(w.ld) * 8);
-  w.topk = align256(w.bitmap + size_t(T) * size_t(topk_bitmap_words(w.ld)) * 4);
+  w.cand = align256(w.counters + size_t(T) * kTopkCtlWords * 4);
+  w.topk = align256(w.cand + size_t(T) * size_t(w.ld) * 8);
   w.mid_o = align256(w.topk + size_t(T) * size_t(d->topk) * 4);
   const size_t mo = splits > 1 ? size_t(T) * d->num_heads * splits * dsa::kVDim * 4 : 0;
   w.mid_lse = align256(w.mid_o + mo);
@@ -201,7 +198,7 @@ dsa_status dsa_topk(const dsa_decode_desc* d, const float* logits, int64_t ld, i
     return DSA_ERR_INVALID_ARG;
   if (ld < static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE || ld % 4 != 0)
     return DSA_ERR_INVALID_ARG;
-  if (ld > int64_t(dsa::kTopkMaxChunks) * dsa::kTopkChunk) return DSA_ERR_UNSUPPORTED;
+  if (ld > dsa::kTopkMaxLd) return DSA_ERR_UNSUPPORTED;
   const TopkWs lay = topk_ws_layout(rows_of(d), ld);
   if (!ws || !aligned(ws, 16) || ws_bytes < lay.total) return DSA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -213,7 +210,6 @@ dsa_status dsa_topk(const dsa_decode_desc* d, const float* logits, int64_t ld, i
   a.hist = reinterpret_cast<uint32_t*>(base + lay.hist);
   a.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
   a.cand = reinterpret_cast<uint2*>(base + lay.cand);
-  a.bitmap = reinterpret_cast<uint32_t*>(base + lay.bitmap);
   a.batch = d->batch; a.nq = d->q_per_req; a.k = d->topk; a.hist_ready = 0;
   return cuda_status(dsa::launch_topk(a, s));
 }
@@ -288,7 +284,7 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
   if (max_seqlen < 1 || static_cast<int64_t>(max_seqlen) > static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE)
     return DSA_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(max_seqlen) > int64_t(dsa::kTopkMaxChunks) * dsa::kTopkChunk)
+  if (static_cast<int64_t>(max_seqlen) > dsa::kTopkMaxLd)
     return DSA_ERR_UNSUPPORTED;
   const int splits = resolve_splits(d, num_splits);
   if (splits < 1 || splits > max_splits(d)) return DSA_ERR_INVALID_ARG;
@@ -328,7 +324,6 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
     ta.seqlens = d->seqlens; ta.logits = ia.logits; ta.ld = lay.ld; ta.out = sel;
     ta.hist = ia.hist; ta.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
     ta.cand = reinterpret_cast<uint2*>(base + lay.cand);
-    ta.bitmap = reinterpret_cast<uint32_t*>(base + lay.bitmap);
     ta.batch = d->batch; ta.nq = d->q_per_req; ta.k = d->topk; ta.hist_ready = 1;
     ta.pdl = 1;   // overlaps its launch with the indexer's last CTAs
     e = dsa::launch_topk(ta, s);

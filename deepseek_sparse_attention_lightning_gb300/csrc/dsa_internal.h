@@ -17,15 +17,12 @@ constexpr int kPage = 64;
 constexpr int kHistBins = 2048;     // top 11 bits of the order-preserving score key
 constexpr int kHistShift = 21;
 constexpr int kTopkChunk = 8192;    // logits per CTA in the top-k passes
-constexpr int kTopkMaxChunks = 256; // chunks per row: rows of up to 2^21 scores
-
-// Top-k control words of one query row: [0] ticket, [1..3] spare,
-// [4 + c] candidate count of chunk c.
-__host__ __device__ constexpr int topk_ctl_words(int64_t ld) {
-  return 4 + static_cast<int>((ld + kTopkChunk - 1) / kTopkChunk);
-}
-// Selection bitmap words of one query row.
-__host__ __device__ constexpr int64_t topk_bitmap_words(int64_t ld) { return (ld + 31) / 32; }
+constexpr int kTopkClusterCtas = 16;  // CTAs (chunks) per query row in the select pass
+// Rows of up to 16 chunks of 4 x 8192 scores.
+constexpr int64_t kTopkMaxLd = int64_t(kTopkClusterCtas) * kTopkChunk * 4;
+// Top-k control words of one query row: [0..3] spare, [4 + c] candidate
+// count of chunk c.
+constexpr int kTopkCtlWords = 4 + kTopkClusterCtas;
 
 struct IndexerLaunch {
   const uint8_t* q_fp8;
@@ -49,9 +46,8 @@ struct TopkLaunch {
   int64_t ld;
   int32_t* out;         // [T][k]
   uint32_t* hist;       // [T][kHistBins], zeroed (or filled by the indexer)
-  uint32_t* counters;   // [T][topk_ctl_words(ld)], zeroed
-  uint2* cand;          // [T][ld]: chunk c's candidates at [c * kTopkChunk, ...)
-  uint32_t* bitmap;     // [T][topk_bitmap_words(ld)]: the selection, one bit per position
+  uint32_t* counters;   // [T][kTopkCtlWords]
+  uint2* cand;          // [T][ld]: chunk c's candidates at the chunk's first position
   int batch, nq, k;
   int hist_ready;       // 1: hist already holds the row histograms
   int pdl;              // 1: launched as a programmatic dependent of the indexer

@@ -8,17 +8,21 @@
 // Scores are compared through an order-preserving 32-bit key (-0 == +0).
 //   pass 1  histogram of the top 11 key bits per row (fused into the indexer
 //           epilogue on the fused path, else topk_hist_kernel);
-//   pass 2  topk_select_kernel, one CTA per 8192 positions of a row: finds the
-//           bin b* where the count from the top crosses k, marks every
-//           position above b* in the row's selection bitmap (one bit per
-//           position, written without atomics: each thread owns 16
-//           consecutive positions) and stores the positions in b* as
-//           candidates in its chunk's own slice of the candidate list; the
-//           last CTA of the row (ticket counter) resolves the candidates with
-//           more radix levels over the remaining 21 key bits and, for exact
-//           ties, a radix select over the position, sets the winners' bits,
-//           and writes the row in ascending position order by a scan of the
-//           bitmap.
+//   pass 2  topk_select_kernel: each row is one cluster of 16 CTAs, CTA x
+//           owning chunk x of the row (8192, 16384 or 32768 positions, 16, 32
+//           or 64 consecutive ones per thread).  Every CTA finds the bin b*
+//           where the count from the top crosses k, marks the positions above
+//           b* in its shared-memory slice of the selection bitmap and stores
+//           the positions in b* as candidates in its own slice of a global
+//           list.  After a cluster barrier, CTA 0 resolves the candidates
+//           with more radix levels over the remaining 21 key bits (a pairwise
+//           rank once few are left, a radix select over the position for
+//           exact ties) into one threshold (key, position): a candidate is in
+//           iff its key is larger, or equal with a position not larger.
+//           After a second barrier every CTA marks its own winners, the CTAs
+//           exchange their selected counts through distributed shared
+//           memory, and each writes its chunk's positions, ascending, at its
+//           offset in the row.
 #include <mutex>
 
 #include "dsa.h"
@@ -31,13 +35,14 @@ namespace dsa {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kPer = kTopkChunk / kThreads;           // consecutive positions per thread
-constexpr int kPairMax = 1024;                        // sub-candidates ranked pairwise
+constexpr int kPairMax = 128;                         // sub-candidates ranked pairwise
 constexpr int kOffHist = 0;                           // 2048 x u32
-constexpr int kOffCand = kOffHist + kHistBins * 4;    // kTopkChunk x uint2
+constexpr int kOffCand = kOffHist + kHistBins * 4;    // kTopkChunk x uint2 (resolver)
 constexpr int kOffSub = kOffCand + kTopkChunk * 8;    // kPairMax x uint2
-constexpr int kSmemBytes = kOffSub + kPairMax * 8;    // 80 KB
-static_assert(kPer == 16, "a thread pair fills one 32-bit bitmap word");
+constexpr int kOffBits = kOffSub + kPairMax * 8;      // this chunk's bitmap words
+constexpr int kMaxChunkMul = 4;                       // chunk = 8192 x {1, 2, 4}
+constexpr int kCandSlot = kTopkChunk / 16;            // candidates per chunk kept in CTA 0's smem
+constexpr int kSmemBytes = kOffBits + (kTopkChunk * kMaxChunkMul / 32) * 4;   // 84 KB
 
 __device__ __forceinline__ int visible(const int32_t* seqlens, int t, int nq) {
   return seqlens[t / nq] - (nq - 1 - t % nq);
@@ -144,16 +149,25 @@ __global__ void __launch_bounds__(kThreads)
     if (sh[i]) atomicAdd(gh + i, sh[i]);
 }
 
+// One cluster of kTopkClusterCtas CTAs per query row; CTA x owns chunk x of
+// C = 512 * 16 * M positions, 16 M consecutive ones per thread.
+template <int M>
 __global__ void __launch_bounds__(kThreads)
     topk_select_kernel(const TopkLaunch p) {
+  constexpr int P = 16 * M;            // positions per thread
+  constexpr int C = kThreads * P;      // positions per CTA
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* sh = reinterpret_cast<uint32_t*>(smem + kOffHist);
   uint2* scand = reinterpret_cast<uint2*>(smem + kOffCand);
   uint2* sub = reinterpret_cast<uint2*>(smem + kOffSub);
+  uint32_t* sbits = reinterpret_cast<uint32_t*>(smem + kOffBits);
   __shared__ uint32_t scratch[40];
   __shared__ int res[2];
-  __shared__ int s_info[4];   // candidates of this CTA, last flag, winners, sub count
-  __shared__ int s_pref[kTopkMaxChunks + 1];
+  __shared__ int s_info[4];   // candidates of this CTA, -, -, sub count
+  __shared__ int s_pref[kTopkClusterCtas + 1];
+  __shared__ uint32_t s_thr[2];   // the threshold (key, position), pushed by CTA 0
+  __shared__ uint32_t s_allsel[kTopkClusterCtas];   // every chunk's selected count, pushed by each
+  __shared__ uint32_t s_ccnt[kTopkClusterCtas];   // (CTA 0) every chunk's candidate count
 
   // Everything this kernel reads may come from the kernel before it.
   grid_dep_wait();
@@ -165,65 +179,78 @@ __global__ void __launch_bounds__(kThreads)
   int32_t* out_row = p.out + static_cast<long long>(t) * k;
 
   if (vis <= k) {
-    // Every visible token is selected (the short-context case).
+    // Every visible token is selected (the short-context case); the whole
+    // cluster of the row leaves here.
     if (blockIdx.x == 0)
       for (int i = threadIdx.x; i < k; i += kThreads) out_row[i] = i < vis ? i : -1;
     return;
   }
-  const int nch = (vis + kTopkChunk - 1) / kTopkChunk;
-  const int x = blockIdx.x;
-  if (x >= nch) return;
-  uint32_t* ctl = p.counters + static_cast<long long>(t) * topk_ctl_words(p.ld);
+  const int x = static_cast<int>(cluster_ctarank());
+  const int nch = (vis + C - 1) / C;   // <= kTopkClusterCtas (checked on the host)
+  const bool has = x < nch;
   uint2* cand_row = p.cand + static_cast<long long>(t) * p.ld;
-  uint32_t* bm_row = p.bitmap + static_cast<long long>(t) * topk_bitmap_words(p.ld);
+  const int lo = x * C;
+  const int hi = has ? min(vis, lo + C) : lo;
+  const int s0 = lo + P * static_cast<int>(threadIdx.x);
 
-  // ---- this CTA's chunk: 16 consecutive scores per thread (through L1: a
-  //      warp's four 16-byte loads share their cache lines), loaded before
-  //      the row histogram (one latency for both).
+  // ---- scores of this thread's P positions (through L1: a warp's loads
+  //      share cache lines), in flight together with the row histogram.
   const float* row = p.logits + static_cast<long long>(t) * p.ld;
-  const int lo = x * kTopkChunk;
-  const int hi = min(vis, lo + kTopkChunk);
-  const int s0 = lo + kPer * static_cast<int>(threadIdx.x);
-  float v[kPer];
-  if (s0 + kPer <= hi) {
+  float v[P];
+  if (s0 + P <= hi) {
 #pragma unroll
-    for (int q = 0; q < kPer / 4; ++q) {
+    for (int q = 0; q < P / 4; ++q) {
       const float4 f = __ldg(reinterpret_cast<const float4*>(row + s0) + q);
       v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) v[j] = s0 + j < hi ? __ldg(row + s0 + j) : 0.f;
+    for (int j = 0; j < P; ++j) v[j] = s0 + j < hi ? __ldg(row + s0 + j) : 0.f;
   }
   const uint32_t* gh = p.hist + static_cast<long long>(t) * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = __ldcg(gh + i);
   if (threadIdx.x == 0) s_info[0] = 0;
   __syncthreads();
   // ---- threshold bin b*: the count of scores in bins above it (nabove) is
-  //      < k and reaches k with it.
+  //      < k and reaches k with it.  Every CTA gets the same answer.
   find_crossing(sh, static_cast<uint32_t>(k), true, res, scratch);
   const int bstar = res[0];
   const int nabove = res[1];
-  if (bstar < 0) {  // histogram inconsistent with the row
+  if (bstar < 0) {  // histogram inconsistent with the row (the whole cluster leaves)
     if (threadIdx.x == 0) raise_error(kErrCheck);
     return;
   }
   const uint32_t ub = static_cast<uint32_t>(bstar);
-  uint32_t above = 0, inbin = 0;
+  // ---- classify: positions above b* -> this chunk's bitmap words, those in
+  //      b* -> this chunk's slice of the candidate list (global).
+  uint32_t inbin[M];
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    if (s0 + j < hi) {
-      const uint32_t bin = float_key(v[j]) >> kHistShift;
-      if (bin > ub) above |= 1u << j;
-      else if (bin == ub) inbin |= 1u << j;
+  for (int h = 0; h < M; ++h) {
+    uint32_t above = 0, in = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int jj = 16 * h + j;
+      if (s0 + jj < hi) {
+        const uint32_t bin = float_key(v[jj]) >> kHistShift;
+        if (bin > ub) above |= 1u << j;
+        else if (bin == ub) in |= 1u << j;
+      }
+    }
+    inbin[h] = in;
+    // 16-bit half h of this thread's positions; thread pairs fill a word
+    // when P = 16, else the thread owns whole words.
+    if (M == 1) {
+      const uint32_t upper = __shfl_down_sync(0xffffffffu, above, 1);
+      if ((threadIdx.x & 1) == 0) sbits[threadIdx.x >> 1] = above | (upper << 16);
+    } else {
+      const int wi = static_cast<int>(threadIdx.x) * (P / 32) + (h >> 1);
+      if ((h & 1) == 0) sbits[wi] = above;
+      else sbits[wi] |= above << 16;
     }
   }
-  // Positions above b* -> the bitmap: threads 2w and 2w+1 fill word w of the
-  // chunk (every word of [lo, hi) is written, so the bitmap needs no clear).
-  const uint32_t upper = __shfl_down_sync(0xffffffffu, above, 1);
-  if ((threadIdx.x & 1) == 0 && s0 < hi) bm_row[s0 >> 5] = above | (upper << 16);
-  // Positions in b* -> this chunk's slice of the candidate list.
-  const int mine = __popc(inbin);
+  int mine = 0;
+#pragma unroll
+  for (int h = 0; h < M; ++h) mine += __popc(inbin[h]);
   int incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -234,213 +261,206 @@ __global__ void __launch_bounds__(kThreads)
   if (lane == 31) wbase = atomicAdd(&s_info[0], incl);
   wbase = __shfl_sync(0xffffffffu, wbase, 31);
   {
-    int pos = lo + wbase + incl - mine;
+    // Candidate i of this chunk goes to CTA 0's shared memory at slot
+    // x * kCandSlot + i (if i < kCandSlot) and to this chunk's slice of the
+    // global list (read by CTA 0 only for a chunk with more candidates).
+    const uint32_t cand0 = mapa_shared(smem_u32(scand), 0);
+    int i = wbase + incl - mine;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j)
-      if ((inbin >> j) & 1u) cand_row[pos++] = make_uint2(float_key(v[j]), static_cast<uint32_t>(s0 + j));
-  }
-  // The barrier orders the block's writes before thread 0's release fence;
-  // the last CTA's acquire fence then sees every CTA's writes.
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    ctl[4 + x] = static_cast<uint32_t>(s_info[0]);
-    __threadfence();
-    const uint32_t ticket = atomicAdd(ctl, 1u);
-    const bool last = ticket == static_cast<uint32_t>(nch - 1);
-    if (last) __threadfence();
-    s_info[1] = last ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_info[1]) return;
-
-  // ---- last CTA of the row: gather the candidates of bin b*.
-  {
-    const uint32_t c = threadIdx.x < static_cast<unsigned>(nch) ? __ldcg(ctl + 4 + threadIdx.x) : 0u;
-    const uint32_t e = block_excl_scan_512(c, scratch);
-    if (threadIdx.x <= static_cast<unsigned>(nch)) s_pref[threadIdx.x] = static_cast<int>(e);
-  }
-  if (threadIdx.x == 0) { s_info[2] = 0; s_info[3] = 0; }
-  __syncthreads();
-  const int nc = s_pref[nch];
-  if (static_cast<uint32_t>(nc) != sh[ub]) {   // candidates disagree with the histogram
-    if (threadIdx.x == 0) raise_error(kErrCheck);
-    return;
-  }
-  // Candidate e lives in chunk c (s_pref[c] <= e < s_pref[c + 1]).
-  auto chunk_of = [&](int e) -> int {
-    int a = 0, b = nch - 1;
-    while (a < b) {
-      const int m = (a + b + 1) >> 1;
-      if (s_pref[m] <= e) a = m; else b = m - 1;
-    }
-    return a;
-  };
-  const bool in_smem = nc <= kTopkChunk;
-  auto cget = [&](int e) -> uint2 {
-    if (in_smem) return scand[e];
-    const int c = chunk_of(e);
-    return __ldcg(cand_row + static_cast<long long>(c) * kTopkChunk + (e - s_pref[c]));
-  };
-  if (in_smem) {
-    // Four loads in flight per thread, then their four stores.
-    for (int e0 = threadIdx.x; e0 < nc; e0 += 4 * kThreads) {
-      uint2 cv[4];
+    for (int h = 0; h < M; ++h)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * kThreads;
-        if (e < nc) {
-          const int c = chunk_of(e);
-          cv[u] = __ldcg(cand_row + static_cast<long long>(c) * kTopkChunk + (e - s_pref[c]));
+      for (int j = 0; j < 16; ++j)
+        if ((inbin[h] >> j) & 1u) {
+          const int jj = 16 * h + j;
+          const uint2 c = make_uint2(float_key(v[jj]), static_cast<uint32_t>(s0 + jj));
+          cand_row[lo + i] = c;
+          if (i < kCandSlot) st_shared_cluster_v2(cand0 + 8u * (x * kCandSlot + i), c.x, c.y);
+          ++i;
         }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (e0 + u * kThreads < nc) scand[e0 + u * kThreads] = cv[u];
-    }
-    __syncthreads();
   }
-  // A winner's bit goes into the bitmap (the CTAs that wrote it are done).
-  auto take = [&](uint32_t s) {
-    atomicOr(bm_row + (s >> 5), 1u << (s & 31));
-    atomicAdd(&s_info[2], 1);
-  };
-
-  // ---- resolve: the need best candidates by (key desc, position asc).
-  const uint32_t need = static_cast<uint32_t>(k - nabove);
-  uint32_t kprefix = ub << kHistShift, kmask = 0xFFFFFFFFu << kHistShift;
-  uint32_t need_l = need;
-  uint32_t cnt_eq = 0;
-  const int kshift[2] = {10, 0};
-  const int kwidth[2] = {11, 10};
-  bool ok = need >= 1;
-  bool pairwise = false;
-  for (int lvl = 0; lvl < 2 && ok; ++lvl) {
-    const int sh_ = kshift[lvl];
-    const uint32_t dm = (1u << kwidth[lvl]) - 1u;
-    for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
-    __syncthreads();
-    for (int e = threadIdx.x; e < nc; e += kThreads) {
-      const uint32_t key = cget(e).x;
-      if ((key & kmask) == kprefix) atomicAdd(&sh[(key >> sh_) & dm], 1u);
-    }
-    __syncthreads();
-    find_crossing(sh, need_l, true, res, scratch);
-    if (res[0] < 0) { ok = false; break; }
-    const uint32_t d = static_cast<uint32_t>(res[0]);
-    cnt_eq = sh[d];
-    need_l -= static_cast<uint32_t>(res[1]);
-    kprefix |= d << sh_;
-    kmask |= dm << sh_;
-    __syncthreads();
-    // Few candidates left in the crossing digit: rank them pairwise instead
-    // of further radix levels.
-    if (lvl == 0 && cnt_eq <= static_cast<uint32_t>(kPairMax)) {
-      pairwise = true;
-      break;
-    }
-  }
-  if (!ok) {
-    if (threadIdx.x == 0) raise_error(kErrCheck);
-    return;
-  }
-  if (pairwise) {
-    // Candidates whose digit is above the crossing one are in; of those with
-    // the crossing digit (m <= kPairMax), the need_l best by (key desc,
-    // position asc) are in.
-    const uint32_t hi_digits = kprefix >> 10;
-    for (int e = threadIdx.x; e < nc; e += kThreads) {
-      const uint2 c = cget(e);
-      const uint32_t cd = c.x >> 10;
-      if (cd > hi_digits) take(c.y);
-      else if (cd == hi_digits) sub[atomicAdd(&s_info[3], 1)] = c;
-    }
-    __syncthreads();
-    const int m = s_info[3];
-    for (int i = threadIdx.x; i < m; i += kThreads) {
-      const uint2 ci = sub[i];
-      uint32_t rank = 0;
-      for (int j2 = 0; j2 < m; ++j2) {
-        const uint2 cj = sub[j2];
-        rank += (cj.x > ci.x || (cj.x == ci.x && cj.y < ci.y)) ? 1u : 0u;
-      }
-      if (rank < need_l) take(ci.y);
-    }
-  } else {
-    const uint32_t kstar = kprefix;
-    // Exact ties at the threshold key: keep the need_l lowest positions.
-    uint32_t istar = 0xFFFFFFFFu;
-    if (need_l < cnt_eq) {
-      uint32_t iprefix = 0, imask = 0, need_i = need_l;
-      const int ishift[3] = {20, 10, 0};
-      const int iwidth[3] = {11, 10, 10};
-      for (int lvl = 0; lvl < 3 && ok; ++lvl) {
-        const int sh_ = ishift[lvl];
-        const uint32_t dm = (1u << iwidth[lvl]) - 1u;
-        for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
-        __syncthreads();
-        for (int e = threadIdx.x; e < nc; e += kThreads) {
-          const uint2 c = cget(e);
-          if (c.x == kstar && (c.y & imask) == iprefix) atomicAdd(&sh[(c.y >> sh_) & dm], 1u);
-        }
-        __syncthreads();
-        find_crossing(sh, need_i, false, res, scratch);
-        if (res[0] < 0) { ok = false; break; }
-        need_i -= static_cast<uint32_t>(res[1]);
-        iprefix |= static_cast<uint32_t>(res[0]) << sh_;
-        imask |= dm << sh_;
-        __syncthreads();
-      }
-      istar = iprefix;
-    }
-    if (!ok) {
-      if (threadIdx.x == 0) raise_error(kErrCheck);
-      return;
-    }
-    for (int e = threadIdx.x; e < nc; e += kThreads) {
-      const uint2 c = cget(e);
-      if (c.x > kstar || (c.x == kstar && c.y <= istar)) take(c.y);
-    }
-  }
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0 && nabove + s_info[2] != k) raise_error(kErrCheck);
+  if (threadIdx.x == 0)
+    st_shared_cluster_u32(mapa_shared(smem_u32(&s_ccnt[x]), 0), has ? static_cast<uint32_t>(s_info[0]) : 0u);
+  cluster_sync();   // #1: every chunk's candidates and count are in place
 
-  // ---- the row in ascending position order from the bitmap, staged in
-  //      shared memory (the candidate buffer) in slices of 8192 words with
-  //      their exclusive bit-count prefix.  Output j is then found by a
-  //      binary search over the prefix, so every thread writes about k / 512
-  //      outputs however the selected bits cluster.
-  const int nwords = (vis + 31) >> 5;
-  uint32_t* sbm = reinterpret_cast<uint32_t*>(smem + kOffCand);
-  constexpr int kSlice = kTopkChunk;       // words: bitmap + prefix = the 64 KB buffer
-  uint32_t* spre = sbm + kSlice;
-  uint32_t base = 0;
-  for (int c0 = 0; c0 < nwords; c0 += kSlice) {
-    const int cn = min(kSlice, nwords - c0);
-    __syncthreads();   // the previous slice (or the candidates) is no longer read
-    for (int i = threadIdx.x; i < cn; i += kThreads) sbm[i] = __ldcg(bm_row + c0 + i);
-    __syncthreads();
-    const int per = (cn + kThreads - 1) / kThreads;
-    const int w0 = min(cn, static_cast<int>(threadIdx.x) * per), w1 = min(cn, w0 + per);
-    uint32_t cnt = 0;
-    for (int w = w0; w < w1; ++w) cnt += __popc(sbm[w]);
-    uint32_t run = block_excl_scan_512(cnt, scratch);
-    const uint32_t total = scratch[16 + 15];   // inclusive sum over the block
-    for (int w = w0; w < w1; ++w) {
-      spre[w] = run;
-      run += __popc(sbm[w]);
+  // ---- CTA 0 resolves the candidates of bin b* into the threshold.
+  if (x == 0) {
+    {
+      const uint32_t c = threadIdx.x < static_cast<unsigned>(nch) ? s_ccnt[threadIdx.x] : 0u;
+      const uint32_t e = block_excl_scan_512(c, scratch);
+      if (threadIdx.x <= static_cast<unsigned>(nch)) s_pref[threadIdx.x] = static_cast<int>(e);
+    }
+    if (threadIdx.x == 0) {
+      s_info[3] = 0;
+      s_thr[0] = 0xFFFFFFFFu;   // selects no candidate (error fallback)
+      s_thr[1] = 0u;
     }
     __syncthreads();
-    for (uint32_t j = threadIdx.x; j < total; j += kThreads) {
-      int a = 0, b = cn - 1;   // the last word whose prefix is <= j holds output j
+    const int nc = s_pref[nch];
+    bool ok = static_cast<uint32_t>(nc) == sh[ub];   // candidates agree with the histogram
+    auto chunk_of = [&](int e) -> int {
+      int a = 0, b = nch - 1;
       while (a < b) {
         const int m = (a + b + 1) >> 1;
-        if (spre[m] <= j) a = m; else b = m - 1;
+        if (s_pref[m] <= e) a = m; else b = m - 1;
       }
-      if (base + j < static_cast<uint32_t>(k))
-        out_row[base + j] = (c0 + a) * 32 + nth_set_bit(sbm[a], static_cast<int>(j - spre[a]));
+      return a;
+    };
+    // Candidate e: chunk c, index i; in shared memory if i < kCandSlot.
+    auto cget = [&](int e) -> uint2 {
+      const int c = chunk_of(e), i = e - s_pref[c];
+      return i < kCandSlot ? scand[c * kCandSlot + i]
+                           : __ldcg(cand_row + static_cast<long long>(c) * C + i);
+    };
+    // The need best candidates by (key desc, position asc).
+    const uint32_t need = static_cast<uint32_t>(k - nabove);
+    uint32_t kprefix = ub << kHistShift, kmask = 0xFFFFFFFFu << kHistShift;
+    uint32_t need_l = need;
+    uint32_t cnt_eq = 0;
+    const int kshift[2] = {10, 0};
+    const int kwidth[2] = {11, 10};
+    ok = ok && need >= 1;
+    bool pairwise = false;
+    for (int lvl = 0; lvl < 2 && ok; ++lvl) {
+      const int sh_ = kshift[lvl];
+      const uint32_t dm = (1u << kwidth[lvl]) - 1u;
+      for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
+      __syncthreads();
+      for (int e = threadIdx.x; e < nc; e += kThreads) {
+        const uint32_t key = cget(e).x;
+        if ((key & kmask) == kprefix) atomicAdd(&sh[(key >> sh_) & dm], 1u);
+      }
+      __syncthreads();
+      find_crossing(sh, need_l, true, res, scratch);
+      if (res[0] < 0) { ok = false; break; }
+      const uint32_t d = static_cast<uint32_t>(res[0]);
+      cnt_eq = sh[d];
+      need_l -= static_cast<uint32_t>(res[1]);
+      kprefix |= d << sh_;
+      kmask |= dm << sh_;
+      __syncthreads();
+      if (lvl == 0 && cnt_eq <= static_cast<uint32_t>(kPairMax)) {
+        pairwise = true;
+        break;
+      }
     }
-    base += total;
+    if (ok && pairwise) {
+      // Of the candidates with the crossing digit (m <= kPairMax), the
+      // need_l-th best by (key desc, position asc) is the threshold.
+      const uint32_t hi_digits = kprefix >> 10;
+      for (int e = threadIdx.x; e < nc; e += kThreads) {
+        const uint2 c = cget(e);
+        if ((c.x >> 10) == hi_digits) sub[atomicAdd(&s_info[3], 1)] = c;
+      }
+      __syncthreads();
+      const int m = s_info[3];
+      for (int i = threadIdx.x; i < m; i += kThreads) {
+        const uint2 ci = sub[i];
+        uint32_t rank = 0;
+        for (int j2 = 0; j2 < m; ++j2) {
+          const uint2 cj = sub[j2];
+          rank += (cj.x > ci.x || (cj.x == ci.x && cj.y < ci.y)) ? 1u : 0u;
+        }
+        if (rank == need_l - 1) {
+          s_thr[0] = ci.x;
+          s_thr[1] = ci.y;
+        }
+      }
+    } else if (ok) {
+      // Exact ties at the threshold key: keep the need_l lowest positions.
+      const uint32_t kstar = kprefix;
+      uint32_t istar = 0xFFFFFFFFu;
+      if (need_l < cnt_eq) {
+        uint32_t iprefix = 0, imask = 0, need_i = need_l;
+        const int ishift[3] = {20, 10, 0};
+        const int iwidth[3] = {11, 10, 10};
+        for (int lvl = 0; lvl < 3 && ok; ++lvl) {
+          const int sh_ = ishift[lvl];
+          const uint32_t dm = (1u << iwidth[lvl]) - 1u;
+          for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
+          __syncthreads();
+          for (int e = threadIdx.x; e < nc; e += kThreads) {
+            const uint2 c = cget(e);
+            if (c.x == kstar && (c.y & imask) == iprefix) atomicAdd(&sh[(c.y >> sh_) & dm], 1u);
+          }
+          __syncthreads();
+          find_crossing(sh, need_i, false, res, scratch);
+          if (res[0] < 0) { ok = false; break; }
+          need_i -= static_cast<uint32_t>(res[1]);
+          iprefix |= static_cast<uint32_t>(res[0]) << sh_;
+          imask |= dm << sh_;
+          __syncthreads();
+        }
+        istar = iprefix;
+      }
+      if (ok && threadIdx.x == 0) {
+        s_thr[0] = kstar;
+        s_thr[1] = istar;
+      }
+    }
+    if (!ok && threadIdx.x == 0) raise_error(kErrCheck);
+    __syncthreads();
+    // Push the threshold to every CTA of the row.
+    if (threadIdx.x < kTopkClusterCtas) {
+      const uint32_t a = mapa_shared(smem_u32(&s_thr[0]), threadIdx.x);
+      st_shared_cluster_u32(a, s_thr[0]);
+      st_shared_cluster_u32(a + 4, s_thr[1]);
+    }
+  }
+  cluster_sync();   // #2: every CTA has the threshold
+
+  // ---- every CTA: its winners among its candidates, then its selected count.
+  const uint32_t tkey = s_thr[0];
+  const uint32_t tpos = s_thr[1];
+  if (has) {
+    const int nmine = s_info[0];
+    for (int e = threadIdx.x; e < nmine; e += kThreads) {
+      const uint2 c = __ldcg(cand_row + lo + e);
+      if (c.x > tkey || (c.x == tkey && c.y <= tpos)) {
+        const int off = static_cast<int>(c.y) - lo;
+        atomicOr(&sbits[off >> 5], 1u << (off & 31));
+      }
+    }
+  }
+  __syncthreads();
+  constexpr int kWords = C / 32;                       // this chunk's bitmap words
+  constexpr int kWPT = (kWords + kThreads - 1) / kThreads;
+  const int nw = has ? (hi - lo + 31) / 32 : 0;
+  uint32_t wv[kWPT];
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int u = 0; u < kWPT; ++u) {
+    const int w = static_cast<int>(threadIdx.x) * kWPT + u;
+    wv[u] = w < nw ? sbits[w] : 0u;
+    cnt += __popc(wv[u]);
+  }
+  uint32_t pos = block_excl_scan_512(cnt, scratch);
+  // Push this chunk's selected count to every CTA of the row.
+  {
+    const uint32_t mysel = scratch[16 + 15];   // the block's inclusive total
+    if (threadIdx.x < kTopkClusterCtas)
+      st_shared_cluster_u32(mapa_shared(smem_u32(&s_allsel[x]), threadIdx.x), mysel);
+  }
+  cluster_sync();   // #3: every CTA has every chunk's count; no remote access after this
+  uint32_t base = 0, total = 0;
+#pragma unroll
+  for (int y = 0; y < kTopkClusterCtas; ++y) {
+    const uint32_t c = s_allsel[y];
+    if (y < x) base += c;
+    total += c;
+  }
+  if (x == 0 && threadIdx.x == 0 && total != static_cast<uint32_t>(k)) raise_error(kErrCheck);
+  pos += base;
+#pragma unroll
+  for (int u = 0; u < kWPT; ++u) {
+    uint32_t bits = wv[u];
+    const int w = static_cast<int>(threadIdx.x) * kWPT + u;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < static_cast<uint32_t>(k)) out_row[pos] = lo + w * 32 + b;
+      ++pos;
+    }
   }
 }
 
@@ -448,27 +468,34 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   const int T = a.batch * a.nq;
-  const int chunks = static_cast<int>((a.ld + kTopkChunk - 1) / kTopkChunk);
-  if (chunks > kTopkMaxChunks) return cudaErrorInvalidValue;
-  dim3 grid(chunks > 0 ? chunks : 1, T);
+  const int64_t per_mul = int64_t(kTopkClusterCtas) * kTopkChunk;   // ld covered with M = 1
+  const int mul = a.ld <= per_mul ? 1 : (a.ld <= 2 * per_mul ? 2 : (a.ld <= 4 * per_mul ? 4 : 0));
+  if (mul == 0) return cudaErrorInvalidValue;
   if (!a.hist_ready) {
-    topk_hist_kernel<<<grid, kThreads, 0, stream>>>(a);
+    const int chunks = static_cast<int>((a.ld + kTopkChunk - 1) / kTopkChunk);
+    topk_hist_kernel<<<dim3(chunks > 0 ? chunks : 1, T), kThreads, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return launch_kernel(topk_select_kernel, grid, dim3(kThreads), kSmemBytes, stream,
-                       a.pdl != 0 && a.hist_ready, 1, a);
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, dim3(kTopkClusterCtas, T), dim3(kThreads), kSmemBytes, stream,
+                         a.pdl != 0 && a.hist_ready, kTopkClusterCtas, a);
+  };
+  if (mul == 1) return go(topk_select_kernel<1>);
+  if (mul == 2) return go(topk_select_kernel<2>);
+  return go(topk_select_kernel<4>);
 }
 
 // ---------------------------------------------------------------------------
 // Top-k without a caller-provided workspace (dsa_topk_noalloc).
 //
 // For callers that cannot allocate device memory at the point where they run
-// the selection, the histogram, control words, candidate lists and selection
-// bitmap live in one statically sized device array.  Every GPU that loads the library reserves
+// the selection, the histogram, control words and candidate lists live in one
+// statically sized device array.  Every GPU that loads the library reserves
 // it (kNoAllocScratchBytes) until the process exits.
 // ---------------------------------------------------------------------------
 namespace {
@@ -477,16 +504,9 @@ constexpr int kNoAllocMaxRows = 64;                 // query rows T
 constexpr long long kNoAllocMaxScores = 1ll << 21;  // T * ld_logits
 constexpr size_t kNoAllocHistBytes = size_t(kNoAllocMaxRows) * kHistBins * 4;
 constexpr size_t kNoAllocCounterOff = kNoAllocHistBytes;
-// Control words: 4 per row plus one per 8192-score chunk, over all rows at
-// most 4 T + T + 2^21 / 8192 words.
-constexpr size_t kNoAllocCounterWords =
-    size_t(kNoAllocMaxRows) * 5 + size_t(kNoAllocMaxScores) / kTopkChunk;
 constexpr size_t kNoAllocCandOff =
-    (kNoAllocCounterOff + kNoAllocCounterWords * 4 + 255) & ~size_t(255);
-constexpr size_t kNoAllocBitmapOff = kNoAllocCandOff + size_t(kNoAllocMaxScores) * 8;
-// Bitmap: ceil(ld / 32) words per row, at most 2^21 / 32 + T words.
-constexpr size_t kNoAllocScratchBytes =
-    kNoAllocBitmapOff + (size_t(kNoAllocMaxScores) / 32 + kNoAllocMaxRows) * 4;
+    (kNoAllocCounterOff + size_t(kNoAllocMaxRows) * kTopkCtlWords * 4 + 255) & ~size_t(255);
+constexpr size_t kNoAllocScratchBytes = kNoAllocCandOff + size_t(kNoAllocMaxScores) * 8;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -535,6 +555,7 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_decode_desc* d, const float* lo
   const int T = d->batch * d->q_per_req;
   if (T > kNoAllocMaxRows || static_cast<long long>(T) * ld > kNoAllocMaxScores)
     return DSA_ERR_UNSUPPORTED;   // beyond the fixed scratch: use dsa_topk with a workspace
+  if (ld > kTopkMaxLd) return DSA_ERR_UNSUPPORTED;
   cudaError_t e;
   uint8_t* base = static_cast<uint8_t*>(noalloc_scratch(&e));
   if (!base) return DSA_ERR_CUDA;
@@ -547,7 +568,6 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_decode_desc* d, const float* lo
   a.hist = reinterpret_cast<uint32_t*>(base);
   a.counters = reinterpret_cast<uint32_t*>(base + kNoAllocCounterOff);
   a.cand = reinterpret_cast<uint2*>(base + kNoAllocCandOff);
-  a.bitmap = reinterpret_cast<uint32_t*>(base + kNoAllocBitmapOff);
   a.batch = d->batch; a.nq = d->q_per_req; a.k = d->topk; a.hist_ready = 0;
   return launch_topk(a, s) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
