@@ -129,8 +129,10 @@ dsa_status dsa_indexer_logits(const dsa_decode_desc* desc, const uint8_t* q_fp8,
  * the largest logits[t*ld + s]; equal scores go to the lower position, -0.0
  * equals +0.0.  The n positions are written in ascending order at [0, n) and
  * the rest of the row is -1.  Exact: the set equals that of a full sort.
- * No full sort is done (radix select with shared-memory histograms).
- *   logits   [dev] float [T, ld_logits] (only s < vis[t] is read)
+ * No full sort is done (radix select with shared-memory histograms; each row
+ * is one cluster of 16 CTAs, launched with the non-portable cluster size).
+ *   logits   [dev] float [T, ld_logits] (only s < vis[t] is read),
+ *            ld_logits <= 524288 (else DSA_ERR_UNSUPPORTED)
  *   topk_idx [dev] int32 [T, k]
  *   ws       [dev] workspace of dsa_topk_workspace_bytes() bytes, 16-B aligned
  */
@@ -148,10 +150,11 @@ size_t dsa_topk_workspace_bytes(const dsa_decode_desc* desc, int64_t ld_logits);
  * the engine has reserved all of the device's memory for its caches, or a
  * host runtime without a device allocator of its own, where a cudaMalloc
  * would fail or stall the device.  The histogram, counters and candidate
- * lists then live in a file-scope device array of fixed size (about 16.8 MB)
+ * lists then live in a file-scope device array of fixed size (about 16.5 MB)
  * that every GPU loading this library reserves until the process exits.  No
  * call allocates or frees memory.
- *   Limits: T = batch * q_per_req <= 64 and T * ld_logits <= 2^21 scores;
+ *   Limits: T = batch * q_per_req <= 64, T * ld_logits <= 2^21 scores and
+ *   ld_logits <= 524288 (as dsa_topk);
  *   larger batches return DSA_ERR_UNSUPPORTED (use dsa_topk with a workspace).
  *   The first call on a device looks up the array's device address (once per
  *   device); make that first call before capturing the stream into a graph.
