@@ -49,6 +49,7 @@ constexpr int kMaxBatch = 1024;
 constexpr int kPageWin = 512;   // page ids cached in shared memory (256 tiles)
 constexpr int kScaleAhead = 3;  // epilogue scale prefetch distance (own tiles)
 constexpr int kGroup = 4;       // tiles whose copies the producer warp issues together
+constexpr int kHistFlushTiles = 500;   // a group's tiles per histogram flush (< 65536 / 128)
 constexpr int kSmemLimit = 232448;
 
 template <int NQ>
@@ -56,12 +57,12 @@ struct Cfg {
   static constexpr int kN = 64 * NQ;
   static constexpr int kQBytes = kN * kIndexDim;
   // Everything but the key ring; the ring then takes what shared memory is
-  // left (up to 12 stages): the ring's bytes in flight set the bandwidth.
-  static constexpr int kFixed = 2 * kQBytes + kEpiGroups * NQ * kHistBins * 4 +
-                                kEpiGroups * kN * 4 + kPageWin * 4 + (1024 + 4) * 4 + 64 * 4 +
-                                (2 * 12 + 4 + 2 * 4) * 8 + 16 + 1024;
+  // left (up to 14 stages): the ring's bytes in flight set the bandwidth.
+  static constexpr int kHistBytes = kEpiGroups * NQ * kHistBins * 2;   // 16-bit bins
+  static constexpr int kFixed = 2 * kQBytes + kHistBytes + kEpiGroups * kN * 4 + kPageWin * 4 +
+                                (1024 + 4) * 4 + 64 * 4 + (2 * 14 + 4 + 2 * 4 + 1) * 8 + 16 + 1024;
   static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
+  static constexpr int kStages = kStagesFit > 14 ? 14 : kStagesFit;
   // Accumulator buffers: four when they fit in TMEM, so the MMA of a tile
   // never waits for the epilogue of the tile two before it.
   static constexpr int kAccBufs = (4 * kN <= 512) ? 4 : 2;
@@ -70,12 +71,12 @@ struct Cfg {
   static constexpr int kOffStages = 0;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffHist = kOffQ + 2 * kQBytes;
-  static constexpr int kOffW = kOffHist + kEpiGroups * NQ * kHistBins * 4;
+  static constexpr int kOffW = kOffHist + kHistBytes;
   static constexpr int kOffPages = kOffW + kEpiGroups * kN * 4;
   static constexpr int kOffPrefix = kOffPages + kPageWin * 4;
   static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 4) * 4;
   static constexpr int kOffBar = kOffScratch + 64 * 4;
-  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccBufs;
+  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccBufs + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffTmemSlot + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory");
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define Q_EMPTY(b) (bar0 + 8u * (2 * C::kStages + 2 + (b)))
 #define ACC_FULL(b) (bar0 + 8u * (2 * C::kStages + 4 + (b)))
 #define ACC_EMPTY(b) (bar0 + 8u * (2 * C::kStages + 4 + C::kAccBufs + (b)))
+  const uint32_t PAGES = bar0 + 8u * (2 * C::kStages + 4 + 2 * C::kAccBufs);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.batch;
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r < B) prefix[r + 1] = run;
     }
   }
-  for (int i = threadIdx.x; i < kEpiGroups * NQ * kHistBins; i += kThreads) shist[i] = 0u;
+  for (int i = threadIdx.x; i < C::kHistBytes / 4; i += kThreads) shist[i] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(KV_FULL(s), 1);
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(ACC_FULL(b), 1);
       mbar_init(ACC_EMPTY(b), 128);
     }
+    mbar_init(PAGES, 1);   // warps 1-11 stored the shared page ids
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -219,17 +222,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g0 = static_cast<int>((static_cast<long long>(blockIdx.x) * total) / G);
   const int g1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total) / G);
 
-  // Page ids of the first kPageWin / 2 tiles of the range, fetched by all
-  // threads at once.
-  {
+  grid_dep_launch();   // the top-k may be scheduled as this kernel's CTAs retire
+  // Page ids of the first kPageWin / 2 tiles of the range, fetched into
+  // shared memory by warps 1-11 at once; the producer warp does not wait for
+  // them: it looks up its first group's pages itself and starts streaming.
+  if (warp != 0) {
     const int n = min(2 * (g1 - g0), kPageWin);
-    for (int i = threadIdx.x; i < n; i += kThreads) {
+    for (int i = threadIdx.x - 32; i < n; i += kThreads - 32) {
       const int g = g0 + (i >> 1);
       pages[i] = tile_page(p, prefix, find_request(prefix, B, g), g, i & 1);
     }
+    named_bar_sync(3, kThreads - 32);
+    if (threadIdx.x == 32) mbar_arrive(PAGES);
   }
-  __syncthreads();
-  grid_dep_launch();   // the top-k may be scheduled as this kernel's CTAs retire
   auto page_of = [&](int r, int g, int which) -> int {
     const int i = 2 * (g - g0) + which;
     return i < kPageWin ? pages[i] : tile_page(p, prefix, r, g, which);
@@ -284,13 +289,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // cache end (TMA fills zeros); the epilogue masks its tokens.
           const int g = g0 + it;
           while (prefix[rl + 1] <= g) ++rl;
-          const int pg = page_of(rl, g, which);
+          const int pg = it0 == 0 ? tile_page(p, prefix, rl, g, which) : page_of(rl, g, which);
           if (pg < 0) raise_error(kErrCheck);
           const int y = pg >= 0 ? pg * kPage : p.num_pages * kPage;
           tma_load_2d(sbase + C::kOffStages + st * kStageBytes + which * (kPage * kIndexDim), &tmap_k,
                       0, y, KV_FULL(st), pol_k);
         }
         done = min(it0 + kGroup, ntl);
+        // From the second group on, the pages come from shared memory.
+        if (it0 == 0 && ntl > kGroup && !mbar_wait(PAGES, 0)) {
+          ok = false;
+          break;
+        }
       }
       if (lane == 0) {
         if (!ok) raise_error(kErrTimeout);
@@ -366,7 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q4 * 32 + lane;        // token within the tile
     const int tid = (warp - kEpiWarp0 - 4 * gi) * 32 + lane;
     const uint32_t bar_id = 1 + gi;
-    uint32_t* ghist = shist + gi * NQ * kHistBins;
+    // Histogram bins are 16-bit halves of 32-bit words (bin b: word b / 2),
+    // flushed to the global histogram at a request change and every
+    // kHistFlushTiles tiles, so no bin can overflow.
+    uint32_t* ghist = shist + gi * NQ * (kHistBins / 2);
+    int seg_tiles = 0;
     float* gw = wbuf + gi * C::kN;
     const float ninf = __int_as_float(0xff800000);
     // Key scale of this thread's token in tile g (0 if the page is invalid).
@@ -390,21 +404,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(bar_id, 128);
       for (int i = 0; i < NQ; ++i) {
         uint32_t* gh = p.hist + static_cast<long long>(req * NQ + i) * kHistBins;
-        for (int b = tid; b < kHistBins; b += 128) {
-          const uint32_t v = ghist[i * kHistBins + b];
+        for (int w = tid; w < kHistBins / 2; w += 128) {
+          const uint32_t v = ghist[i * (kHistBins / 2) + w];
           if (v) {
-            atomicAdd(gh + b, v);
-            ghist[i * kHistBins + b] = 0u;
+            if (v & 0xFFFFu) atomicAdd(gh + 2 * w, v & 0xFFFFu);
+            if (v >> 16) atomicAdd(gh + 2 * w + 1, v >> 16);
+            ghist[i * (kHistBins / 2) + w] = 0u;
           }
         }
       }
       named_bar_sync(bar_id, 128);
+      seg_tiles = 0;
     };
     for (int g = g0 + gi; g < g1; g += kEpiGroups) {
       const uint32_t it = static_cast<uint32_t>(g - g0);
       while (prefix[r + 1] <= g) ++r;
       if (r != cur) {
         if (cur >= 0 && p.hist) flush_hist(cur);
+        seg_tiles = 0;
         named_bar_sync(bar_id, 128);
         cur = r;
         S = p.seqlens[r];
@@ -447,9 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool live = tok_ok && s < vis;
           const float v = live ? (s0 + s1) * sk : ninf;
           p.logits[static_cast<long long>(r * NQ + i) * p.ld + s] = v;
-          if (p.hist && live) atomicAdd(&ghist[i * kHistBins + (float_key(v) >> kHistShift)], 1u);
+          if (p.hist && live) {
+            const uint32_t bin = float_key(v) >> kHistShift;
+            atomicAdd(&ghist[i * (kHistBins / 2) + (bin >> 1)], 1u << (16 * (bin & 1)));
+          }
         }
       }
+      if (p.hist && ++seg_tiles == kHistFlushTiles) flush_hist(cur);
     }
     if (!ok) raise_error(kErrTimeout);
     if (cur >= 0 && p.hist) flush_hist(cur);
