@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the per-configuration table (other workloads)")
     return p.parse_args()
 
 
@@ -282,6 +284,135 @@ def run_reference(args, world, rank):
 # GPU leg
 # ---------------------------------------------------------------------------
 
+def pctl(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, int(q * len(xs)))]
+
+
+def measure_configs(torch, api, W, dev, steps):
+    """The other workloads of the benchmark table, each timed like the
+    headline (graph-replayed layer call, L2 flushed between steps, median and
+    p10/p90 of per-step events): tiny_4k cold and warm, mtp_32k, long_varlen,
+    short_dense as the DSA layer and as the dense path (the same attention
+    over every visible token, given as the selection), and mli_195k's two
+    layers serial vs with the second layer's indexer + top-k on a second
+    stream while its attention reuses the first layer's selection."""
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    res = {}
+
+    def timed(fn, n, do_flush=True):
+        g = torch.cuda.CUDAGraph()
+        fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            a.record()
+            b.record()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        for i in range(n):
+            if do_flush:
+                flush.zero_()
+            ev[i][0].record()
+            g.replay()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        if api.dsa_get_device_error() != 0:
+            raise RuntimeError("device error while timing a configuration")
+        us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+        return {"us_median": statistics.median(us), "us_p10": pctl(us, 0.1), "us_p90": pctl(us, 0.9)}
+
+    def layer_fn(wl, layer=0, topk_in=None, topk_out=None, ws=None, out=None):
+        spec = wl.spec
+        desc = api.workload_desc(wl)
+        splits = api.dsa_num_splits_auto(desc)
+        msl = wl.max_seqlen
+        ws = api.alloc_workspace(wl, splits) if ws is None else ws
+        out = torch.empty((spec.num_tokens, spec.num_heads, 512), dtype=torch.float32, device=dev) \
+            if out is None else out
+        lc = wl.layers[layer]
+
+        def fn():
+            api.dsa_decode_fused(desc, wl.q_fp8, wl.q_scale, wl.w, lc.k_fp8, lc.k_scale, lc.q, lc.kv,
+                                 out, ws, msl, spec.sm_scale, splits, topk_in, topk_out,
+                                 stream=torch.cuda.current_stream())
+        return fn
+
+    def record(name, wl, t):
+        u = accounting(wl.spec, wl.seqlens.cpu().tolist())
+        t.update(query_tokens_per_s=u["query_tokens"] / (t["us_median"] * 1e-6),
+                 layer_bytes=u["layer_bytes"],
+                 layer_gbs=u["layer_bytes"] / (t["us_median"] * 1e-6) / 1e9,
+                 frac_of_8tbs=u["layer_bytes"] / (t["us_median"] * 1e-6) / 1e9 / TARGET_HBM_GBS)
+        res[name] = t
+
+    n = max(20, min(steps, 200))
+    for name in ("tiny_4k", "mtp_32k", "long_varlen", "short_dense", "mli_195k"):
+        wl = W.make_workload(name, device=dev)
+        if name == "tiny_4k":
+            record(name, wl, timed(layer_fn(wl), n))
+            record(name + "_warm", wl, timed(layer_fn(wl), n, do_flush=False))
+        elif name == "short_dense":
+            record(name, wl, timed(layer_fn(wl), n))
+            # dense path: every visible position given as the selection
+            T, k = wl.spec.num_tokens, wl.spec.topk
+            vis = [max(int(s), 0) for s in wl.seqlens.cpu().tolist()]
+            ident = torch.full((T, k), -1, dtype=torch.int32)
+            for t, v in enumerate(vis):
+                ident[t, :min(v, k)] = torch.arange(min(v, k), dtype=torch.int32)
+            ident = ident.to(dev)
+            r = timed(layer_fn(wl, topk_in=ident), n)
+            record(name + "_dense", wl, r)
+            res[name]["overhead_vs_dense_us"] = res[name]["us_median"] - r["us_median"]
+        elif name == "mli_195k":
+            T, k = wl.spec.num_tokens, wl.spec.topk
+            sel1 = torch.empty((T, k), dtype=torch.int32, device=dev)
+            sel2 = torch.empty((T, k), dtype=torch.int32, device=dev)
+            f1 = layer_fn(wl, 0, topk_out=sel1)
+            f2 = layer_fn(wl, 1)
+            f2_reuse = layer_fn(wl, 1, topk_in=sel1)
+            desc = api.workload_desc(wl)
+            ld = api.logits_ld(wl)
+            logits2 = torch.empty((T, ld), dtype=torch.float32, device=dev)
+            tws = torch.empty(api.dsa_topk_workspace_bytes(desc, ld), dtype=torch.uint8, device=dev)
+            lc2 = wl.layers[1]
+            side = torch.cuda.Stream()
+
+            def serial():
+                f1()
+                f2()
+
+            def overlapped():
+                f1()
+                main = torch.cuda.current_stream()
+                side.wait_stream(main)
+                with torch.cuda.stream(side):
+                    api.dsa_indexer_logits(desc, wl.q_fp8, wl.q_scale, wl.w, lc2.k_fp8, lc2.k_scale,
+                                           logits2, ld, side)
+                    api.dsa_topk(desc, logits2, sel2, tws, ld, side)
+                f2_reuse()
+                main.wait_stream(side)
+
+            a = timed(serial, n)
+            b = timed(overlapped, n)
+            u = accounting(wl.spec, wl.seqlens.cpu().tolist())
+            for key, t in (("mli_195k_serial_2layers", a), ("mli_195k_overlapped_2layers", b)):
+                t.update(query_tokens_per_s=u["query_tokens"] / (t["us_median"] * 1e-6),
+                         layer_bytes=2 * u["layer_bytes"],
+                         layer_gbs=2 * u["layer_bytes"] / (t["us_median"] * 1e-6) / 1e9)
+                res[key] = t
+            res["mli_195k_overlapped_2layers"]["speedup_vs_serial"] = a["us_median"] / b["us_median"]
+        else:
+            record(name, wl, timed(layer_fn(wl), n))
+        del wl
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, world, rank, local):
     import torch
     from deepseek_sparse_attention_lightning_gb300 import api, build
@@ -440,6 +571,10 @@ def run_ours(args, world, rank, local):
                "sample": f"{n} query rows ({nreq} whole requests of {args.workload}, one at a time, "
                          f"{spent:.1f} s), float64 numpy oracle (BLAS threads = cores)"}
 
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = measure_configs(torch, api, W, dev, K)
+
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     idx_mean_ms = statistics.mean(idx_ms)
@@ -478,6 +613,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "gpu_launches": K * (3 + (1 if splits > 1 else 0)),
         "clocks": clocks,
+        "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

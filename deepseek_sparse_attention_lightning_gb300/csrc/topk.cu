@@ -23,6 +23,7 @@
 //           exchange their selected counts through distributed shared
 //           memory, and each writes its chunk's positions, ascending, at its
 //           offset in the row.
+#include <algorithm>
 #include <mutex>
 
 #include "dsa.h"
@@ -149,7 +150,8 @@ __global__ void __launch_bounds__(kThreads)
     if (sh[i]) atomicAdd(gh + i, sh[i]);
 }
 
-// One cluster of kTopkClusterCtas CTAs per query row; CTA x owns chunk x of
+// One cluster of gridDim.x (<= kTopkClusterCtas) CTAs per query row, as many
+// as the longest row needs chunks; CTA x owns chunk x of
 // C = 512 * 16 * M positions, 16 M consecutive ones per thread.
 template <int M>
 __global__ void __launch_bounds__(kThreads)
@@ -186,7 +188,8 @@ __global__ void __launch_bounds__(kThreads)
     return;
   }
   const int x = static_cast<int>(cluster_ctarank());
-  const int nch = (vis + C - 1) / C;   // <= kTopkClusterCtas (checked on the host)
+  const int cs = static_cast<int>(gridDim.x);   // CTAs of the row's cluster
+  const int nch = (vis + C - 1) / C;   // <= cs (the host sizes the cluster)
   const bool has = x < nch;
   uint2* cand_row = p.cand + static_cast<long long>(t) * p.ld;
   const int lo = x * C;
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(kThreads)
     if (!ok && threadIdx.x == 0) raise_error(kErrCheck);
     __syncthreads();
     // Push the threshold to every CTA of the row.
-    if (threadIdx.x < kTopkClusterCtas) {
+    if (threadIdx.x < static_cast<unsigned>(cs)) {
       const uint32_t a = mapa_shared(smem_u32(&s_thr[0]), threadIdx.x);
       st_shared_cluster_u32(a, s_thr[0]);
       st_shared_cluster_u32(a + 4, s_thr[1]);
@@ -438,13 +441,13 @@ __global__ void __launch_bounds__(kThreads)
   // Push this chunk's selected count to every CTA of the row.
   {
     const uint32_t mysel = scratch[16 + 15];   // the block's inclusive total
-    if (threadIdx.x < kTopkClusterCtas)
+    if (threadIdx.x < static_cast<unsigned>(cs))
       st_shared_cluster_u32(mapa_shared(smem_u32(&s_allsel[x]), threadIdx.x), mysel);
   }
   cluster_sync();   // #3: every CTA has every chunk's count; no remote access after this
   uint32_t base = 0, total = 0;
 #pragma unroll
-  for (int y = 0; y < kTopkClusterCtas; ++y) {
+  for (int y = 0; y < cs; ++y) {
     const uint32_t c = s_allsel[y];
     if (y < x) base += c;
     total += c;
@@ -482,8 +485,11 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, dim3(kTopkClusterCtas, T), dim3(kThreads), kSmemBytes, stream,
-                         a.pdl != 0 && a.hist_ready, kTopkClusterCtas, a);
+    // As many CTAs per row as the longest row (ld) has chunks.
+    const int64_t chunk = int64_t(kTopkChunk) * mul;
+    const int cs = static_cast<int>(std::min<int64_t>(kTopkClusterCtas, (a.ld + chunk - 1) / chunk));
+    return launch_kernel(kern, dim3(cs > 0 ? cs : 1, T), dim3(kThreads), kSmemBytes, stream,
+                         a.pdl != 0 && a.hist_ready, cs > 0 ? cs : 1, a);
   };
   if (mul == 1) return go(topk_select_kernel<1>);
   if (mul == 2) return go(topk_select_kernel<2>);
