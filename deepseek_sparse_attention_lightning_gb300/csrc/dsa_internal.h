@@ -114,6 +114,11 @@ int fetch_error_merge();
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer, CUtensorMapSwizzle swizzle);
+// Rank-r map (r <= 5): dims[0] is contiguous, byte_strides[i] is the stride
+// of dimension i + 1; no fill for out-of-range loads, clipped stores.
+bool encode_tmap_nd(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                    const uint64_t* dims, const uint64_t* byte_strides, const uint32_t* box,
+                    CUtensorMapSwizzle swizzle);
 int device_sm_count();
 
 }  // namespace dsa

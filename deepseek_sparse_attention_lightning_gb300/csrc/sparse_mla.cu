@@ -27,20 +27,24 @@
 //
 // Per tile: S = Q K^T is 20 TMEM-A MMAs (dims 0..319) + 16 smem-A MMAs (dims
 // 320..575), M = 128, N = 64, K = 16 (kind::f16, bf16 in, fp32 out).  The
-// softmax warps (one thread per head = per TMEM lane) read S, apply the scale
-// in the exp2 domain, keep a running maximum that is raised lazily (the
-// accumulator is rescaled only when a tile's maximum exceeds it by 2^8), write
-// P to TMEM, and P V (4 MMAs, N = 256, V read MN-major from the same smem
-// stage) accumulates into O.
+// softmax threads (two per head = per TMEM lane, each with 32 of the tile's
+// 64 keys) read S, apply the scale in the exp2 domain, keep a running
+// maximum that is raised lazily (the accumulator is rescaled only when a
+// tile's maximum exceeds it by 2^8), write P to TMEM, and P V (4 MMAs,
+// N = 256, V read MN-major from the same smem stage) accumulates into O.  The
+// MMA thread issues P V of a tile as soon as its P is written, also between
+// the MMAs of the next tile's Q K^T, because that P V frees the stage the
+// gather two tiles ahead waits for.
 //
-// Warp roles (256 threads): warps 0, 2, 3 resolve every selected position to
-// its cache row (logical index -> page table -> row, fused here) and gather
-// the rows with TMA tile::gather4 copies (4 rows x 64 dims each, written in
-// the 128B-swizzled stage layout by the copy engine); all 96 loader threads
-// issue, because one gather4 costs its issuing thread ~170 cycles while the
-// SM's copy engine accepts many at once (one issuer: ~0.8 TB/s over the GPU,
-// 128 issuers: ~4.7 TB/s, on 1152-byte rows).  Warp 1 issues the MMAs and
-// owns TMEM; warps 4-7 run the softmax and the epilogue.
+// Warp roles (512 threads): warps 0, 2, 3 and 8-11 resolve every selected
+// position to its cache row (logical index -> page table -> row, fused here)
+// and gather the rows with TMA tile::gather4 copies (4 rows x 64 dims each,
+// written in the 128B-swizzled stage layout by the copy engine); 72 threads
+// spread over the seven warps issue one copy each per tile, because the copy
+// engine takes a warp's TMA instructions one lane at a time (~170 cycles
+// each) but the warps' in parallel.  Warp 1 issues the MMAs and owns TMEM;
+// warps 4-7 and 12-15 run the softmax and the epilogue (Mid_O written by
+// 128B-swizzled tensor stores of 32 heads x 32 dims).
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
 
@@ -61,19 +65,23 @@ constexpr int kOffStage = kOffQ + kQSmemAtoms * kQAtomBytes;
 constexpr int kMaxPos = 2048;                            // positions of one split (<= k)
 constexpr int kOffRows = kOffStage + 2 * kStageBytes;    // cache row of every position
 constexpr int kOffMask = kOffRows + kMaxPos * 4;         // validity bits, 32 per word
-constexpr int kOffBar = kOffMask + (kMaxPos / 32) * 4;
+constexpr int kOffXchg = kOffMask + (kMaxPos / 32) * 4;    // softmax groups' exchange, 2 KB
+constexpr int kOffBar = kOffXchg + 2 * 2 * 128 * 4;
 constexpr int kNumBars = 12;
 constexpr int kQStageAtoms = 4;                            // q dims [0, 256) via stage 1
 constexpr int kOffSlot = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;
 constexpr int kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 256;
-constexpr int kSoftWarp0 = 4;
-constexpr int kLoaderWarps = 3;                            // warps 0, 2, 3
+constexpr int kThreads = 512;
+constexpr int kSoftThreads = 256;                          // warps 4-7 and 12-15
+constexpr int kLoaderWarps = 7;                            // warps 0, 2, 3, 8-11
 constexpr int kGathers = (kBN / 4) * kAtoms;               // 144 gather4 copies per tile
-constexpr int kORowPitch = 256 * 4 + 16;                   // staged Mid_O row (epilogue)
-static_assert(128 * kORowPitch <= 2 * kStageBytes, "Mid_O staging fits in the key stages");
+constexpr int kIssuers = kGathers / 2;                     // copies (and issuers) per CTA
+constexpr int kResolveBatch = 4;                           // position groups in flight per loader
+constexpr int kOBoxBytes = 32 * 128;                       // Mid_O box: 32 heads x 32 fp32
+constexpr int kOChunkBytes = 4 * kOBoxBytes;               // the 4 warps' boxes of a chunk
+static_assert(8 * kOChunkBytes <= 2 * kStageBytes, "Mid_O staging fits in the key stages");
 constexpr float kRescaleLog2 = 8.0f;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -83,7 +91,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                      const __grid_constant__ CUtensorMap tmap_kv, const MlaLaunch p) {
+                      const __grid_constant__ CUtensorMap tmap_kv,
+                      const __grid_constant__ CUtensorMap tmap_o, const MlaLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   const int split = blockIdx.x >> 1, half = blockIdx.x & 1, t = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -130,15 +139,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(Q_FULL, 1);
-    mbar_init(Q_TMEM, 128);
+    mbar_init(Q_TMEM, kSoftThreads);
     mbar_init(S_FULL, 1);
-    mbar_init(S_FREE, 128);
-    mbar_init(P_FULL, 128);
+    mbar_init(S_FREE, kSoftThreads);
+    mbar_init(P_FULL, kSoftThreads);
     mbar_init(PV_DONE, 1);
     mbar_init(Q_STAGE, 1);
     mbar_init(Q_PEER, 1);                         // the peer's softmax read its q staging
     for (int s = 0; s < 2; ++s) {
-      mbar_init(KV_FULL(s), kLoaderWarps * 32);   // one expect-tx arrive per loader thread
+      mbar_init(KV_FULL(s), kIssuers);            // one expect-tx arrive per issuing thread
       mbar_init(KV_EMPTY(s), 2);                  // both CTAs' MMAs done with the stage
     }
     fence_mbar_init();
@@ -153,13 +162,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_launch();
   cluster_sync();   // both CTAs' barriers exist before any copy or arrive targets them
 
-  if (warp == 0 || warp == 2 || warp == 3) {
+  if (warp == 0 || warp == 2 || warp == 3 || (warp >= 8 && warp < 12)) {
     // ------------------------------------------------------------ loaders
-    // Three warps (96 threads) gather the selected latent rows with TMA
-    // gather4 copies into the 128B-swizzled stage layout; each thread
+    // Seven warps resolve the positions; 72 of their threads, spread evenly
+    // over the seven warps, gather the selected latent rows with TMA gather4
+    // copies into the 128B-swizzled stage layout; each issuing thread
     // announces its own bytes on the stage's full barrier, then issues.
-    const int lw = warp == 0 ? 0 : warp - 1;           // loader warp 0..2
+    const int lw = warp == 0 ? 0 : (warp < 4 ? warp - 1 : warp - 5);   // loader warp 0..6
     const int ltid = lw * 32 + lane;
+    const int gi = lane * kLoaderWarps + lw;   // this thread's copy of the tile (if < kIssuers)
     const int* ptab = p.page_table + static_cast<long long>(r) * p.max_pages;
     const int* idx_row = p.topk_idx + static_cast<long long>(t) * k;
     // Queries, page table and cache are inputs of the layer; only the
@@ -168,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ltid == 0) {
       prefetch_tmap(&tmap_q);
       prefetch_tmap(&tmap_kv);
+      prefetch_tmap(&tmap_o);
       mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
       mbar_expect_tx(Q_STAGE, kQStageAtoms * kQAtomBytes);
       const uint64_t pol_q = policy_evict_last();
@@ -186,21 +198,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dep_wait();
     // Resolve every position of the split first (logical index -> page table
     // -> cache row).  Groups of 32 positions go round-robin to the three
-    // warps, 8 groups per batch so the loads overlap.
+    // warps, 4 groups per batch so the loads overlap.
     const int npos = ntiles * kBN;
-    for (int g0 = lw; 32 * g0 < npos; g0 += kLoaderWarps * 8) {
-      int idx[8];
+    for (int g0 = lw; 32 * g0 < npos; g0 += kLoaderWarps * kResolveBatch) {
+      int idx[kResolveBatch];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kResolveBatch; ++u) {
         const int i = 32 * (g0 + kLoaderWarps * u);
         const int pos = start + i + lane;
         idx[u] = (i < npos && pos < end) ? __ldg(idx_row + pos) : -1;
       }
-      int pg[8];
+      int pg[kResolveBatch];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) pg[u] = (idx[u] >= 0 && idx[u] < vis) ? __ldg(ptab + (idx[u] >> 6)) : -1;
+      for (int u = 0; u < kResolveBatch; ++u) pg[u] = (idx[u] >= 0 && idx[u] < vis) ? __ldg(ptab + (idx[u] >> 6)) : -1;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kResolveBatch; ++u) {
         const int i = 32 * (g0 + kLoaderWarps * u);
         if (i >= npos) break;
         const int pos = start + i + lane;
@@ -218,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(1, kLoaderWarps * 32);   // rows_s / mask_s complete
     const uint64_t pol_kv = policy_evict_last();   // the sibling half reads the same rows
     int issued = 0;
-    for (int it = 0; it < ntiles; ++it) {
+    for (int it = 0; it < ntiles && gi < kIssuers; ++it) {
       const int st = it & 1;
       if (it >= 2 && !mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1)) {
         raise_error(kErrTimeout);
@@ -232,18 +244,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Copy c = 9 g + a brings rows 4g..4g+3 of the tile, dims [64a, 64a+64),
       // to atom a at byte 512 g of both CTAs (the copy engine applies the 128B
-      // swizzle); this CTA issues the copies c = crank mod 2, 72 loaders one
-      // each.  Every loader announces 1/96 of the tile's bytes.
+      // swizzle); this CTA issues the copies c = crank mod 2, one per issuing
+      // thread, each announcing 1/72 of the bytes landing here.
       const uint32_t dst = sbase + kOffStage + st * kStageBytes;
       const int* rows = rows_s + it * kBN;
-      mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(kStageBytes / (kLoaderWarps * 32)));
-      const int c = 2 * ltid + static_cast<int>(crank);
-      if (c < kGathers) {
-        const int g = c / kAtoms, a = c - g * kAtoms;
-        const int* r4 = rows + 4 * g;
-        tma_gather4_mc(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r4[0], r4[1], r4[2], r4[3],
-                       KV_FULL(st), kBoth, pol_kv);
-      }
+      mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(kStageBytes / kIssuers));
+      const int c = 2 * gi + static_cast<int>(crank);
+      const int g = c / kAtoms, a = c - g * kAtoms;
+      const int* r4 = rows + 4 * g;
+      tma_gather4_mc(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r4[0], r4[1], r4[2], r4[3],
+                     KV_FULL(st), kBoth, pol_kv);
       issued = it + 1;
     }
     // No copy may still be in flight when the CTA exits: the last phase of
@@ -263,32 +273,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = make_idesc(1, 1, 0, 1, 256, 128);
       const uint32_t tS = tmem + kColS, tO = tmem + kColO, tP = tmem + kColP, tQ = tmem + kColQ;
       bool ok = mbar_wait(Q_FULL, 0) && mbar_wait(Q_TMEM, 0);
-      int pv_issued = 0;
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(P_FULL, i & 1)) return false;
+      // P V of tile i goes out as soon as the softmax wrote P(i), also between
+      // the MMAs of a later tile's Q K^T: it frees the stage that the gather
+      // of tile i + 2 waits for, so the gathers do not queue behind the
+      // arrival of the next tile.
+      int npv = 0;
+      auto pv_ready = [&](int nqk) { return npv < nqk && mbar_test_wait(P_FULL, npv & 1); };
+      auto issue_pv = [&]() {
         tc_fence_after();
-        const uint32_t stage = sbase + kOffStage + (i & 1) * kStageBytes + 4 * half * kAtomBytes;
+        const uint32_t stage = sbase + kOffStage + (npv & 1) * kStageBytes + 4 * half * kAtomBytes;
 #pragma unroll
         for (int j = 0; j < kBN / 16; ++j)
           mma_f16_ts(tO, tP + 8 * j, smem_desc_sw128(stage + j * 2048, kAtomBytes, 1024), idesc_pv,
-                     (i > 0 || j > 0) ? 1u : 0u);
-        // The stage is reused by tile i + 2 (if any), whose copies land in
+                     (npv > 0 || j > 0) ? 1u : 0u);
+        // The stage is reused by tile npv + 2 (if any), whose copies land in
         // both CTAs: both MMAs must be done with it.
-        if (i + 2 < ntiles) tc_commit_mc(KV_EMPTY(i & 1), kBoth);
+        if (npv + 2 < ntiles) tc_commit_mc(KV_EMPTY(npv & 1), kBoth);
         tc_commit(PV_DONE);
-        ++pv_issued;
-        return true;
+        ++npv;
       };
       for (int it = 0; it < ntiles && ok; ++it) {
         const int st = it & 1;
-        if (!mbar_wait(KV_FULL(st), (it >> 1) & 1)) { ok = false; break; }
-        if (it >= 1 && !mbar_wait(S_FREE, (it - 1) & 1)) { ok = false; break; }
+        // Tile it needs its keys and the softmax done reading S(it - 1).
+        const long long t0 = clock64();
+        for (;;) {
+          if (pv_ready(it)) {
+            issue_pv();
+            continue;
+          }
+          if (mbar_test_wait(KV_FULL(st), (it >> 1) & 1) &&
+              (it == 0 || mbar_test_wait(S_FREE, (it - 1) & 1)))
+            break;
+          if (clock64() - t0 > kWaitCycles) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
         tc_fence_after();
         const uint32_t stage = sbase + kOffStage + st * kStageBytes;
 #pragma unroll
-        for (int j = 0; j < kQTmemDims / 16; ++j)
+        for (int j = 0; j < kQTmemDims / 16; ++j) {
           mma_f16_ts(tS, tQ + 8 * j, smem_desc_sw128(stage + (j >> 2) * kAtomBytes + (j & 3) * 32, 16, 1024),
                      idesc_qk, j > 0 ? 1u : 0u);
+          if ((j & 7) == 7 && pv_ready(it)) issue_pv();
+        }
 #pragma unroll
         for (int j = kQTmemDims / 16; j < kLatentDim / 16; ++j) {
           const int jq = j - kQTmemDims / 16;
@@ -296,35 +325,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                      smem_desc_sw128(sbase + kOffQ + (jq >> 2) * kQAtomBytes + (jq & 3) * 32, 16, 1024),
                      smem_desc_sw128(stage + (j >> 2) * kAtomBytes + (j & 3) * 32, 16, 1024),
                      idesc_qk, 1u);
+          if ((j & 7) == 7 && pv_ready(it)) issue_pv();
         }
         tc_commit(S_FULL);
-        if (it >= 1 && !issue_pv(it - 1)) { ok = false; break; }
       }
-      if (ok && !issue_pv(ntiles - 1)) ok = false;
+      while (ok && npv < ntiles) {
+        if (!mbar_wait(P_FULL, npv & 1)) {
+          ok = false;
+          break;
+        }
+        issue_pv();
+      }
       if (!ok) raise_error(kErrTimeout);
+      const int pv_issued = npv;
       if (pv_issued > 0) mbar_wait(PV_DONE, (pv_issued - 1) & 1);
     }
     __syncwarp();
-  } else if (warp >= kSoftWarp0) {
+  } else {
     // ------------------------------------------------------------ softmax
-    const int q4 = warp - kSoftWarp0;
+    // Two groups of four warps share the heads: group sg (warps 4-7 or
+    // 12-15) owns key columns [32 sg, 32 sg + 32) of each tile, the value
+    // dims [128 sg, 128 sg + 128) of the rescale and the epilogue.  A thread
+    // and its partner (same head, other group) exchange the tile maximum
+    // through shared memory, so both take the same lazy-rescale decision.
+    // Every named barrier below is passed once per tile by all 256 threads,
+    // also after a failed wait (which only clears `ok`).
+    const int sg = warp >> 3;
+    const int q4 = warp & 3;
     const int h = q4 * 32 + lane;
     const uint32_t lanebase = static_cast<uint32_t>(q4 * 32) << 16;
     const bool live = h < H;
+    bool ok = true;
     // q dims [0, 320) -> TMEM columns [kColQ, kColQ + 160): dims [0, 256)
-    // from the TMA copy in stage 1 (row h of each 128B-swizzled atom), dims
-    // [256, 320) loaded here.
+    // from the TMA copy in stage 1 (row h of each 128B-swizzled atom; group
+    // sg moves atoms 2 sg and 2 sg + 1), dims [256, 320) loaded by group 1.
     {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<long long>(t) * H + (live ? h : 0)) * kLatentDim) +
-          kQStageAtoms * 8;
       uint4 qv[8];
+      if (sg == 1) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (static_cast<long long>(t) * H + (live ? h : 0)) * kLatentDim) +
+            kQStageAtoms * 8;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) qv[u] = live ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-      bool qok = mbar_wait(Q_STAGE, 0);
+        for (int u = 0; u < 8; ++u) qv[u] = live ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (!mbar_wait(Q_STAGE, 0)) ok = false;
       const uint8_t* qs = smem + kOffStage + kStageBytes + h * 128;
 #pragma unroll 1
-      for (int c = 0; c < kQStageAtoms; ++c) {
+      for (int c = 2 * sg; c < 2 * sg + 2; ++c) {
         uint32_t rr[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -336,54 +383,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tmem + lanebase + kColQ + 32 * c, rr);
       }
-      uint32_t rr[32];
+      if (sg == 1) {
+        uint32_t rr[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        rr[4 * u + 0] = qv[u].x;
-        rr[4 * u + 1] = qv[u].y;
-        rr[4 * u + 2] = qv[u].z;
-        rr[4 * u + 3] = qv[u].w;
+        for (int u = 0; u < 8; ++u) {
+          rr[4 * u + 0] = qv[u].x;
+          rr[4 * u + 1] = qv[u].y;
+          rr[4 * u + 2] = qv[u].z;
+          rr[4 * u + 3] = qv[u].w;
+        }
+        tmem_st32(tmem + lanebase + kColQ + 32 * kQStageAtoms, rr);
       }
-      tmem_st32(tmem + lanebase + kColQ + 32 * kQStageAtoms, rr);
-      if (!qok) raise_error(kErrTimeout);
       tc_fence_before();
       mbar_arrive(Q_TMEM);
-      named_bar_sync(2, 128);   // this CTA's softmax threads all read stage 1
-      if (h == 0) mbar_arrive_remote(mapa_shared(Q_PEER, peer));
+      named_bar_sync(2, kSoftThreads);   // this CTA's softmax threads all read stage 1
+      if (threadIdx.x == 128) mbar_arrive_remote(mapa_shared(Q_PEER, peer));
     }
+    float* xchg = reinterpret_cast<float*>(smem + kOffXchg);   // [2 parities][2 groups][128 heads]
     const float sc = p.sm_scale * 1.4426950408889634f;  // exp -> exp2
     float mrun = ninf, lrun = 0.f;
-    bool ok = true;
     for (int it = 0; it < ntiles; ++it) {
       const int st = it & 1;
-      if (!mbar_wait(S_FULL, it & 1) || !mbar_wait(KV_FULL(st), (it >> 1) & 1)) { ok = false; break; }
+      if (ok && !(mbar_wait(S_FULL, it & 1) && mbar_wait(KV_FULL(st), (it >> 1) & 1))) ok = false;
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld64(tmem + lanebase + kColS, sr);
+      uint32_t sr[32];
+      tmem_ld32(tmem + lanebase + kColS + 32 * sg, sr);
       tc_fence_before();
       mbar_arrive(S_FREE);
-      const unsigned long long msk = static_cast<unsigned long long>(mask_s[2 * it]) |
-                                     (static_cast<unsigned long long>(mask_s[2 * it + 1]) << 32);
-      float x[64];
+      const uint32_t msk = mask_s[2 * it + sg];
+      float x[32];
       float tmax = ninf;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        x[j] = ((msk >> j) & 1ull) ? __uint_as_float(sr[j]) * sc : ninf;
+      for (int j = 0; j < 32; ++j) {
+        x[j] = ((msk >> j) & 1u) ? __uint_as_float(sr[j]) * sc : ninf;
         tmax = fmaxf(tmax, x[j]);
       }
-      if (it >= 1) {
-        if (!mbar_wait(PV_DONE, (it - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-      }
+      // Tile maximum of the head over both groups' columns.
+      xchg[((it & 1) * 2 + sg) * 128 + h] = tmax;
+      named_bar_sync(3, kSoftThreads);
+      tmax = fmaxf(tmax, xchg[((it & 1) * 2 + (sg ^ 1)) * 128 + h]);
+      if (it >= 1 && ok && !mbar_wait(PV_DONE, (it - 1) & 1)) ok = false;
+      tc_fence_after();
       const bool raise = tmax > mrun + kRescaleLog2;
       const float mnew = raise ? tmax : mrun;
-      // O holds a partial sum under the old maximum: rescale it (warp-wide,
-      // since TMEM loads and stores are warp-collective).
+      // O holds a partial sum under the old maximum: rescale this group's
+      // half of it (warp-wide, since TMEM loads and stores are warp-collective).
       const bool need = raise && mrun > ninf;
       if (__any_sync(0xffffffffu, need)) {
         const float f = need ? exp2f(mrun - mnew) : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 4 * sg; c < 4 * sg + 4; ++c) {
           uint32_t o[32];
           tmem_ld32(tmem + lanebase + kColO + 32 * c, o);
 #pragma unroll
@@ -393,52 +442,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         lrun *= f;
       }
       mrun = mnew;
-      uint32_t pk[32];
+      uint32_t pk[16];
       float ls = 0.f;
       const bool any = mrun > ninf;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
+      for (int jj = 0; jj < 16; ++jj) {
         const float p0 = any ? exp2f(x[2 * jj] - mrun) : 0.f;
         const float p1 = any ? exp2f(x[2 * jj + 1] - mrun) : 0.f;
         pk[jj] = pack_bf16x2(p0, p1);
         ls += bf16lo_to_f32(pk[jj]) + bf16hi_to_f32(pk[jj]);
       }
       lrun += ls;
-      tmem_st32(tmem + lanebase + kColP, pk);
+      tmem_st16(tmem + lanebase + kColP + 16 * sg, pk);
       tc_fence_before();
       mbar_arrive(P_FULL);
     }
-    if (!ok) raise_error(kErrTimeout);
-    if (ok) ok = mbar_wait(PV_DONE, (ntiles - 1) & 1);
+    if (ok && !mbar_wait(PV_DONE, (ntiles - 1) & 1)) ok = false;
     tc_fence_after();
-    // epilogue: O / l -> Mid_O, log-sum-exp -> Mid_LSE.  Each thread owns
-    // one head's 1 KB row of Mid_O; it stages the row in shared memory (the
-    // key stages are idle once the last P V is done) and writes it with one
-    // bulk copy, instead of 64 scattered 16-byte stores per thread.
-    const float inv = (ok && lrun > 0.f) ? 1.f / lrun : 0.f;
-    // Row pitch 1040 B: eight consecutive threads' 16-byte stores hit
-    // distinct banks.
-    const uint32_t orow = sbase + kOffStage + static_cast<uint32_t>(h) * kORowPitch;
-    uint8_t* orow_p = smem + kOffStage + h * kORowPitch;
+    // Row sum over both groups' columns (parity slot 0 or 1 is free again:
+    // both groups passed the last tile's barrier after reading it).
+    float* lx = xchg + (ntiles & 1) * 256;
+    lx[sg * 128 + h] = ok ? lrun : -1.f;
+    named_bar_sync(3, kSoftThreads);
+    const float lo = lx[(sg ^ 1) * 128 + h];
+    ok = ok && lo >= 0.f;
+    const float ltot = lrun + lo;
+    if (!ok) raise_error(kErrTimeout);
+    // epilogue: O / l -> Mid_O, log-sum-exp -> Mid_LSE.  Each warp owns 32
+    // heads and its group's four 32-column chunks; per chunk it stages its
+    // 32 x 128 B box in shared memory (the key stages are idle once the last
+    // P V is done), 128B-swizzled so that eight consecutive rows' 16-byte
+    // stores hit distinct banks, and one lane writes the box with a tensor
+    // store (rows past H are clipped).  One TMA instruction per 4 KB instead
+    // of one per thread and 1 KB: the copy engine takes a warp's TMA
+    // instructions one lane at a time.
+    const float inv = (ok && ltot > 0.f) ? 1.f / ltot : 0.f;
+    const bool warp_live = q4 * 32 < H;
+    const uint32_t box0 = sbase + kOffStage + static_cast<uint32_t>(q4) * kOBoxBytes;
+    uint8_t* box0_p = smem + kOffStage + q4 * kOBoxBytes;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * sg; c < 4 * sg + 4; ++c) {
       uint32_t o[32];
       tmem_ld32(tmem + lanebase + kColO + 32 * c, o);
-      float4* d4 = reinterpret_cast<float4*>(orow_p + 128 * c);
+      uint8_t* row_p = box0_p + c * kOChunkBytes + lane * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        d4[u] = make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
-                            __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+        *reinterpret_cast<float4*>(row_p + ((u ^ (lane & 7)) << 4)) =
+            make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                        __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+      fence_proxy_async_smem();   // generic-proxy writes -> tensor-store reads
+      __syncwarp();
+      if (warp_live && lane == 0) {
+        tma_store_4d(&tmap_o, box0 + c * kOChunkBytes, 256 * half + 32 * c, split, q4 * 32, t);
+        bulk_commit();
+      }
     }
-    if (live) {
-      fence_proxy_async_smem();   // generic-proxy writes -> bulk-copy reads
-      bulk_store(out_base + static_cast<long long>(h) * S * kVDim, orow, 256 * 4);
-      bulk_commit();
-      bulk_wait_read_all();
-    }
-    if (live && half == 0)
+    if (warp_live && lane == 0) bulk_wait_read_all();
+    if (live && half == 0 && sg == 0)
       p.mid_lse[(static_cast<long long>(t) * H + h) * S + split] =
-          (ok && lrun > 0.f) ? (mrun + log2f(lrun)) * 0.6931471805599453f : ninf;
+          (ok && ltot > 0.f) ? (mrun + log2f(ltot)) * 0.6931471805599453f : ninf;
   }
   // Neither CTA leaves while the other may still signal or copy into it.
   cluster_sync();
@@ -463,12 +525,24 @@ cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
                       static_cast<uint64_t>(a.num_pages) * kPage, kLatentDim * 2, 64, 1,
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  // Mid_O [T][H][S][512] fp32 as a 4-D map; a box is 32 dims x 1 split x 32
+  // heads x 1 row, 128B-swizzled.
+  CUtensorMap to;
+  {
+    const uint64_t T = static_cast<uint64_t>(a.batch) * a.nq, S = a.num_splits, H = a.heads;
+    const uint64_t dims[4] = {kVDim, S, H, T};
+    const uint64_t strides[3] = {kVDim * 4, S * kVDim * 4, H * S * kVDim * 4};
+    const uint32_t box[4] = {32, 1, 32, 1};
+    if (!encode_tmap_nd(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.mid_o, 4, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.num_splits, a.batch * a.nq);
   return launch_kernel(sparse_mla_kernel, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0,
-                       2, tq, tkv, a);
+                       2, tq, tkv, to, a);
 }
 
 }  // namespace dsa
