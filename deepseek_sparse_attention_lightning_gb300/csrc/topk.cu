@@ -9,20 +9,21 @@
 //   pass 1  histogram of the top 11 key bits per row (fused into the indexer
 //           epilogue on the fused path, else topk_hist_kernel);
 //   pass 2  topk_select_kernel: each row is one cluster of 16 CTAs, CTA x
-//           owning chunk x of the row (8192, 16384 or 32768 positions, 16, 32
-//           or 64 consecutive ones per thread).  Every CTA finds the bin b*
-//           where the count from the top crosses k, marks the positions above
-//           b* in its shared-memory slice of the selection bitmap and stores
-//           the positions in b* as candidates in its own slice of a global
-//           list.  After a cluster barrier, CTA 0 resolves the candidates
-//           with more radix levels over the remaining 21 key bits (a pairwise
-//           rank once few are left, a radix select over the position for
-//           exact ties) into one threshold (key, position): a candidate is in
-//           iff its key is larger, or equal with a position not larger.
-//           After a second barrier every CTA marks its own winners, the CTAs
-//           exchange their selected counts through distributed shared
-//           memory, and each writes its chunk's positions, ascending, at its
-//           offset in the row.
+//           owning chunk x of the row (8192, 16384 or 32768 positions; a
+//           warp's score loads are 512 consecutive bytes).  Every CTA finds
+//           the bin b* where the count from the top crosses k, marks the
+//           positions above b* in its shared-memory slice of the selection
+//           bitmap and keeps the positions in b* as candidates in its own
+//           shared memory (the rare excess over 512 in a global list).  After
+//           a cluster barrier, CTA 0 reads every CTA's candidates through
+//           distributed shared memory and resolves them with more radix
+//           levels over the remaining 21 key bits (a pairwise rank once few
+//           are left, a radix select over the position for exact ties) into
+//           one threshold (key, position): a candidate is in iff its key is
+//           larger, or equal with a position not larger.  After a second
+//           barrier every CTA marks its own winners, the CTAs exchange their
+//           selected counts through distributed shared memory, and each
+//           writes its chunk's positions, ascending, at its offset in the row.
 #include <algorithm>
 #include <mutex>
 
@@ -37,13 +38,15 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kPairMax = 128;                         // sub-candidates ranked pairwise
-constexpr int kOffHist = 0;                           // 2048 x u32
-constexpr int kOffCand = kOffHist + kHistBins * 4;    // kTopkChunk x uint2 (resolver)
-constexpr int kOffSub = kOffCand + kTopkChunk * 8;    // kPairMax x uint2
+constexpr int kOffHist = 0;                           // 2048 x u32: the row histogram
+constexpr int kOffLvl = kOffHist + kHistBins * 4;     // 2048 x u32: (CTA 0) first resolve level
+constexpr int kCandSlot = kTopkChunk / 16;            // candidates per chunk kept in shared memory
+static_assert(kCandSlot == kThreads, "one candidate slot per thread");
+constexpr int kOffCand = kOffLvl + kHistBins * 4;     // kCandSlot x uint2: this chunk's candidates
+constexpr int kOffSub = kOffCand + kCandSlot * 8;     // kPairMax x uint2
 constexpr int kOffBits = kOffSub + kPairMax * 8;      // this chunk's bitmap words
 constexpr int kMaxChunkMul = 4;                       // chunk = 8192 x {1, 2, 4}
-constexpr int kCandSlot = kTopkChunk / 16;            // candidates per chunk kept in CTA 0's smem
-constexpr int kSmemBytes = kOffBits + (kTopkChunk * kMaxChunkMul / 32) * 4;   // 84 KB
+constexpr int kSmemBytes = kOffBits + (kTopkChunk * kMaxChunkMul / 32) * 4;   // 25 KB
 
 __device__ __forceinline__ int visible(const int32_t* seqlens, int t, int nq) {
   return seqlens[t / nq] - (nq - 1 - t % nq);
@@ -160,16 +163,16 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int C = kThreads * P;      // positions per CTA
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* sh = reinterpret_cast<uint32_t*>(smem + kOffHist);
+  uint32_t* slv = reinterpret_cast<uint32_t*>(smem + kOffLvl);
   uint2* scand = reinterpret_cast<uint2*>(smem + kOffCand);
   uint2* sub = reinterpret_cast<uint2*>(smem + kOffSub);
   uint32_t* sbits = reinterpret_cast<uint32_t*>(smem + kOffBits);
   __shared__ uint32_t scratch[40];
   __shared__ int res[2];
-  __shared__ int s_info[4];   // candidates of this CTA, -, -, sub count
-  __shared__ int s_pref[kTopkClusterCtas + 1];
+  __shared__ int s_info[4];   // candidates of this CTA, (CTA 0) all candidates, overflow, sub count
   __shared__ uint32_t s_thr[2];   // the threshold (key, position), pushed by CTA 0
   __shared__ uint32_t s_allsel[kTopkClusterCtas];   // every chunk's selected count, pushed by each
-  __shared__ uint32_t s_ccnt[kTopkClusterCtas];   // (CTA 0) every chunk's candidate count
+  __shared__ uint32_t s_ccnt[kTopkClusterCtas];   // (CTA 0) every chunk's candidate count, pushed by each
 
   // Everything this kernel reads may come from the kernel before it.
   grid_dep_wait();
@@ -194,24 +197,37 @@ __global__ void __launch_bounds__(kThreads)
   uint2* cand_row = p.cand + static_cast<long long>(t) * p.ld;
   const int lo = x * C;
   const int hi = has ? min(vis, lo + C) : lo;
-  const int s0 = lo + P * static_cast<int>(threadIdx.x);
 
-  // ---- scores of this thread's P positions (through L1: a warp's loads
-  //      share cache lines), in flight together with the row histogram.
+  // ---- scores: this thread's float4 f = threadIdx.x + kThreads * q holds
+  //      positions lo + 4 f .. lo + 4 f + 3, so a warp's loads are 512
+  //      consecutive bytes (four whole cache lines per instruction).
+  constexpr int Q = P / 4;
   const float* row = p.logits + static_cast<long long>(t) * p.ld;
+  auto pos_of = [&](int q) { return lo + 4 * (static_cast<int>(threadIdx.x) + kThreads * q); };
   float v[P];
-  if (s0 + P <= hi) {
 #pragma unroll
-    for (int q = 0; q < P / 4; ++q) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(row + s0) + q);
+  for (int q = 0; q < Q; ++q) {
+    const int pq = pos_of(q);
+    if (pq + 4 <= hi) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + pq));
       v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-    }
-  } else {
+    } else {
 #pragma unroll
-    for (int j = 0; j < P; ++j) v[j] = s0 + j < hi ? __ldg(row + s0 + j) : 0.f;
+      for (int b = 0; b < 4; ++b) v[4 * q + b] = pq + b < hi ? __ldg(row + pq + b) : 0.f;
+    }
   }
+  if (x == 0)   // the first resolve level's histogram, ready before it is needed
+    for (int i = threadIdx.x; i < kHistBins; i += kThreads) slv[i] = 0u;
+  // The histogram's four words per thread are all in flight before any is
+  // stored (one round trip instead of four).
   const uint32_t* gh = p.hist + static_cast<long long>(t) * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = __ldcg(gh + i);
+  {
+    uint32_t hv[kHistBins / kThreads];
+#pragma unroll
+    for (int u = 0; u < kHistBins / kThreads; ++u) hv[u] = __ldcg(gh + threadIdx.x + u * kThreads);
+#pragma unroll
+    for (int u = 0; u < kHistBins / kThreads; ++u) sh[threadIdx.x + u * kThreads] = hv[u];
+  }
   if (threadIdx.x == 0) s_info[0] = 0;
   __syncthreads();
   // ---- threshold bin b*: the count of scores in bins above it (nabove) is
@@ -225,31 +241,29 @@ __global__ void __launch_bounds__(kThreads)
   }
   const uint32_t ub = static_cast<uint32_t>(bstar);
   // ---- classify: positions above b* -> this chunk's bitmap words, those in
-  //      b* -> this chunk's slice of the candidate list (global).
+  //      b* -> candidates.  Bit 4 (q mod 4) + b of inbin[q / 4] is position
+  //      pos_of(q) + b.  Bitmap word 64 q + threadIdx.x / 8 holds the nibbles
+  //      of eight consecutive threads (four positions each).
   uint32_t inbin[M];
 #pragma unroll
-  for (int h = 0; h < M; ++h) {
+  for (int h = 0; h < M; ++h) inbin[h] = 0u;
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    const int pq = pos_of(q);
     uint32_t above = 0, in = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int jj = 16 * h + j;
-      if (s0 + jj < hi) {
-        const uint32_t bin = float_key(v[jj]) >> kHistShift;
-        if (bin > ub) above |= 1u << j;
-        else if (bin == ub) in |= 1u << j;
+    for (int b = 0; b < 4; ++b)
+      if (pq + b < hi) {
+        const uint32_t bin = float_key(v[4 * q + b]) >> kHistShift;
+        if (bin > ub) above |= 1u << b;
+        else if (bin == ub) in |= 1u << b;
       }
-    }
-    inbin[h] = in;
-    // 16-bit half h of this thread's positions; thread pairs fill a word
-    // when P = 16, else the thread owns whole words.
-    if (M == 1) {
-      const uint32_t upper = __shfl_down_sync(0xffffffffu, above, 1);
-      if ((threadIdx.x & 1) == 0) sbits[threadIdx.x >> 1] = above | (upper << 16);
-    } else {
-      const int wi = static_cast<int>(threadIdx.x) * (P / 32) + (h >> 1);
-      if ((h & 1) == 0) sbits[wi] = above;
-      else sbits[wi] |= above << 16;
-    }
+    inbin[q >> 2] |= in << (4 * (q & 3));
+    uint32_t w = above << (4 * (lane & 7));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    w |= __shfl_xor_sync(0xffffffffu, w, 4);
+    if ((lane & 7) == 0) sbits[64 * q + (threadIdx.x >> 3)] = w;
   }
   int mine = 0;
 #pragma unroll
@@ -264,20 +278,19 @@ __global__ void __launch_bounds__(kThreads)
   if (lane == 31) wbase = atomicAdd(&s_info[0], incl);
   wbase = __shfl_sync(0xffffffffu, wbase, 31);
   {
-    // Candidate i of this chunk goes to CTA 0's shared memory at slot
-    // x * kCandSlot + i (if i < kCandSlot) and to this chunk's slice of the
-    // global list (read by CTA 0 only for a chunk with more candidates).
-    const uint32_t cand0 = mapa_shared(smem_u32(scand), 0);
+    // Candidate i of this chunk goes to its slot i of this CTA's shared
+    // memory if i < kCandSlot (CTA 0 reads the slots through distributed
+    // shared memory after the barrier), else to the chunk's global slice.
     int i = wbase + incl - mine;
 #pragma unroll
     for (int h = 0; h < M; ++h)
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         if ((inbin[h] >> j) & 1u) {
-          const int jj = 16 * h + j;
-          const uint2 c = make_uint2(float_key(v[jj]), static_cast<uint32_t>(s0 + jj));
-          cand_row[lo + i] = c;
-          if (i < kCandSlot) st_shared_cluster_v2(cand0 + 8u * (x * kCandSlot + i), c.x, c.y);
+          const int q = 4 * h + (j >> 2), b = j & 3;
+          const uint2 c = make_uint2(float_key(v[4 * q + b]), static_cast<uint32_t>(pos_of(q) + b));
+          if (i < kCandSlot) scand[i] = c;
+          else cand_row[lo + i] = c;
           ++i;
         }
   }
@@ -288,32 +301,55 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---- CTA 0 resolves the candidates of bin b* into the threshold.
   if (x == 0) {
-    {
+    if (threadIdx.x < 32) {
+      // All candidates of the row, and whether a chunk overflowed its slots.
       const uint32_t c = threadIdx.x < static_cast<unsigned>(nch) ? s_ccnt[threadIdx.x] : 0u;
-      const uint32_t e = block_excl_scan_512(c, scratch);
-      if (threadIdx.x <= static_cast<unsigned>(nch)) s_pref[threadIdx.x] = static_cast<int>(e);
-    }
-    if (threadIdx.x == 0) {
-      s_info[3] = 0;
-      s_thr[0] = 0xFFFFFFFFu;   // selects no candidate (error fallback)
-      s_thr[1] = 0u;
+      uint32_t tot = c, mx = c;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (threadIdx.x == 0) {
+        s_info[1] = static_cast<int>(tot);
+        s_info[2] = mx > static_cast<uint32_t>(kCandSlot) ? 1 : 0;
+        s_info[3] = 0;
+        s_thr[0] = 0xFFFFFFFFu;   // selects no candidate (error fallback)
+        s_thr[1] = 0u;
+      }
     }
     __syncthreads();
-    const int nc = s_pref[nch];
+    const int nc = s_info[1];
+    const bool over = s_info[2] != 0;
     bool ok = static_cast<uint32_t>(nc) == sh[ub];   // candidates agree with the histogram
-    auto chunk_of = [&](int e) -> int {
-      int a = 0, b = nch - 1;
-      while (a < b) {
-        const int m = (a + b + 1) >> 1;
-        if (s_pref[m] <= e) a = m; else b = m - 1;
-      }
-      return a;
+    // Candidates past a chunk's slots, from its global slice (rare).
+    auto for_each_overflow = [&](auto&& f) {
+      if (!over) return;
+      for (int cx = 0; cx < nch; ++cx)
+        for (int i = kCandSlot + static_cast<int>(threadIdx.x); i < static_cast<int>(s_ccnt[cx]);
+             i += kThreads)
+          f(__ldcg(cand_row + static_cast<long long>(cx) * C + i));
     };
-    // Candidate e: chunk c, index i; in shared memory if i < kCandSlot.
-    auto cget = [&](int e) -> uint2 {
-      const int c = chunk_of(e), i = e - s_pref[c];
-      return i < kCandSlot ? scand[c * kCandSlot + i]
-                           : __ldcg(cand_row + static_cast<long long>(c) * C + i);
+    // This thread's slot of every chunk, read from the chunk's CTA: the keys
+    // stay in registers for the histogram and collection passes (loaded
+    // together, not one per pass behind the previous pass's atomics).
+    const uint32_t slot = smem_u32(scand) + 8u * threadIdx.x;
+    uint32_t ck[kTopkClusterCtas];
+    uint32_t cvalid = 0;
+#pragma unroll
+    for (int cx = 0; cx < kTopkClusterCtas; ++cx) {
+      const bool in = cx < nch && threadIdx.x < s_ccnt[cx];
+      ck[cx] = in ? ld_shared_cluster_u32(mapa_shared(slot, cx)) : 0u;
+      cvalid |= (in ? 1u : 0u) << cx;
+    }
+    // Every candidate once (the slots, then the overflow).
+    auto for_each_cand = [&](auto&& f) {
+      for (int cx = 0; cx < nch; ++cx)
+        if (threadIdx.x < s_ccnt[cx]) {
+          const uint32_t a = mapa_shared(slot, cx);
+          f(make_uint2(ld_shared_cluster_u32(a), ld_shared_cluster_u32(a + 4)));
+        }
+      for_each_overflow(f);
     };
     // The need best candidates by (key desc, position asc).
     const uint32_t need = static_cast<uint32_t>(k - nabove);
@@ -327,17 +363,25 @@ __global__ void __launch_bounds__(kThreads)
     for (int lvl = 0; lvl < 2 && ok; ++lvl) {
       const int sh_ = kshift[lvl];
       const uint32_t dm = (1u << kwidth[lvl]) - 1u;
-      for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
-      __syncthreads();
-      for (int e = threadIdx.x; e < nc; e += kThreads) {
-        const uint32_t key = cget(e).x;
-        if ((key & kmask) == kprefix) atomicAdd(&sh[(key >> sh_) & dm], 1u);
+      // Level 0 counts into its own array (zeroed at the start); level 1
+      // reuses the row histogram's, no longer needed.
+      uint32_t* hl = lvl == 0 ? slv : sh;
+      if (lvl > 0) {
+        for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
+        __syncthreads();
       }
+#pragma unroll
+      for (int cx = 0; cx < kTopkClusterCtas; ++cx)
+        if (((cvalid >> cx) & 1u) && (ck[cx] & kmask) == kprefix)
+          atomicAdd(&hl[(ck[cx] >> sh_) & dm], 1u);
+      for_each_overflow([&](uint2 c) {
+        if ((c.x & kmask) == kprefix) atomicAdd(&hl[(c.x >> sh_) & dm], 1u);
+      });
       __syncthreads();
-      find_crossing(sh, need_l, true, res, scratch);
+      find_crossing(hl, need_l, true, res, scratch);
       if (res[0] < 0) { ok = false; break; }
       const uint32_t d = static_cast<uint32_t>(res[0]);
-      cnt_eq = sh[d];
+      cnt_eq = hl[d];
       need_l -= static_cast<uint32_t>(res[1]);
       kprefix |= d << sh_;
       kmask |= dm << sh_;
@@ -351,10 +395,14 @@ __global__ void __launch_bounds__(kThreads)
       // Of the candidates with the crossing digit (m <= kPairMax), the
       // need_l-th best by (key desc, position asc) is the threshold.
       const uint32_t hi_digits = kprefix >> 10;
-      for (int e = threadIdx.x; e < nc; e += kThreads) {
-        const uint2 c = cget(e);
+#pragma unroll
+      for (int cx = 0; cx < kTopkClusterCtas; ++cx)
+        if (((cvalid >> cx) & 1u) && (ck[cx] >> 10) == hi_digits)
+          sub[atomicAdd(&s_info[3], 1)] =
+              make_uint2(ck[cx], ld_shared_cluster_u32(mapa_shared(slot, cx) + 4u));
+      for_each_overflow([&](uint2 c) {
         if ((c.x >> 10) == hi_digits) sub[atomicAdd(&s_info[3], 1)] = c;
-      }
+      });
       __syncthreads();
       const int m = s_info[3];
       for (int i = threadIdx.x; i < m; i += kThreads) {
@@ -382,10 +430,9 @@ __global__ void __launch_bounds__(kThreads)
           const uint32_t dm = (1u << iwidth[lvl]) - 1u;
           for (int i = threadIdx.x; i < kHistBins; i += kThreads) sh[i] = 0u;
           __syncthreads();
-          for (int e = threadIdx.x; e < nc; e += kThreads) {
-            const uint2 c = cget(e);
+          for_each_cand([&](uint2 c) {
             if (c.x == kstar && (c.y & imask) == iprefix) atomicAdd(&sh[(c.y >> sh_) & dm], 1u);
-          }
+          });
           __syncthreads();
           find_crossing(sh, need_i, false, res, scratch);
           if (res[0] < 0) { ok = false; break; }
@@ -412,13 +459,14 @@ __global__ void __launch_bounds__(kThreads)
   }
   cluster_sync();   // #2: every CTA has the threshold
 
-  // ---- every CTA: its winners among its candidates, then its selected count.
+  // ---- every CTA: its winners among its candidates (its own slots, then
+  //      the global overflow), then its selected count.
   const uint32_t tkey = s_thr[0];
   const uint32_t tpos = s_thr[1];
   if (has) {
     const int nmine = s_info[0];
     for (int e = threadIdx.x; e < nmine; e += kThreads) {
-      const uint2 c = __ldcg(cand_row + lo + e);
+      const uint2 c = e < kCandSlot ? scand[e] : __ldcg(cand_row + lo + e);
       if (c.x > tkey || (c.x == tkey && c.y <= tpos)) {
         const int off = static_cast<int>(c.y) - lo;
         atomicOr(&sbits[off >> 5], 1u << (off & 31));
