@@ -365,7 +365,10 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
   cudaError_t e = dsa::launch_sparse_mla(ma, s);
   if (e != cudaSuccess || !mark(3)) return DSA_ERR_CUDA;
   if (splits > 1) {
-    e = dsa::launch_merge(T * d->num_heads, splits, ma.mid_o, ma.mid_lse, out, nullptr, s, true);
+    // A plain launch: launched early, the merge's CTAs would sit on the
+    // attention's SMs (they need no shared memory) while it runs, and the
+    // layer measured ~1 us slower.
+    e = dsa::launch_merge(T * d->num_heads, splits, ma.mid_o, ma.mid_lse, out, nullptr, s, false);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
   }
   if (!mark(4)) return DSA_ERR_CUDA;
