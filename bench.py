@@ -6,11 +6,14 @@
 
 Prints ONE JSON line (rank 0).  A step is one pass of the whole decode layer
 over one synthetic batch (default: 8 requests x 131072 cached tokens, one
-query token each, k = 2048, 128 MLA heads), inputs resident in HBM.  Every
-step (one dsa_decode_fused call: workspace clear and the four kernels,
-captured once into a CUDA graph and replayed) is timed with one pair of CUDA
-events on the launching stream; L2 is flushed (a 256 MB write) between steps,
-outside the timed events.  A separate pass through the library's timed entry
+query token each, k = 2048, 128 MLA heads), inputs resident in HBM.  A step
+is one dsa_decode_fused call (workspace clear and the four kernels).  The K
+timed steps run back to back as the layers of a decode step do, each on its
+own copy of the inputs (8 copies in turn, so no step finds its inputs in L2;
+no flush), from CUDA graphs of up to 64 calls; one pair of CUDA events on the
+launching stream brackets all K.  For comparison the line also gives the
+median of steps run one per graph replay with L2 flushed before each (each
+then also pays the replay's launch).  A separate pass through the library's timed entry
 point (an event before each kernel) gives the per-stage times and the
 dominant kernel's (the indexer's) duration for the roofline.  `--impl reference` times the float64 CPU oracle on
 a bounded sample of the same workload.
@@ -289,42 +292,101 @@ def pctl(xs, q):
     return xs[min(len(xs) - 1, int(q * len(xs)))]
 
 
+NCOPY = 8   # input copies a timed sequence of layers cycles through
+
+
+def clone_workload(W, wl):
+    """The same workload in new device memory: every layer of a model reads
+    its own caches, so a run of layers cycling through NCOPY such copies
+    finds none of a layer's inputs in L2 (8 x ~160 MB touched in between)."""
+    import dataclasses
+    return dataclasses.replace(
+        wl, seqlens=wl.seqlens.clone(), page_table=wl.page_table.clone(), q_fp8=wl.q_fp8.clone(),
+        q_scale=wl.q_scale.clone(), w=wl.w.clone(),
+        layers=[W.LayerCache(lc.k_fp8.clone(), lc.k_scale.clone(), lc.q.clone(), lc.kv.clone())
+                for lc in wl.layers])
+
+
+def time_layer_sequence(torch, fns, steps, sampler=None, barrier=None):
+    """Time `steps` layer calls run back to back as in a decode step: call j
+    is fns[j % len(fns)] (each on its own copy of the inputs), captured into
+    CUDA graphs of up to 64 calls; one event pair brackets all of them.
+    Returns (total ms, how it was timed)."""
+    G = max(1, min(steps, 64))
+    nfull, rem = divmod(steps, G)
+
+    def cap(n):
+        if n == 0:
+            return None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for j in range(n):
+                fns[j % len(fns)]()
+        torch.cuda.synchronize()
+        return g
+
+    try:
+        gfull, grem = cap(G), cap(rem)
+        how = f"CUDA graphs of {G} back-to-back layer calls, replayed"
+    except Exception as exc:  # noqa: BLE001 -- reported in the JSON line
+        torch.cuda.synchronize()
+        gfull = grem = None
+        how = "direct calls (graph capture failed: " + f"{type(exc).__name__}: {exc}"[:160] + ")"
+
+    def run(n_full, with_rem):
+        if gfull is None:
+            for j in range(n_full * G + (rem if with_rem else 0)):
+                fns[j % len(fns)]()
+            return
+        for _ in range(n_full):
+            gfull.replay()
+        if with_rem and grem is not None:
+            grem.replay()
+
+    # untimed load first: the clocks are sampled under load, the caches and
+    # TLBs see the same cycle of copies as the timed run
+    if sampler is not None:
+        sampler.start()
+    t_end = time.time() + 0.3
+    while time.time() < t_end:
+        run(1, False)
+        torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20_000_000)   # keep the host ahead: every replay is queued before e0 fires
+    e0.record()
+    run(nfull, True)
+    e1.record()
+    torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
+    return e0.elapsed_time(e1), how
+
+
 def measure_configs(torch, api, W, dev, steps):
     """The other workloads of the benchmark table, each timed like the
-    headline (graph-replayed layer call, L2 flushed between steps, median and
-    p10/p90 of per-step events): tiny_4k cold and warm, mtp_32k, long_varlen,
-    short_dense as the DSA layer and as the dense path (the same attention
-    over every visible token, given as the selection), and mli_195k's two
-    layers serial vs with the second layer's indexer + top-k on a second
-    stream while its attention reuses the first layer's selection."""
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    headline (a run of back-to-back layer calls cycling through NCOPY copies
+    of the inputs, from CUDA graphs, one event pair around the run):
+    tiny_4k cold and warm (warm: one copy, so its inputs stay in L2),
+    mtp_32k, long_varlen, short_dense as the DSA layer and as the dense path
+    (the same attention over every visible token, given as the selection),
+    and mli_195k's two layers serial vs with the second layer's indexer +
+    top-k on a second stream while its attention reuses the first layer's
+    selection."""
     res = {}
 
-    def timed(fn, n, do_flush=True):
-        g = torch.cuda.CUDAGraph()
-        fn()
+    def timed(make_fn, wls, n):
+        fns = [make_fn(c) for c in wls]
+        for f in fns:
+            f()
         torch.cuda.synchronize()
-        with torch.cuda.graph(g):
-            fn()
-        torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n)]
-        for a, b in ev:
-            a.record()
-            b.record()
-        torch.cuda.synchronize()
-        torch.cuda._sleep(20_000_000)
-        for i in range(n):
-            if do_flush:
-                flush.zero_()
-            ev[i][0].record()
-            g.replay()
-            ev[i][1].record()
-        torch.cuda.synchronize()
+        total_ms, _ = time_layer_sequence(torch, fns, n)
         if api.dsa_get_device_error() != 0:
             raise RuntimeError("device error while timing a configuration")
-        us = [a.elapsed_time(b) * 1e3 for a, b in ev]
-        return {"us_median": statistics.median(us), "us_p10": pctl(us, 0.1), "us_p90": pctl(us, 0.9)}
+        return {"us_per_step": total_ms / n * 1e3}
 
     def layer_fn(wl, layer=0, topk_in=None, topk_out=None, ws=None, out=None):
         spec = wl.spec
@@ -342,22 +404,31 @@ def measure_configs(torch, api, W, dev, steps):
                                  stream=torch.cuda.current_stream())
         return fn
 
-    def record(name, wl, t):
+    def record(name, wl, t, layers=1):
         u = accounting(wl.spec, wl.seqlens.cpu().tolist())
-        t.update(query_tokens_per_s=u["query_tokens"] / (t["us_median"] * 1e-6),
-                 layer_bytes=u["layer_bytes"],
-                 layer_gbs=u["layer_bytes"] / (t["us_median"] * 1e-6) / 1e9,
-                 frac_of_8tbs=u["layer_bytes"] / (t["us_median"] * 1e-6) / 1e9 / TARGET_HBM_GBS)
+        us = t["us_per_step"]
+        t.update(query_tokens_per_s=u["query_tokens"] / (us * 1e-6),
+                 layer_bytes=layers * u["layer_bytes"],
+                 layer_gbs=layers * u["layer_bytes"] / (us * 1e-6) / 1e9,
+                 frac_of_8tbs=layers * u["layer_bytes"] / (us * 1e-6) / 1e9 / TARGET_HBM_GBS)
         res[name] = t
 
-    n = max(20, min(steps, 200))
+    n = max(24, min(steps, 200))
     for name in ("tiny_4k", "mtp_32k", "long_varlen", "short_dense", "mli_195k"):
         wl = W.make_workload(name, device=dev)
+        copies = [wl] + [clone_workload(W, wl) for _ in range(NCOPY - 1)]
+        # one workspace and output for all copies, as a model reuses them
+        ws0 = api.alloc_workspace(wl, api.dsa_num_splits_auto(api.workload_desc(wl)))
+        out0 = torch.empty((wl.spec.num_tokens, wl.spec.num_heads, 512), dtype=torch.float32,
+                           device=dev)
+
+        def plain(c, **kw):
+            return layer_fn(c, ws=ws0, out=out0, **kw)
         if name == "tiny_4k":
-            record(name, wl, timed(layer_fn(wl), n))
-            record(name + "_warm", wl, timed(layer_fn(wl), n, do_flush=False))
+            record(name, wl, timed(plain, copies, n))
+            record(name + "_warm", wl, timed(plain, [wl], n))
         elif name == "short_dense":
-            record(name, wl, timed(layer_fn(wl), n))
+            record(name, wl, timed(plain, copies, n))
             # dense path: every visible position given as the selection
             T, k = wl.spec.num_tokens, wl.spec.topk
             vis = [max(int(s), 0) for s in wl.seqlens.cpu().tolist()]
@@ -365,50 +436,51 @@ def measure_configs(torch, api, W, dev, steps):
             for t, v in enumerate(vis):
                 ident[t, :min(v, k)] = torch.arange(min(v, k), dtype=torch.int32)
             ident = ident.to(dev)
-            r = timed(layer_fn(wl, topk_in=ident), n)
+            r = timed(lambda c: plain(c, topk_in=ident), copies, n)
             record(name + "_dense", wl, r)
-            res[name]["overhead_vs_dense_us"] = res[name]["us_median"] - r["us_median"]
+            res[name]["overhead_vs_dense_us"] = res[name]["us_per_step"] - r["us_per_step"]
         elif name == "mli_195k":
             T, k = wl.spec.num_tokens, wl.spec.topk
             sel1 = torch.empty((T, k), dtype=torch.int32, device=dev)
             sel2 = torch.empty((T, k), dtype=torch.int32, device=dev)
-            f1 = layer_fn(wl, 0, topk_out=sel1)
-            f2 = layer_fn(wl, 1)
-            f2_reuse = layer_fn(wl, 1, topk_in=sel1)
-            desc = api.workload_desc(wl)
+            desc0 = api.workload_desc(wl)
             ld = api.logits_ld(wl)
             logits2 = torch.empty((T, ld), dtype=torch.float32, device=dev)
-            tws = torch.empty(api.dsa_topk_workspace_bytes(desc, ld), dtype=torch.uint8, device=dev)
-            lc2 = wl.layers[1]
+            tws = torch.empty(api.dsa_topk_workspace_bytes(desc0, ld), dtype=torch.uint8, device=dev)
             side = torch.cuda.Stream()
 
-            def serial():
-                f1()
-                f2()
+            def serial(c):
+                f1, f2 = plain(c, layer=0, topk_out=sel1), plain(c, layer=1)
 
-            def overlapped():
-                f1()
-                main = torch.cuda.current_stream()
-                side.wait_stream(main)
-                with torch.cuda.stream(side):
-                    api.dsa_indexer_logits(desc, wl.q_fp8, wl.q_scale, wl.w, lc2.k_fp8, lc2.k_scale,
-                                           logits2, ld, side)
-                    api.dsa_topk(desc, logits2, sel2, tws, ld, side)
-                f2_reuse()
-                main.wait_stream(side)
+                def fn():
+                    f1()
+                    f2()
+                return fn
 
-            a = timed(serial, n)
-            b = timed(overlapped, n)
-            u = accounting(wl.spec, wl.seqlens.cpu().tolist())
-            for key, t in (("mli_195k_serial_2layers", a), ("mli_195k_overlapped_2layers", b)):
-                t.update(query_tokens_per_s=u["query_tokens"] / (t["us_median"] * 1e-6),
-                         layer_bytes=2 * u["layer_bytes"],
-                         layer_gbs=2 * u["layer_bytes"] / (t["us_median"] * 1e-6) / 1e9)
-                res[key] = t
-            res["mli_195k_overlapped_2layers"]["speedup_vs_serial"] = a["us_median"] / b["us_median"]
+            def overlapped(c):
+                f1, f2_reuse = plain(c, layer=0, topk_out=sel1), plain(c, layer=1, topk_in=sel1)
+                desc, lc2 = api.workload_desc(c), c.layers[1]
+
+                def fn():
+                    f1()
+                    main = torch.cuda.current_stream()
+                    side.wait_stream(main)
+                    with torch.cuda.stream(side):
+                        api.dsa_indexer_logits(desc, c.q_fp8, c.q_scale, c.w, lc2.k_fp8, lc2.k_scale,
+                                               logits2, ld, side)
+                        api.dsa_topk(desc, logits2, sel2, tws, ld, side)
+                    f2_reuse()
+                    main.wait_stream(side)
+                return fn
+
+            a = timed(serial, copies, n)
+            b = timed(overlapped, copies, n)
+            record("mli_195k_serial_2layers", wl, a, layers=2)
+            record("mli_195k_overlapped_2layers", wl, b, layers=2)
+            res["mli_195k_overlapped_2layers"]["speedup_vs_serial"] = a["us_per_step"] / b["us_per_step"]
         else:
-            record(name, wl, timed(layer_fn(wl), n))
-        del wl
+            record(name, wl, timed(plain, copies, n))
+        del wl, copies, ws0, out0
         torch.cuda.empty_cache()
     return res
 
@@ -470,21 +542,40 @@ def run_ours(args, world, rank, local):
     if api.dsa_get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
-    # A step is one dsa_decode_fused call (workspace clear + four kernels)
-    # replayed from a CUDA graph, so the device never waits on the host's
-    # launches; one event pair per step brackets it.
-    graph = capture(layer)
+    # A step is one dsa_decode_fused call (workspace clear + four kernels).
+    # The K timed steps run back to back, as the layers of a decode step do,
+    # each on its own copy of the inputs (NCOPY copies in turn, so no step
+    # finds its inputs in L2), from CUDA graphs; one event pair brackets all
+    # K steps.
+    copies = [wl] + [clone_workload(W, wl) for _ in range(NCOPY - 1)]
+
+    def layer_on(c):
+        cdesc = api.workload_desc(c)
+
+        def fn():
+            api.dsa_decode_fused(cdesc, c.q_fp8, c.q_scale, c.w, c.k_fp8, c.k_scale, c.q, c.kv,
+                                 out, ws, max_seqlen, spec.sm_scale, splits,
+                                 stream=torch.cuda.current_stream())
+        return fn
+
     K = args.steps
-    ev = make_events(K, 2)
-    torch.cuda.synchronize()
     sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    dist_barrier(world)
+    total_ms, timed_how = time_layer_sequence(torch, [layer_on(c) for c in copies], K,
+                                              sampler=sampler, barrier=lambda: dist_barrier(world))
+    clocks = sampler.stop()
+    if api.dsa_get_device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+    del copies
+
+    # For comparison: one layer per graph replay with L2 flushed before each
+    # (the flush outside the events), so each step also pays the graph's
+    # launch; median over up to 300 steps.
+    graph = capture(layer)
+    KP = max(1, min(K, 300))
+    ev = make_events(KP, 2)
     torch.cuda.synchronize()
-    # keep the host ahead of the device so no step waits on a launch
     torch.cuda._sleep(20_000_000)
-    for i in range(K):
+    for i in range(KP):
         flush.zero_()
         ev[i][0].record()
         if graph is not None:
@@ -492,14 +583,8 @@ def run_ours(args, world, rank, local):
         else:
             layer()
         ev[i][1].record()
-        if i % 256 == 255:
-            torch.cuda._sleep(2_000_000)
     torch.cuda.synchronize()
-    dist_barrier(world)
-    clocks = sampler.stop()
-    if api.dsa_get_device_error() != 0:
-        raise RuntimeError("device error during the timed steps")
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(KP)]
 
     # Stage breakdown, a separate pass: the layer with an event before each
     # kernel, read back after every step (a device sleep first keeps the host
@@ -518,7 +603,6 @@ def run_ours(args, world, rank, local):
         topk_ms.append(sev[1].elapsed_time(sev[2]))
         mla_ms.append(sev[2].elapsed_time(sev[3]))
         merge_ms.append(sev[3].elapsed_time(sev[4]))
-    total_ms = sum(step_ms)
     total_ms_max = dist_max(total_ms, world)
     ms_per_step = total_ms_max / K
     value = throughput(units["query_tokens"], K, world, total_ms_max)
@@ -588,14 +672,21 @@ def run_ours(args, world, rank, local):
         "config": {"workload": args.workload, "batch": spec.batch, "q_per_req": spec.q_per_req,
                    "seqlen": spec.seqlen, "topk": k, "heads": H, "index_heads": 64,
                    "page_size": 64, "num_splits": splits,
-                   "l2": "flushed between steps (256 MB write, outside the timed events)",
-                   "timed_region": "one dsa_decode_fused call (workspace clear + indexer + "
-                                   "top-k + sparse MLA + merge) per step, "
-                                   + ("replayed from a CUDA graph" if graph is not None
-                                      else "called directly (graph capture failed: "
-                                      + "; ".join(capture_errors) + ")"),
+                   "l2": f"not flushed: the steps cycle through {NCOPY} copies of the inputs "
+                         "(each layer its own caches and queries), so a step's inputs were "
+                         f"last touched {NCOPY} layers (>1 GB) earlier",
+                   "timed_region": f"{K} dsa_decode_fused calls (workspace clear + indexer + "
+                                   "top-k + sparse MLA + merge each) back to back, "
+                                   + timed_how + "; one event pair around all of them",
                    "parallelism": f"replicas x{world} (independent batches per GPU)"},
         "us_per_layer": ms_per_step * 1e3,
+        "us_per_layer_single_graph_flushed": {
+            "median": statistics.median(step_ms) * 1e3, "p10": pctl(step_ms, 0.1) * 1e3,
+            "p90": pctl(step_ms, 0.9) * 1e3,
+            "note": f"{KP} steps, each one layer per graph replay with L2 flushed before it "
+                    "(flush outside the events): includes each replay's launch latency"
+                    + ("" if graph is not None else "; graph capture failed: "
+                       + "; ".join(capture_errors))},
         "layer_bytes": units["layer_bytes"],
         "layer_gbs": layer_gbs,
         "layer_frac_of_8tbs": layer_gbs / TARGET_HBM_GBS,
@@ -611,7 +702,7 @@ def run_ours(args, world, rank, local):
                      "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * (3 + (1 if splits > 1 else 0)),
+        "gpu_launches": K * (4 + (1 if splits > 1 else 0)),
         "clocks": clocks,
         "configs": configs,
     }
