@@ -42,6 +42,7 @@ UNIT = "query-tokens/s"
 TARGET_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+NCOPY = 8   # input copies a timed sequence of layers cycles through
 
 
 def parse_args():
@@ -56,6 +57,9 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the per-configuration table (other workloads)")
+    p.add_argument("--copies", type=int, default=NCOPY,
+                   help="input copies the timed layers cycle through (1: every layer on the same "
+                        "inputs, for profiling with a small device footprint)")
     return p.parse_args()
 
 
@@ -205,22 +209,29 @@ def accounting(spec, seqlens):
 # CPU (oracle) leg
 # ---------------------------------------------------------------------------
 
-def oracle_rows_per_second(wl, seconds: float):
-    """Times the float64 oracle on whole requests of the workload (one request
-    at a time, its data already in host memory) until ``seconds`` elapse."""
-    import numpy as np
-    import torch
-    import oracle as O
-    from deepseek_sparse_attention_lightning_gb300 import workloads as W
+class OracleSampler:
+    """Times the float64 oracle on whole requests of the workload, one request
+    at a time with its data already in host memory (each request's inputs are
+    prepared once, outside the timed part), cycling over the requests."""
 
-    spec = wl.spec
-    nq = spec.q_per_req
-    seqlens = wl.seqlens.cpu().numpy()
-    table = wl.page_table.cpu().numpy()
-    done_rows, spent, requests = 0, 0.0, 0
-    for r in range(spec.batch):
-        S = int(seqlens[r])
-        rows = torch.from_numpy(O.physical_rows(table[r], np.arange(S))).to(wl.k_fp8.device)
+    def __init__(self, wl):
+        import numpy as np
+        self.wl, self.np = wl, np
+        self.seqlens = wl.seqlens.cpu().numpy()
+        self.table = wl.page_table.cpu().numpy()
+        self.prepared = {}
+        self.cursor = 0
+
+    def _inputs(self, r):
+        if r in self.prepared:
+            return self.prepared[r]
+        import torch
+        import oracle as O
+        from deepseek_sparse_attention_lightning_gb300 import workloads as W
+        np, wl, spec = self.np, self.wl, self.wl.spec
+        nq = spec.q_per_req
+        S = int(self.seqlens[r])
+        rows = torch.from_numpy(O.physical_rows(self.table[r], np.arange(S))).to(wl.k_fp8.device)
         t0, t1 = r * nq, (r + 1) * nq
         inputs = dict(
             seqlens=np.array([S]), page_table=np.arange((S + 63) // 64)[None, :], q_per_req=nq,
@@ -233,14 +244,24 @@ def oracle_rows_per_second(wl, seconds: float):
             inputs["k_fp8"] = np.concatenate([inputs["k_fp8"], np.zeros((pad, 128), np.uint8)])
             inputs["k_scale"] = np.concatenate([inputs["k_scale"], np.ones(pad, np.float32)])
             inputs["kv"] = np.concatenate([inputs["kv"], np.zeros((pad, 576), np.uint16)])
-        start = time.perf_counter()
-        O.decode_layer(inputs)
-        spent += time.perf_counter() - start
-        done_rows += nq
-        requests += 1
-        if spent >= seconds:
-            break
-    return done_rows / spent, done_rows, spent, requests
+        self.prepared[r] = inputs
+        return inputs
+
+    def sample(self, seconds: float):
+        """Whole requests (at least one) until ``seconds`` of oracle time:
+        (query rows, seconds spent, requests)."""
+        import oracle as O
+        spec = self.wl.spec
+        rows, spent, requests = 0, 0.0, 0
+        while requests == 0 or spent < seconds:
+            inputs = self._inputs(self.cursor % spec.batch)
+            self.cursor += 1
+            start = time.perf_counter()
+            O.decode_layer(inputs)
+            spent += time.perf_counter() - start
+            rows += spec.q_per_req
+            requests += 1
+        return rows, spent, requests
 
 
 def cpu_cores():
@@ -260,9 +281,12 @@ def run_reference(args, world, rank):
     units = accounting(wl.spec, wl.seqlens.cpu().tolist())
     per_step = []
     rows = 0
-    budget = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    # each step a bounded sample (at least one whole request), the whole run
+    # about --cpu-seconds of oracle time beyond one request per step
+    sampler = OracleSampler(wl)
+    budget = args.cpu_seconds / max(1, args.steps + args.warmup)
     for i in range(args.warmup + args.steps):
-        rps, n, spent, nreq = oracle_rows_per_second(wl, budget)
+        n, spent, nreq = sampler.sample(budget)
         if i >= args.warmup:
             per_step.append(spent / n)
             rows += n
@@ -290,9 +314,6 @@ def run_reference(args, world, rank):
 def pctl(xs, q):
     xs = sorted(xs)
     return xs[min(len(xs) - 1, int(q * len(xs)))]
-
-
-NCOPY = 8   # input copies a timed sequence of layers cycles through
 
 
 def clone_workload(W, wl):
@@ -547,7 +568,7 @@ def run_ours(args, world, rank, local):
     # each on its own copy of the inputs (NCOPY copies in turn, so no step
     # finds its inputs in L2), from CUDA graphs; one event pair brackets all
     # K steps.
-    copies = [wl] + [clone_workload(W, wl) for _ in range(NCOPY - 1)]
+    copies = [wl] + [clone_workload(W, wl) for _ in range(max(1, args.copies) - 1)]
 
     def layer_on(c):
         cdesc = api.workload_desc(c)
@@ -650,10 +671,12 @@ def run_ours(args, world, rank, local):
     # ---- CPU oracle baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rps, n, spent, nreq = oracle_rows_per_second(wl, args.cpu_seconds)
+        n, spent, nreq = OracleSampler(wl).sample(args.cpu_seconds)
+        rps = n / spent
         cpu = {"value": rps, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{n} query rows ({nreq} whole requests of {args.workload}, one at a time, "
-                         f"{spent:.1f} s), float64 numpy oracle (BLAS threads = cores)"}
+                         f"cycling over its {spec.batch} requests, {spent:.1f} s of oracle time), "
+                         "float64 numpy oracle (BLAS threads = cores)"}
 
     configs = None
     if rank == 0 and not args.no_configs:
@@ -672,9 +695,9 @@ def run_ours(args, world, rank, local):
         "config": {"workload": args.workload, "batch": spec.batch, "q_per_req": spec.q_per_req,
                    "seqlen": spec.seqlen, "topk": k, "heads": H, "index_heads": 64,
                    "page_size": 64, "num_splits": splits,
-                   "l2": f"not flushed: the steps cycle through {NCOPY} copies of the inputs "
-                         "(each layer its own caches and queries), so a step's inputs were "
-                         f"last touched {NCOPY} layers (>1 GB) earlier",
+                   "l2": (f"not flushed: the steps cycle through {args.copies} copies of the "
+                          "inputs (each layer its own caches and queries), so a step's inputs "
+                          f"were last touched {args.copies} layers earlier"),
                    "timed_region": f"{K} dsa_decode_fused calls (workspace clear + indexer + "
                                    "top-k + sparse MLA + merge each) back to back, "
                                    + timed_how + "; one event pair around all of them",

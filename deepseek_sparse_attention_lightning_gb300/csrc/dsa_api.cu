@@ -324,12 +324,12 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
     // Histogram and control words start at zero: a small kernel clears them
     // and the indexer runs as its dependent (prologue and key stream overlap
     // the clear; only its first histogram flush waits for it).
-    if (!mark(0)) return DSA_ERR_CUDA;
     const long long n16 = static_cast<long long>((lay.cand - lay.hist) / 16);
     const int cgrid = static_cast<int>(std::min<long long>((n16 + 255) / 256, 148));
     cudaError_t e = dsa::launch_kernel(ws_clear_kernel, dim3(cgrid), dim3(256), 0, s, false, 1,
                                        reinterpret_cast<uint4*>(base + lay.hist), n16);
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    // Stage 0 (timed entry only) starts after the clear: it times the indexer.
+    if (e != cudaSuccess || !mark(0)) return DSA_ERR_CUDA;
     dsa::IndexerLaunch ia{};
     ia.q_fp8 = q_fp8; ia.q_scale = q_scale; ia.w = w; ia.k_fp8 = k_fp8; ia.k_scale = k_scale;
     ia.seqlens = d->seqlens; ia.page_table = d->page_table;

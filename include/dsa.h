@@ -232,9 +232,10 @@ dsa_status dsa_decode_fused(const dsa_decode_desc* desc,
 /*
  * dsa_decode_fused with per-stage timing: stage_events[0..4] (cudaEvent_t
  * handles passed as void*, any of them NULL) are recorded on `stream` before
- * stage 1, after stage 1 (indexer), after stage 2 (top-k), after stage 3
- * (sparse MLA) and after stage 4 (merge).  With stage_events == NULL this is
- * dsa_decode_fused.  When topk_in is given, events 1 and 2 mark the same point.
+ * stage 1 (after the workspace clear that precedes the indexer), after stage 1
+ * (indexer), after stage 2 (top-k), after stage 3 (sparse MLA) and after
+ * stage 4 (merge).  With stage_events == NULL this is dsa_decode_fused.  When
+ * topk_in is given, events 0, 1 and 2 mark the same point.
  */
 dsa_status dsa_decode_fused_timed(const dsa_decode_desc* desc,
                                   const uint8_t* q_fp8, const float* q_scale, const float* w,
