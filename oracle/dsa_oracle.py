@@ -27,6 +27,15 @@ What it computes, and where the pages define it:
   online-softmax merge ("Deepseek Details", section "DSA", stages 2 and 3).
 * ``decode_bytes`` / ``decode_flops`` -- the per-layer cost model printed in
   "Sparse attention: NSA and DSA" (its code cell and output table).
+* ``encode_e4m3`` / ``quantize_index_key`` / ``cache_write`` -- the step before
+  the indexer: each new token's latent row is written into the paged MLA
+  cache at its position ("[SGLang] NSA", section "forward_decode":
+  set_mla_kv_buffer before the attention), and its indexer key is stored as
+  FP8 with one fp32 scale per token ("Sparse attention: NSA and DSA": the
+  indexer key, FP8 + scale; "[SGLang] NSA", module list: quant_k_cache, the
+  NSA-specific FP8 quantisation of the K cache).  The pages do not give the
+  scale rule; the reading here is scale = amax / 448 over the token's 128
+  values (448 being E4M3's largest finite magnitude), in fp32.
 
 Pinned by ``tests/test_oracle_pins.py``: every function above is checked
 against something other than itself (the pages' printed numbers and worked
@@ -47,7 +56,8 @@ V_DIM = 512
 
 __all__ = [
     "PAGE_SIZE", "INDEX_HEADS", "INDEX_DIM", "LATENT_DIM", "V_DIM",
-    "e4m3_table", "decode_e4m3", "decode_bf16", "visible_lengths",
+    "e4m3_table", "decode_e4m3", "decode_bf16", "encode_e4m3", "quantize_index_key",
+    "new_token_positions", "cache_write", "visible_lengths",
     "physical_rows", "indexer_logits", "indexer_logits_at", "topk", "attend",
     "selection_count", "split_bounds", "sparse_mla", "sparse_mla_split",
     "merge", "decode_layer", "pair_flops_mla", "pair_flops_indexer",
@@ -95,6 +105,34 @@ def decode_bf16(u16: np.ndarray) -> np.ndarray:
     return bits.view(np.float32).astype(np.float64)
 
 
+def encode_e4m3(x: np.ndarray) -> np.ndarray:
+    """Real values -> E4M3 bytes: the nearest finite E4M3 value, ties to the
+    code with an even mantissa, magnitudes beyond 448 saturated to 448, the
+    sign kept (also for zero).  NaN inputs are not defined here."""
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.abs(x)
+    codes = np.arange(0x7F, dtype=np.int64)            # 0x00..0x7E: the finite magnitudes, ascending
+    vals = _E4M3[codes]
+    hi = np.clip(np.searchsorted(vals, mag, side="left"), 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    d_lo, d_hi = np.abs(mag - vals[lo]), np.abs(vals[hi] - mag)
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (codes[hi] % 2 == 0))
+    out = np.where(pick_hi, codes[hi], codes[lo])
+    out = np.where(mag >= 448.0, 0x7E, out)             # saturate
+    return (out | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_index_key(k_bits: np.ndarray):
+    """One token's indexer key, [..., 128] bf16 bit patterns -> (E4M3 codes,
+    fp32 scale per token).  In fp32: amax = max |k|; scale = amax / 448;
+    codes = E4M3(k / scale).  A token of zeros gets scale 1 and zero codes."""
+    k = (np.asarray(k_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    amax = np.max(np.abs(k), axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    x = (k / scale[..., None]).astype(np.float32)
+    return encode_e4m3(x), scale
+
+
 # ---------------------------------------------------------------------------
 # Batch geometry
 # ---------------------------------------------------------------------------
@@ -115,6 +153,33 @@ def physical_rows(page_table_row, positions, page_size: int = PAGE_SIZE) -> np.n
     pos = np.asarray(positions, dtype=np.int64)
     pages = np.asarray(page_table_row, dtype=np.int64)[pos // page_size]
     return pages * page_size + pos % page_size
+
+
+def new_token_positions(seqlens, q_per_req: int) -> np.ndarray:
+    """Logical position of every new token, rows request-major: request r's
+    S_r cached tokens include its q_per_req new ones, which are the last."""
+    s = np.asarray(seqlens, dtype=np.int64)
+    i = np.arange(q_per_req, dtype=np.int64)
+    return (s[:, None] - q_per_req + i[None, :]).reshape(-1)
+
+
+def cache_write(new_latent, new_index_k, kv, k_fp8, k_scale, page_table, seqlens,
+                q_per_req: int):
+    """The cache-write step: copies of the caches with every new token's
+    latent row written at its position and its indexer key quantised there.
+
+    new_latent [T, 576] and new_index_k [T, 128] are bf16 bit patterns; kv
+    [rows, 576] uint16, k_fp8 [rows, 128] uint8, k_scale [rows] float32."""
+    kv, k_fp8, k_scale = np.array(kv), np.array(k_fp8), np.array(k_scale)
+    pos = new_token_positions(seqlens, q_per_req)
+    codes, scales = quantize_index_key(new_index_k)
+    for t, p in enumerate(pos):
+        r = t // q_per_req
+        row = int(physical_rows(page_table[r], [p])[0])
+        kv[row] = np.asarray(new_latent[t], dtype=np.uint16)
+        k_fp8[row] = codes[t]
+        k_scale[row] = scales[t]
+    return kv, k_fp8, k_scale
 
 
 # ---------------------------------------------------------------------------

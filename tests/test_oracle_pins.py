@@ -46,6 +46,44 @@ def test_bf16_decode_matches_torch():
     assert np.array_equal(O.decode_bf16(bits), x.to(torch.float64).numpy())
 
 
+def test_e4m3_encode_matches_torch_in_range():
+    # random magnitudes over the whole finite range, every code's value, and
+    # every midpoint between neighbouring codes (ties go to the even mantissa)
+    rng = np.random.default_rng(3)
+    vals = O.decode_e4m3(np.arange(0x7F, dtype=np.uint8))          # 0 .. 448
+    mids = (vals[:-1] + vals[1:]) / 2
+    rand = np.exp(rng.uniform(np.log(2.0 ** -12), np.log(440.0), 20000))
+    x = np.concatenate([vals, mids, rand, rand * 0.999, 2.0 ** -10 * rng.random(1000)])
+    x = np.concatenate([x, -x]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.encode_e4m3(x), ref)
+
+
+def test_e4m3_encode_saturates_and_keeps_sign():
+    x = np.array([448.0, 449.0, 464.0, 480.0, 1e30, -1e30, -0.0, 0.0])
+    assert O.encode_e4m3(x).tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x80, 0x00]
+
+
+def test_index_key_quantisation_bound_and_amax():
+    rng = np.random.default_rng(4)
+    k = torch.from_numpy(rng.standard_normal((64, 128)) * rng.uniform(0.01, 30, (64, 1)))
+    kb = k.to(torch.bfloat16)
+    bits = kb.view(torch.int16).numpy().view(np.uint16)
+    codes, scale = O.quantize_index_key(bits)
+    kf = kb.to(torch.float64).numpy()
+    assert np.allclose(scale, np.abs(kf).max(axis=1) / 448.0, rtol=1e-7, atol=0)
+    x = kf / scale[:, None]
+    err = np.abs(O.decode_e4m3(codes) - x)
+    # round to nearest: half a step of 3 mantissa bits, or of the subnormal grid
+    assert np.all(err <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10) * (1 + 1e-6))
+    # the largest magnitude of each token lands on +-448
+    am = np.abs(kf).argmax(axis=1)
+    assert set(codes[np.arange(64), am].tolist()) <= {0x7E, 0xFE}
+    # a token of zeros: zero codes, scale 1
+    c0, s0 = O.quantize_index_key(np.zeros((1, 128), np.uint16))
+    assert not c0.any() and s0[0] == 1.0
+
+
 # ---------------------------------------------------------------- geometry
 
 def test_visible_lengths_worked_example(golden_dir):
@@ -61,6 +99,42 @@ def test_physical_rows_follow_page_table():
     table = np.array([7, 2, 9])
     pos = np.array([0, 63, 64, 130])
     assert O.physical_rows(table, pos).tolist() == [7 * 64, 7 * 64 + 63, 2 * 64, 9 * 64 + 2]
+
+
+def test_new_token_positions_are_the_last_visible(golden_dir):
+    # the new tokens are the last q_per_req of the request: token i sits at
+    # the position just before what query i sees (worked example: 7, 8, 9)
+    g = {r[0]: r[1:] for r in _read_golden(golden_dir, "mtp_visible_lengths.txt")}
+    nq, s = int(g["q_per_req"][0]), int(g["seqlen"][0])
+    want = [int(v) - 1 for v in g["visible"]]
+    assert O.new_token_positions([s], nq).tolist() == want
+    assert O.new_token_positions([s, 5], nq).tolist() == want + [2, 3, 4]
+
+
+def test_cache_write_touches_only_the_new_rows():
+    rng = np.random.default_rng(6)
+    B, nq, pages = 3, 2, 12
+    table = rng.permutation(pages).reshape(B, 4).astype(np.int32)
+    seqlens = np.array([70, 129, 2])
+    kv = rng.integers(0, 65535, (pages * 64, 576), dtype=np.uint16)
+    kf8 = rng.integers(0, 255, (pages * 64, 128), dtype=np.uint8)
+    ksc = rng.random(pages * 64).astype(np.float32)
+    lat = rng.integers(0, 65535, (B * nq, 576), dtype=np.uint16)
+    key = torch.randn(B * nq, 128, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16)
+    kbits = key.view(torch.int16).numpy().view(np.uint16)
+    kv2, kf2, ks2 = O.cache_write(lat, kbits, kv, kf8, ksc, table, seqlens, nq)
+    rows = []
+    for t, p in enumerate(O.new_token_positions(seqlens, nq)):
+        r = t // nq
+        row = table[r][p // 64] * 64 + p % 64
+        rows.append(row)
+        assert np.array_equal(kv2[row], lat[t])
+        deq = O.decode_e4m3(kf2[row]) * ks2[row]
+        assert np.allclose(deq, key[t].to(torch.float64).numpy(), rtol=0.07, atol=ks2[row] * 2.0 ** -9)
+    other = np.setdiff1d(np.arange(pages * 64), rows)
+    assert np.array_equal(kv2[other], kv[other]) and np.array_equal(kf2[other], kf8[other])
+    assert np.array_equal(ks2[other], ksc[other])
+    assert len(set(rows)) == B * nq
 
 
 # ---------------------------------------------------------------- indexer
