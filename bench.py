@@ -445,6 +445,27 @@ def measure_configs(torch, api, W, dev, steps):
 
         def plain(c, **kw):
             return layer_fn(c, ws=ws0, out=out0, **kw)
+
+        def cache_write(c):
+            # the step before the indexer: the new tokens' latent rows and
+            # FP8 indexer keys written into the caches (same rows every call)
+            T = c.spec.num_tokens
+            gen = torch.Generator(device=dev).manual_seed(1)
+            lat = torch.randn(T, 576, generator=gen, device=dev).to(torch.bfloat16)
+            key = torch.randn(T, 128, generator=gen, device=dev).to(torch.bfloat16)
+            cdesc = api.workload_desc(c)
+
+            def fn():
+                api.dsa_cache_write(cdesc, lat, key, c.kv, c.k_fp8, c.k_scale,
+                                    stream=torch.cuda.current_stream())
+            return fn
+
+        if name != "mli_195k":
+            t = timed(cache_write, copies, n)
+            T = wl.spec.num_tokens
+            t.update(rows=T, bytes=T * (2 * 576 * 2 + 128 * 2 + 128 + 4),
+                     note="latent rows + FP8 index keys of the new tokens; launch-bound")
+            res[name + "_cache_write"] = t
         if name == "tiny_4k":
             record(name, wl, timed(plain, copies, n))
             record(name + "_warm", wl, timed(plain, [wl], n))

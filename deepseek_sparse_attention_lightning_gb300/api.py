@@ -47,6 +47,8 @@ _SIGS = {
                                               c_void_p, c_int32, c_float, c_void_p, c_void_p,
                                               c_void_p]),
     "dsa_merge": (c_int32, [c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dsa_cache_write": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_void_p]),
     "dsa_decode_fused": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_float, c_int32, c_int32, c_void_p, c_void_p, c_size_t,
@@ -167,6 +169,14 @@ def dsa_sparse_mla_decode_split(desc, q, kv, topk_idx, num_splits, sm_scale, mid
         ctypes.byref(desc), _u16(q, "q"), _u16(kv, "kv"), _ptr(topk_idx, torch.int32, "topk_idx"),
         int(num_splits), float(sm_scale), _ptr(mid_o, torch.float32, "mid_o"),
         _ptr(mid_lse, torch.float32, "mid_lse"), _stream(stream)), "dsa_sparse_mla_decode_split")
+
+
+def dsa_cache_write(desc, new_latent, new_index_k, kv, k_fp8, k_scale, stream=None):
+    _check(lib().dsa_cache_write(ctypes.byref(desc), _ptr(new_latent, torch.bfloat16, "new_latent"),
+                                 _ptr(new_index_k, torch.bfloat16, "new_index_k"),
+                                 _ptr(kv, torch.bfloat16, "kv"), _ptr(k_fp8, torch.uint8, "k_fp8"),
+                                 _ptr(k_scale, torch.float32, "k_scale"), _stream(stream)),
+           "dsa_cache_write")
 
 
 def dsa_merge(num_rows, num_splits, mid_o, mid_lse, out, out_lse=None, stream=None):

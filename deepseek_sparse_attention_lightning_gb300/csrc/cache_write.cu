@@ -1,0 +1,77 @@
+// cache_write.cu -- the step before the indexer: every new token's latent row
+// is written into the paged MLA cache at its position, and its indexer key is
+// stored as FP8 E4M3 with one fp32 scale per token ("[SGLang] NSA", section
+// "forward_decode": set_mla_kv_buffer before the attention; the module list's
+// quant_k_cache, the NSA-specific FP8 quantisation of the K cache; "Sparse
+// attention: NSA and DSA": the indexer key, FP8 + scale).
+//
+// Token i of request r (row t = r * n_q + i) is the request's
+// (S_r - n_q + i)-th token: the n_q new tokens are the last of the S_r.  The
+// scale is amax / 448 over the token's 128 key values (448: E4M3's largest
+// finite magnitude), the codes E4M3(k / scale) rounded to nearest even and
+// saturated, all in fp32; a token of zeros gets scale 1 and zero codes.
+//
+// One warp per new token: the 1152-byte latent row moves as 72 16-byte words;
+// each lane holds 4 of the key's 128 values, and a warp-wide maximum gives
+// amax.  The work is a few KB: the kernel is launch-bound.
+#include <cuda_fp8.h>
+
+#include "dsa_ptx.cuh"
+#include "dsa_internal.h"
+
+DSA_DEFINE_ERROR_WORD(cache)
+
+namespace dsa {
+namespace {
+
+constexpr int kWarps = 8;   // tokens per CTA
+
+__global__ void __launch_bounds__(kWarps * 32) cache_write_kernel(const CacheWriteLaunch p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + warp;
+  if (t >= p.batch * p.nq) return;
+  const int r = t / p.nq, i = t % p.nq;
+  const int pos = p.seqlens[r] - p.nq + i;
+  if (pos < 0 || pos >= p.max_pages * kPage) {
+    if (lane == 0) raise_error(kErrCheck);
+    return;
+  }
+  const int pg = p.page_table[static_cast<long long>(r) * p.max_pages + (pos >> 6)];
+  if (pg < 0 || pg >= p.num_pages) {
+    if (lane == 0) raise_error(kErrCheck);
+    return;
+  }
+  const long long row = static_cast<long long>(pg) * kPage + (pos & (kPage - 1));
+
+  // The latent row, bit for bit.
+  const uint4* src = reinterpret_cast<const uint4*>(p.new_latent + static_cast<long long>(t) * kLatentDim);
+  uint4* dst = reinterpret_cast<uint4*>(p.kv + row * kLatentDim);
+  for (int c = lane; c < kLatentDim * 2 / 16; c += 32) dst[c] = __ldg(src + c);
+
+  // The indexer key: values 4 lane .. 4 lane + 3.
+  const uint2 kb =
+      __ldg(reinterpret_cast<const uint2*>(p.new_index_k + static_cast<long long>(t) * kIndexDim) + lane);
+  const float k[4] = {bf16lo_to_f32(kb.x), bf16hi_to_f32(kb.x), bf16lo_to_f32(kb.y), bf16hi_to_f32(kb.y)};
+  float amax = fmaxf(fmaxf(fabsf(k[0]), fabsf(k[1])), fmaxf(fabsf(k[2]), fabsf(k[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = amax > 0.f ? amax / 448.f : 1.f;
+  uint32_t codes = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    codes |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(k[e] / scale, __NV_SATFINITE, __NV_E4M3))
+             << (8 * e);
+  reinterpret_cast<uint32_t*>(p.k_fp8 + row * kIndexDim)[lane] = codes;
+  if (lane == 0) p.k_scale[row] = scale;
+}
+
+}  // namespace
+
+cudaError_t launch_cache_write(const CacheWriteLaunch& a, cudaStream_t stream) {
+  const int T = a.batch * a.nq;
+  if (T <= 0) return cudaSuccess;
+  cache_write_kernel<<<dim3((T + kWarps - 1) / kWarps), dim3(kWarps * 32), 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -266,6 +266,22 @@ dsa_status dsa_merge(int32_t num_rows, int32_t num_splits, const float* mid_o, c
                                        static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status dsa_cache_write(const dsa_decode_desc* d, const uint16_t* new_latent,
+                           const uint16_t* new_index_k, uint16_t* kv, uint8_t* k_fp8, float* k_scale,
+                           void* stream) {
+  dsa_status st = check_desc(d);
+  if (st != DSA_OK) return st;
+  if (!new_latent || !new_index_k || !kv || !k_fp8 || !k_scale) return DSA_ERR_INVALID_ARG;
+  if (!aligned(new_latent, 16) || !aligned(kv, 16) || !aligned(new_index_k, 8) ||
+      !aligned(k_fp8, 4) || !aligned(k_scale, 4))
+    return DSA_ERR_INVALID_ARG;
+  dsa::CacheWriteLaunch a{};
+  a.new_latent = new_latent; a.new_index_k = new_index_k; a.kv = kv; a.k_fp8 = k_fp8;
+  a.k_scale = k_scale; a.seqlens = d->seqlens; a.page_table = d->page_table;
+  a.batch = d->batch; a.nq = d->q_per_req; a.max_pages = d->max_pages; a.num_pages = d->num_pages;
+  return cuda_status(dsa::launch_cache_write(a, static_cast<cudaStream_t>(stream)));
+}
+
 size_t dsa_workspace_bytes(const dsa_decode_desc* d, int32_t max_seqlen, int32_t num_splits) {
   if (!d || d->batch < 1 || d->q_per_req < 1 || d->topk < 1 || d->num_heads < 1 ||
       max_seqlen < 1 || num_splits < 0)
@@ -377,8 +393,8 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
 
 dsa_status dsa_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
-  const int codes[4] = {dsa::fetch_error_indexer(), dsa::fetch_error_topk(), dsa::fetch_error_mla(),
-                        dsa::fetch_error_merge()};
+  const int codes[5] = {dsa::fetch_error_indexer(), dsa::fetch_error_topk(), dsa::fetch_error_mla(),
+                        dsa::fetch_error_merge(), dsa::fetch_error_cache()};
   for (int c : codes)
     if (c != 0) return static_cast<dsa_status>(c);
   return DSA_OK;

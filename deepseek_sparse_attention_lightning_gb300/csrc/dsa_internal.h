@@ -53,6 +53,17 @@ struct TopkLaunch {
   int pdl;              // 1: launched as a programmatic dependent of the indexer
 };
 
+struct CacheWriteLaunch {
+  const uint16_t* new_latent;    // [T][576] bf16: the new tokens' latent rows
+  const uint16_t* new_index_k;   // [T][128] bf16: the new tokens' indexer keys
+  uint16_t* kv;                  // [num_pages * 64][576] bf16 latent cache
+  uint8_t* k_fp8;                // [num_pages * 64][128] E4M3 indexer-key cache
+  float* k_scale;                // [num_pages * 64] its per-token scales
+  const int32_t* seqlens;
+  const int32_t* page_table;
+  int batch, nq, max_pages, num_pages;
+};
+
 struct MlaLaunch {
   const uint16_t* q;
   const uint16_t* kv;
@@ -69,6 +80,7 @@ struct MlaLaunch {
 cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s);
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t s);
+cudaError_t launch_cache_write(const CacheWriteLaunch& a, cudaStream_t s);
 cudaError_t launch_merge(int rows, int splits, const float* mid_o, const float* mid_lse,
                          float* out, float* out_lse, cudaStream_t s, bool pdl = false);
 
@@ -109,6 +121,7 @@ int fetch_error_indexer();
 int fetch_error_topk();
 int fetch_error_mla();
 int fetch_error_merge();
+int fetch_error_cache();
 
 // Host helpers (dsa_api.cu).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,

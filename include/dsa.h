@@ -195,6 +195,32 @@ dsa_status dsa_sparse_mla_decode_split(const dsa_decode_desc* desc, const uint16
                                        float* mid_lse, void* stream);
 
 /*
+ * The step before stage 1 -- the cache write: every new token's latent row is
+ * written into the paged MLA cache and its indexer key, quantised to FP8 E4M3
+ * with one fp32 scale per token, into the indexer's key cache ("[SGLang] NSA
+ * (Narrow Sparse Attention)", section "forward_decode": set_mla_kv_buffer
+ * before the attention; its module list: quant_k_cache, the NSA-specific FP8
+ * quantisation of the K cache; "MTP and sparse attention: NSA and DSA":
+ * the indexer key, FP8 + scale).
+ *   new_latent  [dev] bf16 [T, 576] (kv_lora 512 + rope 64), 16-byte aligned
+ *   new_index_k [dev] bf16 [T, 128], 8-byte aligned
+ *   kv          [dev] bf16 [num_pages * 64, 576], 16-byte aligned (written)
+ *   k_fp8       [dev] E4M3 [num_pages * 64, 128], 4-byte aligned (written)
+ *   k_scale     [dev] float [num_pages * 64] (written)
+ * Row t = r * q_per_req + i is request r's token S_r - q_per_req + i (the
+ * new tokens are the last q_per_req of seqlens[r]); its cache row is
+ * page_table[r][pos / 64] * 64 + pos % 64.  Key: scale = amax / 448 over its
+ * 128 values, codes = E4M3(k / scale) rounded to nearest even and saturated
+ * at 448, in fp32 (a key of zeros: scale 1, zero codes).  Only those rows
+ * are written.  A position outside the page table or a page id outside
+ * [0, num_pages) skips the row and sets DSA_ERR_DEVICE_CHECK (read by
+ * dsa_get_device_error).  Host-detected errors return before any launch.
+ */
+dsa_status dsa_cache_write(const dsa_decode_desc* desc, const uint16_t* new_latent,
+                           const uint16_t* new_index_k, uint16_t* kv, uint8_t* k_fp8,
+                           float* k_scale, void* stream);
+
+/*
  * Stage 4 -- cross-split merge ("Deepseek Details", section "DSA", stage 3:
  * an online-softmax merge of the blocks' Mid_O and Mid_O_LogExpSum).
  * For each of the num_rows = T*H rows, with L = max_b mid_lse[b]:

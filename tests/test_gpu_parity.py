@@ -316,6 +316,83 @@ def test_device_check_flags_bad_page_id():
     assert np.isfinite(row[:3 * 64]).all()
 
 
+# ---------------------------------------------------------------- cache write
+
+def _new_tokens(T, seed):
+    """New tokens' latent rows and indexer keys (bf16): mixed magnitudes, one
+    key of zeros, one with values far above 448 before scaling."""
+    g = torch.Generator().manual_seed(seed)
+    lat = torch.randn(T, 576, generator=g).to(torch.bfloat16)
+    key = torch.randn(T, 128, generator=g) * torch.exp(torch.randn(T, 1, generator=g) * 2)
+    key[0] = 0.0
+    if T > 1:
+        key[1] *= 1e4
+    return lat, key.to(torch.bfloat16)
+
+
+def _check_cache_write(wl, g, seed, whole_oracle):
+    """Runs dsa_cache_write on the device copy g of wl and compares every
+    byte of the written rows and a sample of the others with the oracle
+    (its cache_write on the whole caches, or its per-row pieces when the
+    caches are workload-sized)."""
+    T, nq = wl.spec.num_tokens, wl.spec.q_per_req
+    lat, key = _new_tokens(T, seed)
+    lat_b, key_b = W.bf16_bits(lat), W.bf16_bits(key)
+    table, seqlens = wl.page_table.numpy(), wl.seqlens.numpy()
+    rows = [int(O.physical_rows(table[t // nq], [p])[0])
+            for t, p in enumerate(O.new_token_positions(seqlens, nq))]
+    rng = np.random.default_rng(seed)
+    sample = np.unique(np.concatenate([rows, rng.integers(0, wl.kv.shape[0], 4096)]))
+    if whole_oracle:
+        want_kv, want_k8, want_ks = O.cache_write(lat_b, key_b, W.bf16_bits(wl.kv), wl.k_fp8.numpy(),
+                                                  wl.k_scale.numpy(), table, seqlens, nq)
+        want_kv, want_k8, want_ks = want_kv[sample], want_k8[sample], want_ks[sample]
+    else:
+        idx = torch.from_numpy(sample)
+        want_kv = W.bf16_bits(wl.kv[idx]).copy()
+        want_k8 = wl.k_fp8[idx].numpy().copy()
+        want_ks = wl.k_scale[idx].numpy().copy()
+        codes, scales = O.quantize_index_key(key_b)
+        where = {int(r): n for n, r in enumerate(sample)}
+        for t, r in enumerate(rows):
+            want_kv[where[r]], want_k8[where[r]], want_ks[where[r]] = lat_b[t], codes[t], scales[t]
+    api.dsa_cache_write(api.workload_desc(g), lat.cuda(), key.cuda(), g.kv, g.k_fp8, g.k_scale)
+    _assert_no_device_error()
+    didx = torch.from_numpy(sample).cuda()
+    assert np.array_equal(W.bf16_bits(g.kv[didx]), want_kv)
+    assert np.array_equal(g.k_fp8[didx].cpu().numpy(), want_k8)
+    assert np.array_equal(g.k_scale[didx].cpu().numpy().view(np.uint32), want_ks.view(np.uint32))
+    return rows
+
+
+def test_cache_write_bit_exact_small():
+    wl, g = _gpu_wl("mtp_32k", batch=5, q_per_req=3, num_heads=128, topk=64,
+                    seqlens=[70, 129, 3, 640, 200], heavy="none", seed=81)
+    rows = _check_cache_write(wl, g, 81, whole_oracle=True)
+    assert len(set(rows)) == 15
+
+
+@pytest.mark.parametrize("name", ["long_128k", "mtp_32k"])
+def test_cache_write_bit_exact_workload_sized(name):
+    wl = W.make_workload(name)
+    g = wl.to("cuda")
+    _check_cache_write(wl, g, 82, whole_oracle=False)
+
+
+def test_cache_write_flags_bad_page_id():
+    wl, g = _gpu_wl("long_varlen", batch=2, q_per_req=1, num_heads=128, topk=2048,
+                    seqlens=[3000, 700], heavy="none", seed=83)
+    g.page_table[1, (700 - 1) // 64] = -1                 # the new token's page
+    lat, key = _new_tokens(2, 83)
+    before = g.kv.clone()
+    api.dsa_cache_write(api.workload_desc(g), lat.cuda(), key.cuda(), g.kv, g.k_fp8, g.k_scale)
+    assert api.dsa_get_device_error() == 5               # DSA_ERR_DEVICE_CHECK
+    row0 = int(O.physical_rows(wl.page_table.numpy()[0], [2999])[0])
+    assert torch.equal(g.kv[row0], lat[0].cuda())         # the valid row is still written
+    changed = (g.kv != before).any(dim=1).nonzero().flatten().tolist()
+    assert changed == [row0]
+
+
 def test_host_errors_are_returned_before_launch():
     wl, g = _gpu_wl("long_varlen", batch=1, q_per_req=1, num_heads=128, topk=2048,
                     seqlens=[300], heavy="none", seed=72)
