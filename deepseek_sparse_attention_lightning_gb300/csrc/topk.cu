@@ -154,13 +154,14 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // One cluster of gridDim.x (<= kTopkClusterCtas) CTAs per query row, as many
-// as the longest row needs chunks; CTA x owns chunk x of
-// C = 512 * 16 * M positions, 16 M consecutive ones per thread.
-template <int M>
+// as the longest row needs chunks; CTA x owns chunk x of C = 512 * 4 * Q
+// positions, 4 Q per thread (Q float4 loads).
+template <int Q>
 __global__ void __launch_bounds__(kThreads)
     topk_select_kernel(const TopkLaunch p) {
-  constexpr int P = 16 * M;            // positions per thread
+  constexpr int P = 4 * Q;             // positions per thread
   constexpr int C = kThreads * P;      // positions per CTA
+  constexpr int HW = (Q + 3) / 4;      // 16-bit candidate masks per thread (4 float4 groups each)
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* sh = reinterpret_cast<uint32_t*>(smem + kOffHist);
   uint32_t* slv = reinterpret_cast<uint32_t*>(smem + kOffLvl);
@@ -201,7 +202,6 @@ __global__ void __launch_bounds__(kThreads)
   // ---- scores: this thread's float4 f = threadIdx.x + kThreads * q holds
   //      positions lo + 4 f .. lo + 4 f + 3, so a warp's loads are 512
   //      consecutive bytes (four whole cache lines per instruction).
-  constexpr int Q = P / 4;
   const float* row = p.logits + static_cast<long long>(t) * p.ld;
   auto pos_of = [&](int q) { return lo + 4 * (static_cast<int>(threadIdx.x) + kThreads * q); };
   float v[P];
@@ -244,9 +244,9 @@ __global__ void __launch_bounds__(kThreads)
   //      b* -> candidates.  Bit 4 (q mod 4) + b of inbin[q / 4] is position
   //      pos_of(q) + b.  Bitmap word 64 q + threadIdx.x / 8 holds the nibbles
   //      of eight consecutive threads (four positions each).
-  uint32_t inbin[M];
+  uint32_t inbin[HW];
 #pragma unroll
-  for (int h = 0; h < M; ++h) inbin[h] = 0u;
+  for (int h = 0; h < HW; ++h) inbin[h] = 0u;
 #pragma unroll
   for (int q = 0; q < Q; ++q) {
     const int pq = pos_of(q);
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kThreads)
   }
   int mine = 0;
 #pragma unroll
-  for (int h = 0; h < M; ++h) mine += __popc(inbin[h]);
+  for (int h = 0; h < HW; ++h) mine += __popc(inbin[h]);
   int incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -283,10 +283,10 @@ __global__ void __launch_bounds__(kThreads)
     // shared memory after the barrier), else to the chunk's global slice.
     int i = wbase + incl - mine;
 #pragma unroll
-    for (int h = 0; h < M; ++h)
+    for (int h = 0; h < HW; ++h)
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if ((inbin[h] >> j) & 1u) {
+        if (4 * h + (j >> 2) < Q && ((inbin[h] >> j) & 1u)) {
           const int q = 4 * h + (j >> 2), b = j & 3;
           const uint2 c = make_uint2(float_key(v[4 * q + b]), static_cast<uint32_t>(pos_of(q) + b));
           if (i < kCandSlot) scand[i] = c;
@@ -517,31 +517,124 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace
 
+namespace {
+
+constexpr int kQs[4] = {4, 6, 8, 16};       // float4 groups per thread the launcher chooses from
+constexpr int kOneSmemBytes = 120 * 1024;   // more than half an SM's shared memory: one CTA per SM
+
+template <int Q>
+void* select_kernel_ptr() {
+  return reinterpret_cast<void*>(topk_select_kernel<Q>);
+}
+
+void* select_kernel_for(int q) {
+  switch (q) {
+    case 4: return select_kernel_ptr<4>();
+    case 6: return select_kernel_ptr<6>();
+    case 8: return select_kernel_ptr<8>();
+    default: return select_kernel_ptr<16>();
+  }
+}
+
+// Clusters of cs CTAs that fit on the device at once, one or (as many as the
+// registers allow, two) CTAs per SM; cached per device.  0 if unknown.
+int max_active_clusters(int qi, int cs, bool one) {
+  static std::mutex mu;
+  static int cache[64][4][2][kTopkClusterCtas + 1];
+  static bool filled[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!filled[dev]) {
+    for (auto& a : cache[dev])
+      for (auto& b : a)
+        for (int& c : b) c = -1;
+    filled[dev] = true;
+  }
+  int& slot = cache[dev][qi][one ? 1 : 0][cs];
+  if (slot < 0) {
+    void* kern = select_kernel_for(kQs[qi]);
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = one ? kOneSmemBytes : kSmemBytes;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = static_cast<unsigned>(cs);
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kOneSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess)
+      n = 0;
+    slot = n;
+  }
+  return slot;
+}
+
+}  // namespace
+
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   const int T = a.batch * a.nq;
-  const int64_t per_mul = int64_t(kTopkClusterCtas) * kTopkChunk;   // ld covered with M = 1
-  const int mul = a.ld <= per_mul ? 1 : (a.ld <= 2 * per_mul ? 2 : (a.ld <= 4 * per_mul ? 4 : 0));
-  if (mul == 0) return cudaErrorInvalidValue;
+  if (a.ld > int64_t(kTopkClusterCtas) * kThreads * 4 * kQs[3]) return cudaErrorInvalidValue;
   if (!a.hist_ready) {
     const int chunks = static_cast<int>((a.ld + kTopkChunk - 1) / kTopkChunk);
     topk_hist_kernel<<<dim3(chunks > 0 ? chunks : 1, T), kThreads, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // The plan: the smallest chunk that covers the row, CTAs packed as the
+  // registers allow (two per SM at Q = 4) -- unless one CTA per SM fits every
+  // row's cluster at once and loads fewer score bytes per SM.  One CTA per
+  // SM also leaves CTA 0's resolve the SM to itself, but fewer clusters of 16
+  // fit at once (7 of 16 on 152 SMs, 8 of 12); with more than one wave the
+  // packed plan measured faster.
+  int best_q = -1, best_cs = 0;
+  bool best_one = false;
+  double base_bytes = 0.0;
+  for (int qi = 0; qi < 4 && best_q < 0; ++qi) {
+    const int64_t chunk = int64_t(kThreads) * 4 * kQs[qi];
+    const int cs = static_cast<int>(std::max<int64_t>(1, (a.ld + chunk - 1) / chunk));
+    if (cs > kTopkClusterCtas) continue;
+    best_q = qi;
+    best_cs = cs;
+    cudaFuncAttributes fa{};
+    const int regs = cudaFuncGetAttributes(&fa, select_kernel_for(kQs[qi])) == cudaSuccess
+                         ? std::max(1, fa.numRegs) : 128;
+    const int per_sm = std::max(1, std::min(2, 65536 / (regs * kThreads)));
+    base_bytes = static_cast<double>(chunk) * 4.0 * per_sm;
+  }
+  if (best_q < 0) return cudaErrorInvalidValue;
+  for (int qi = 0; qi < 4; ++qi) {
+    const int64_t chunk = int64_t(kThreads) * 4 * kQs[qi];
+    const int cs = static_cast<int>(std::max<int64_t>(1, (a.ld + chunk - 1) / chunk));
+    if (cs > kTopkClusterCtas || static_cast<double>(chunk) * 4.0 >= base_bytes) continue;
+    if (max_active_clusters(qi, cs, true) >= T) {
+      best_q = qi;
+      best_cs = cs;
+      best_one = true;
+      break;
+    }
+  }
+  const int smem = best_one ? kOneSmemBytes : kSmemBytes;
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kOneSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    // As many CTAs per row as the longest row (ld) has chunks.
-    const int64_t chunk = int64_t(kTopkChunk) * mul;
-    const int cs = static_cast<int>(std::min<int64_t>(kTopkClusterCtas, (a.ld + chunk - 1) / chunk));
-    return launch_kernel(kern, dim3(cs > 0 ? cs : 1, T), dim3(kThreads), kSmemBytes, stream,
-                         a.pdl != 0 && a.hist_ready, cs > 0 ? cs : 1, a);
+    return launch_kernel(kern, dim3(best_cs, T), dim3(kThreads), smem, stream,
+                         a.pdl != 0 && a.hist_ready, best_cs, a);
   };
-  if (mul == 1) return go(topk_select_kernel<1>);
-  if (mul == 2) return go(topk_select_kernel<2>);
-  return go(topk_select_kernel<4>);
+  switch (kQs[best_q]) {
+    case 4: return go(topk_select_kernel<4>);
+    case 6: return go(topk_select_kernel<6>);
+    case 8: return go(topk_select_kernel<8>);
+    default: return go(topk_select_kernel<16>);
+  }
 }
 
 // ---------------------------------------------------------------------------
