@@ -396,7 +396,8 @@ def measure_configs(torch, api, W, dev, steps):
     (the same attention over every visible token, given as the selection),
     and mli_195k's two layers serial vs with the second layer's indexer +
     top-k on a second stream while its attention reuses the first layer's
-    selection."""
+    selection; the new tokens' cache write alone (*_cache_write) and fused
+    in front of the layer (*_with_cache_write)."""
     res = {}
 
     def timed(make_fn, wls, n):
@@ -404,10 +405,13 @@ def measure_configs(torch, api, W, dev, steps):
         for f in fns:
             f()
         torch.cuda.synchronize()
-        total_ms, _ = time_layer_sequence(torch, fns, n)
+        total_ms, how = time_layer_sequence(torch, fns, n)
         if api.dsa_get_device_error() != 0:
             raise RuntimeError("device error while timing a configuration")
-        return {"us_per_step": total_ms / n * 1e3}
+        t = {"us_per_step": total_ms / n * 1e3}
+        if not how.startswith("CUDA graphs"):
+            t["timing"] = how   # a fallback to direct calls times the host's launches too
+        return t
 
     def layer_fn(wl, layer=0, topk_in=None, topk_out=None, ws=None, out=None):
         spec = wl.spec
@@ -460,12 +464,31 @@ def measure_configs(torch, api, W, dev, steps):
                                     stream=torch.cuda.current_stream())
             return fn
 
+        def fused_write(c):
+            # the cache write and the layer in one call (dsa_decode_fused_write)
+            T, spec = c.spec.num_tokens, c.spec
+            gen = torch.Generator(device=dev).manual_seed(1)
+            lat = torch.randn(T, 576, generator=gen, device=dev).to(torch.bfloat16)
+            key = torch.randn(T, 128, generator=gen, device=dev).to(torch.bfloat16)
+            cdesc = api.workload_desc(c)
+            splits = api.dsa_num_splits_auto(cdesc)
+            lc, msl = c.layers[0], c.max_seqlen
+
+            def fn():
+                api.dsa_decode_fused_write(cdesc, lat, key, c.q_fp8, c.q_scale, c.w, lc.k_fp8,
+                                           lc.k_scale, lc.q, lc.kv, out0, ws0, msl,
+                                           spec.sm_scale, splits,
+                                           stream=torch.cuda.current_stream())
+            return fn
+
         if name != "mli_195k":
             t = timed(cache_write, copies, n)
             T = wl.spec.num_tokens
             t.update(rows=T, bytes=T * (2 * 576 * 2 + 128 * 2 + 128 + 4),
                      note="latent rows + FP8 index keys of the new tokens; launch-bound")
             res[name + "_cache_write"] = t
+            if name != "tiny_4k":
+                record(name + "_with_cache_write", wl, timed(fused_write, copies, n))
         if name == "tiny_4k":
             record(name, wl, timed(plain, copies, n))
             record(name + "_warm", wl, timed(plain, [wl], n))

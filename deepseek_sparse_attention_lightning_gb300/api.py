@@ -57,6 +57,10 @@ _SIGS = {
                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_float, c_int32, c_int32, c_void_p, c_void_p,
                                          c_size_t, c_void_p, ctypes.POINTER(c_void_p)]),
+    "dsa_decode_fused_write": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_float, c_int32, c_int32,
+                                         c_void_p, c_void_p, c_size_t, c_void_p]),
     "dsa_workspace_bytes": (c_size_t, [ctypes.POINTER(DecodeDesc), c_int32, c_int32]),
     "dsa_num_splits_auto": (c_int32, [ctypes.POINTER(DecodeDesc)]),
     "dsa_status_str": (ctypes.c_char_p, [c_int32]),
@@ -215,6 +219,20 @@ def dsa_decode_fused(desc, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, out, ws, ma
         _ptr(topk_in, torch.int32, "topk_in"), _ptr(topk_out, torch.int32, "topk_out"),
         float(sm_scale), int(num_splits), int(max_seqlen), _ptr(out, torch.float32, "out"),
         _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "dsa_decode_fused")
+
+
+def dsa_decode_fused_write(desc, new_latent, new_index_k, q_fp8, q_scale, w, k_fp8, k_scale, q,
+                           kv, out, ws, max_seqlen, sm_scale, num_splits=0, topk_in=None,
+                           topk_out=None, stream=None):
+    _check(lib().dsa_decode_fused_write(
+        ctypes.byref(desc), _ptr(new_latent, torch.bfloat16, "new_latent"),
+        _ptr(new_index_k, torch.bfloat16, "new_index_k"), _ptr(q_fp8, torch.uint8, "q_fp8"),
+        _ptr(q_scale, torch.float32, "q_scale"), _ptr(w, torch.float32, "w"),
+        _ptr(k_fp8, torch.uint8, "k_fp8"), _ptr(k_scale, torch.float32, "k_scale"), _u16(q, "q"),
+        _u16(kv, "kv"), _ptr(topk_in, torch.int32, "topk_in"),
+        _ptr(topk_out, torch.int32, "topk_out"), float(sm_scale), int(num_splits),
+        int(max_seqlen), _ptr(out, torch.float32, "out"), _ptr(ws, torch.uint8, "ws"),
+        ws.numel(), _stream(stream)), "dsa_decode_fused_write")
 
 
 def dsa_get_device_error(stream=None) -> int:

@@ -13,8 +13,11 @@
 //
 // One warp per new token: the 1152-byte latent row moves as 72 16-byte words;
 // each lane holds 4 of the key's 128 values, and a warp-wide maximum gives
-// amax.  The work is a few KB: the kernel is launch-bound.
+// amax.  The work is a few KB: the kernel is launch-bound, so on the fused
+// layer it also zero-fills the workspace counters, in CTAs of its own.
 #include <cuda_fp8.h>
+
+#include <algorithm>
 
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
@@ -26,10 +29,8 @@ namespace {
 
 constexpr int kWarps = 8;   // tokens per CTA
 
-__global__ void __launch_bounds__(kWarps * 32) cache_write_kernel(const CacheWriteLaunch p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarps + warp;
-  if (t >= p.batch * p.nq) return;
+// Writes new token t (one warp).
+__device__ __forceinline__ void write_token(const CacheWriteLaunch& p, int t, int lane) {
   const int r = t / p.nq, i = t % p.nq;
   const int pos = p.seqlens[r] - p.nq + i;
   if (pos < 0 || pos >= p.max_pages * kPage) {
@@ -65,13 +66,35 @@ __global__ void __launch_bounds__(kWarps * 32) cache_write_kernel(const CacheWri
   if (lane == 0) p.k_scale[row] = scale;
 }
 
+// CTAs [0, ceil(T / kWarps)) write the new tokens; the CTAs after them, if
+// any, zero-fill p.clear (the layer's workspace counters).  The kernel lets
+// its dependent (the indexer) start at once: that kernel waits for it before
+// it reads the new tokens' keys or its first histogram flush.
+__global__ void __launch_bounds__(kWarps * 32) cache_write_kernel(const CacheWriteLaunch p) {
+  grid_dep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = p.batch * p.nq;
+  const int nw = (T + kWarps - 1) / kWarps;
+  if (static_cast<int>(blockIdx.x) < nw) {
+    const int t = blockIdx.x * kWarps + warp;
+    if (t < T) write_token(p, t, lane);
+    return;
+  }
+  const long long step = static_cast<long long>(gridDim.x - nw) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x - nw) * blockDim.x + threadIdx.x; i < p.clear_n16;
+       i += step)
+    p.clear[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
 
 cudaError_t launch_cache_write(const CacheWriteLaunch& a, cudaStream_t stream) {
   const int T = a.batch * a.nq;
-  if (T <= 0) return cudaSuccess;
-  cache_write_kernel<<<dim3((T + kWarps - 1) / kWarps), dim3(kWarps * 32), 0, stream>>>(a);
-  return cudaGetLastError();
+  const int nw = (T + kWarps - 1) / kWarps;
+  const long long nc = a.clear_n16 > 0 ? std::min<long long>((a.clear_n16 + 255) / 256, 148) : 0;
+  if (nw + nc == 0) return cudaSuccess;
+  return launch_kernel(cache_write_kernel, dim3(static_cast<unsigned>(nw + nc)), dim3(kWarps * 32), 0,
+                       stream, false, 1, a);
 }
 
 }  // namespace dsa

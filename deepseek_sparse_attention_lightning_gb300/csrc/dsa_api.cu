@@ -300,12 +300,17 @@ dsa_status dsa_decode_fused(const dsa_decode_desc* d, const uint8_t* q_fp8, cons
                                 nullptr);
 }
 
-dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8,
-                                  const float* q_scale, const float* w, const uint8_t* k_fp8,
-                                  const float* k_scale, const uint16_t* q, const uint16_t* kv,
-                                  const int32_t* topk_in, int32_t* topk_out, float sm_scale,
-                                  int32_t num_splits, int32_t max_seqlen, float* out, void* ws,
-                                  size_t ws_bytes, void* stream, void* const* stage_events) {
+namespace {
+
+// The layer; with `cw` the new tokens' cache write runs first, in the kernel
+// that also clears the workspace (the indexer waits for it only before each
+// request's last two tiles).
+dsa_status fused_layer(const dsa_decode_desc* d, const dsa::CacheWriteLaunch* cw,
+                       const uint8_t* q_fp8, const float* q_scale, const float* w,
+                       const uint8_t* k_fp8, const float* k_scale, const uint16_t* q,
+                       const uint16_t* kv, const int32_t* topk_in, int32_t* topk_out,
+                       float sm_scale, int32_t num_splits, int32_t max_seqlen, float* out,
+                       void* ws, size_t ws_bytes, void* stream, void* const* stage_events) {
   dsa_status st = check_desc(d);
   if (st != DSA_OK) return st;
   if (!q || !kv || !out || !aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16))
@@ -341,9 +346,17 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
     // and the indexer runs as its dependent (prologue and key stream overlap
     // the clear; only its first histogram flush waits for it).
     const long long n16 = static_cast<long long>((lay.cand - lay.hist) / 16);
-    const int cgrid = static_cast<int>(std::min<long long>((n16 + 255) / 256, 148));
-    cudaError_t e = dsa::launch_kernel(ws_clear_kernel, dim3(cgrid), dim3(256), 0, s, false, 1,
-                                       reinterpret_cast<uint4*>(base + lay.hist), n16);
+    cudaError_t e;
+    if (cw) {
+      dsa::CacheWriteLaunch c = *cw;
+      c.clear = reinterpret_cast<uint4*>(base + lay.hist);
+      c.clear_n16 = n16;
+      e = dsa::launch_cache_write(c, s);
+    } else {
+      const int cgrid = static_cast<int>(std::min<long long>((n16 + 255) / 256, 148));
+      e = dsa::launch_kernel(ws_clear_kernel, dim3(cgrid), dim3(256), 0, s, false, 1,
+                             reinterpret_cast<uint4*>(base + lay.hist), n16);
+    }
     // Stage 0 (timed entry only) starts after the clear: it times the indexer.
     if (e != cudaSuccess || !mark(0)) return DSA_ERR_CUDA;
     dsa::IndexerLaunch ia{};
@@ -353,6 +366,7 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
     ia.hist = reinterpret_cast<uint32_t*>(base + lay.hist);
     ia.batch = d->batch; ia.nq = d->q_per_req; ia.max_pages = d->max_pages;
     ia.num_pages = d->num_pages; ia.topk = d->topk; ia.skip_short = 1; ia.pdl = 1;
+    ia.wait_tail = cw ? 1 : 0;
     e = dsa::launch_indexer(ia, s);
     if (e != cudaSuccess || !mark(1)) return DSA_ERR_CUDA;
     dsa::TopkLaunch ta{};
@@ -364,8 +378,10 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
     e = dsa::launch_topk(ta, s);
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     idx = sel;
-  } else if (!mark(0) || !mark(1)) {
-    return DSA_ERR_CUDA;
+  } else {
+    // The attention below is a plain launch: it starts after the write.
+    if (cw && dsa::launch_cache_write(*cw, s) != cudaSuccess) return DSA_ERR_CUDA;
+    if (!mark(0) || !mark(1)) return DSA_ERR_CUDA;
   }
   if (!mark(2)) return DSA_ERR_CUDA;
   dsa::MlaLaunch ma{};
@@ -389,6 +405,39 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
   }
   if (!mark(4)) return DSA_ERR_CUDA;
   return DSA_OK;
+}
+
+}  // namespace
+
+dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8,
+                                  const float* q_scale, const float* w, const uint8_t* k_fp8,
+                                  const float* k_scale, const uint16_t* q, const uint16_t* kv,
+                                  const int32_t* topk_in, int32_t* topk_out, float sm_scale,
+                                  int32_t num_splits, int32_t max_seqlen, float* out, void* ws,
+                                  size_t ws_bytes, void* stream, void* const* stage_events) {
+  return fused_layer(d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, topk_in, topk_out,
+                     sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream, stage_events);
+}
+
+dsa_status dsa_decode_fused_write(const dsa_decode_desc* d, const uint16_t* new_latent,
+                                  const uint16_t* new_index_k, const uint8_t* q_fp8,
+                                  const float* q_scale, const float* w, uint8_t* k_fp8,
+                                  float* k_scale, const uint16_t* q, uint16_t* kv,
+                                  const int32_t* topk_in, int32_t* topk_out, float sm_scale,
+                                  int32_t num_splits, int32_t max_seqlen, float* out, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  dsa_status st = check_desc(d);
+  if (st != DSA_OK) return st;
+  if (!new_latent || !new_index_k || !kv || !k_fp8 || !k_scale) return DSA_ERR_INVALID_ARG;
+  if (!aligned(new_latent, 16) || !aligned(new_index_k, 8) || !aligned(k_fp8, 4) ||
+      !aligned(k_scale, 4))
+    return DSA_ERR_INVALID_ARG;
+  dsa::CacheWriteLaunch c{};
+  c.new_latent = new_latent; c.new_index_k = new_index_k; c.kv = kv; c.k_fp8 = k_fp8;
+  c.k_scale = k_scale; c.seqlens = d->seqlens; c.page_table = d->page_table;
+  c.batch = d->batch; c.nq = d->q_per_req; c.max_pages = d->max_pages; c.num_pages = d->num_pages;
+  return fused_layer(d, &c, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, topk_in, topk_out, sm_scale,
+                     num_splits, max_seqlen, out, ws, ws_bytes, stream, nullptr);
 }
 
 dsa_status dsa_get_device_error(void* stream) {

@@ -38,6 +38,8 @@ struct IndexerLaunch {
   int batch, nq, max_pages, num_pages, topk;
   int skip_short;       // skip requests whose queries all see <= topk tokens
   int pdl;              // 1: launched as a programmatic dependent of the workspace clear
+  int wait_tail;        // 1: that kernel also writes new tokens' keys: each request's last
+                        //    two tiles are read only after it completed
 };
 
 struct TopkLaunch {
@@ -62,6 +64,8 @@ struct CacheWriteLaunch {
   const int32_t* seqlens;
   const int32_t* page_table;
   int batch, nq, max_pages, num_pages;
+  uint4* clear;                  // zero-filled by CTAs of their own, or nullptr
+  long long clear_n16;           // its 16-byte words
 };
 
 struct MlaLaunch {

@@ -289,6 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // cache end (TMA fills zeros); the epilogue masks its tokens.
           const int g = g0 + it;
           while (prefix[rl + 1] <= g) ++rl;
+          // A request's new tokens (its last n_q <= 4) lie in its last two
+          // tiles, which the kernel before may still be writing.
+          if (p.wait_tail && g >= prefix[rl + 1] - 2) grid_dep_wait();
           const int pg = it0 == 0 ? tile_page(p, prefix, rl, g, which) : page_of(rl, g, which);
           if (pg < 0) raise_error(kErrCheck);
           const int y = pg >= 0 ? pg * kPage : p.num_pages * kPage;
@@ -388,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto scale_of = [&](int g) -> float {
       if (g >= g1) return 0.f;
       while (prefix[rs + 1] <= g) ++rs;
+      if (p.wait_tail && g >= prefix[rs + 1] - 2) grid_dep_wait();   // new tokens' scales
       const int pg = page_of(rs, g, row >> 6);
       return pg >= 0 ? __ldg(p.k_scale + static_cast<long long>(pg) * kPage + (row & (kPage - 1)))
                      : 0.f;
@@ -480,6 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  // This grid completes only after the kernel before it (the stages after
+  // the top-k rely on that, even when no tile here waited for it).
+  if (p.pdl && threadIdx.x == 0) grid_dep_wait();
 #undef KV_FULL
 #undef KV_EMPTY
 #undef Q_FULL

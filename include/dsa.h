@@ -272,6 +272,30 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* desc,
                                   float* out, void* ws, size_t ws_bytes, void* stream,
                                   void* const* stage_events);
 
+/*
+ * The cache write of the step's new tokens, then the layer: dsa_cache_write
+ * followed by dsa_decode_fused on the same caches, in one call (the new
+ * tokens' latent rows and FP8 index keys are written before the indexer reads
+ * them: "[SGLang] NSA (Narrow Sparse Attention)", section "forward_decode",
+ * set_mla_kv_buffer before the attention; "MTP and sparse attention: NSA and
+ * DSA", section "Sparse attention: NSA and DSA", the indexer key in FP8 with
+ * a scale).  The write shares a kernel with the workspace clear, and the
+ * indexer waits for it only before the tiles that hold new tokens (a
+ * request's last two 128-token tiles, since q_per_req <= 4).
+ * Arguments: those of dsa_cache_write (new_latent, new_index_k; kv, k_fp8 and
+ * k_scale are written, then read) and of dsa_decode_fused; the same alignment
+ * rules and errors.  topk_in non-NULL: the write, then the attention over the
+ * given selection.
+ */
+dsa_status dsa_decode_fused_write(const dsa_decode_desc* desc, const uint16_t* new_latent,
+                                  const uint16_t* new_index_k,
+                                  const uint8_t* q_fp8, const float* q_scale, const float* w,
+                                  uint8_t* k_fp8, float* k_scale,
+                                  const uint16_t* q, uint16_t* kv,
+                                  const int32_t* topk_in, int32_t* topk_out,
+                                  float sm_scale, int32_t num_splits, int32_t max_seqlen,
+                                  float* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes dsa_decode_fused needs (num_splits 0 = auto). */
 size_t dsa_workspace_bytes(const dsa_decode_desc* desc, int32_t max_seqlen,
                            int32_t num_splits);

@@ -95,6 +95,11 @@ def test_workspace_checks(L):
     assert L.dsa_decode_fused(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, -1.0, 1, 256,
                               FAKE, FAKE, n1, None) == 1
     assert L.dsa_sparse_mla_decode_split(d, FAKE, FAKE, FAKE, 33, 0.07, FAKE, FAKE, None) == 1
+    # the layer with the cache write: a misaligned new latent row, a short workspace
+    assert L.dsa_decode_fused_write(d, FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    None, None, 0.07, 1, 256, FAKE, FAKE, n1, None) == 1
+    assert L.dsa_decode_fused_write(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    None, None, 0.07, 1, 256, FAKE, FAKE, n1 - 1, None) == 3
 
 
 def test_merge_validation(L):

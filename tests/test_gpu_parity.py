@@ -393,6 +393,81 @@ def test_cache_write_flags_bad_page_id():
     assert changed == [row0]
 
 
+FUSED_WRITE_CASES = [
+    # 2049 with n_q = 2: the new tokens (2047, 2048) straddle the last two tiles
+    dict(base="mtp_32k", batch=3, q_per_req=2, num_heads=128, topk=2048, seqlens=[5000, 2049, 9000],
+         heavy="frac:0.01", seed=91),
+    dict(base="long_varlen", batch=2, q_per_req=1, num_heads=128, topk=2048, seqlens=[20000, 12345],
+         heavy="runs:0.005:8", seed=92),
+    # 129 and 2048: requests whose queries select every token (no scan)
+    dict(base="short_dense", batch=3, q_per_req=1, num_heads=128, topk=2048, seqlens=[129, 3000, 2048],
+         heavy="none", seed=93),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_WRITE_CASES, ids=lambda c: c["base"])
+@pytest.mark.parametrize("given_selection", [False, True], ids=["indexer", "topk_in"])
+def test_fused_layer_with_cache_write(case, given_selection):
+    """dsa_decode_fused_write = the oracle's cache write, then the layer on
+    the written caches.  Each new token's index key is ten times its own
+    query's highest-weighted index head and its latent row four times a
+    random one, so a stale key or row changes the selection or the output."""
+    case = dict(case)
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    wl, g = _gpu_wl(base, seqlens=seqlens, **case)
+    T, k, nq = wl.spec.num_tokens, wl.spec.topk, wl.spec.q_per_req
+    lat, _ = _new_tokens(T, case["seed"])
+    lat = (lat.float() * 4).to(torch.bfloat16)
+    qhat = wl.q_fp8.view(torch.float8_e4m3fn).float() * wl.q_scale[:, None, None]
+    best = torch.argmax(wl.w, dim=1)
+    key = (10 * qhat[torch.arange(T), best]).to(torch.bfloat16)
+    a = W.host_arrays(wl)
+    a["kv"], a["k_fp8"], a["k_scale"] = O.cache_write(
+        W.bf16_bits(lat), W.bf16_bits(key), a["kv"], a["k_fp8"], a["k_scale"], a["page_table"],
+        a["seqlens"], nq)
+    vis = O.visible_lengths(a["seqlens"], nq)
+    lc = g.layers[0]
+    out = torch.empty((T, wl.spec.num_heads, 512), dtype=torch.float32, device="cuda")
+    ws = api.alloc_workspace(g)
+    if given_selection:
+        sel_np = O.topk(np.random.default_rng(3).random((T, int(max(vis)))), vis, k)
+        sel = torch.from_numpy(sel_np.astype(np.int32)).cuda()
+        api.dsa_decode_fused_write(api.workload_desc(g), lat.cuda(), key.cuda(), g.q_fp8, g.q_scale,
+                                   g.w, lc.k_fp8, lc.k_scale, lc.q, lc.kv, out, ws, g.max_seqlen,
+                                   wl.spec.sm_scale, topk_in=sel)
+    else:
+        sel = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+        api.dsa_decode_fused_write(api.workload_desc(g), lat.cuda(), key.cuda(), g.q_fp8, g.q_scale,
+                                   g.w, lc.k_fp8, lc.k_scale, lc.q, lc.kv, out, ws, g.max_seqlen,
+                                   wl.spec.sm_scale, topk_out=sel)
+    torch.cuda.synchronize()
+    _assert_no_device_error()
+    # the caches hold exactly the oracle's written rows
+    rows = np.unique(np.concatenate([
+        O.physical_rows(a["page_table"][t // nq], [p])
+        for t, p in enumerate(O.new_token_positions(a["seqlens"], nq))]))
+    ridx = torch.from_numpy(rows).cuda()
+    assert np.array_equal(W.bf16_bits(lc.kv[ridx]), a["kv"][rows])
+    assert np.array_equal(lc.k_fp8[ridx].cpu().numpy(), a["k_fp8"][rows])
+    assert np.array_equal(lc.k_scale[ridx].cpu().numpy().view(np.uint32),
+                          a["k_scale"][rows].view(np.uint32))
+    if not given_selection:
+        sel_np = sel.cpu().numpy()
+        # the selection is the top-k of the written cache's scores
+        I, E = O.indexer_logits(a["q_fp8"], a["q_scale"], a["w"], a["k_fp8"], a["k_scale"],
+                                a["page_table"], a["seqlens"], nq)
+        for t, n in enumerate(vis):
+            chosen = sel_np[t][sel_np[t] >= 0]
+            if n <= k:
+                assert np.array_equal(chosen, np.arange(n))
+                continue
+            kth = np.sort(I[t, :n])[::-1][k - 1]
+            assert (I[t, chosen] >= kth - 2 * IDX_REL * E[t, chosen]).all()
+            assert n - 1 in chosen                      # the query's own new token
+    o, _ = O.sparse_mla(a["q"], a["kv"], sel_np, a["page_table"], a["seqlens"], nq, a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "O")
+
+
 def test_host_errors_are_returned_before_launch():
     wl, g = _gpu_wl("long_varlen", batch=1, q_per_req=1, num_heads=128, topk=2048,
                     seqlens=[300], heavy="none", seed=72)
