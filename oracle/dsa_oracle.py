@@ -36,6 +36,18 @@ What it computes, and where the pages define it:
   NSA-specific FP8 quantisation of the K cache).  The pages do not give the
   scale rule; the reading here is scale = amax / 448 over the token's 128
   values (448 being E4M3's largest finite magnitude), in fp32.
+* ``quantize_latent`` / ``dequantize_latent`` / ``sparse_mla_fp8`` -- the
+  latent cache kept in FP8 for the attention ("[SGLang] NSA", its module
+  list: quant_k_cache / dequant_k_cache, NSA's own FP8 quantisation of the
+  cache, which the attention reads as FP8 to save memory bandwidth).  The
+  pages give the format only as E4M3 with fine-grained scaling in 1 x 128
+  tiles ("Deepseek Details", section "FP8 Training": activations scaled per
+  1 x 128 tile, E4M3 throughout).  Reading: each row's 512 value
+  dims are four 128-dim tiles, each E4M3 with one fp32 scale (amax / 448, the
+  index key's rule); the 64 rope dims stay bf16 (576 is not a multiple of
+  128, and they are no value dims).  A row is 656 bytes: 512 codes, the four
+  scales, the 64 rope values.  The attention over such rows is the attention
+  over their dequantised values code x scale.
 
 Pinned by ``tests/test_oracle_pins.py``: every function above is checked
 against something other than itself (the pages' printed numbers and worked
@@ -53,9 +65,11 @@ INDEX_HEADS = 64
 INDEX_DIM = 128
 LATENT_DIM = 576
 V_DIM = 512
+LATENT_FP8_BYTES = 656   # 512 E4M3 codes + 4 fp32 scales + 64 bf16 rope values
 
 __all__ = [
     "PAGE_SIZE", "INDEX_HEADS", "INDEX_DIM", "LATENT_DIM", "V_DIM",
+    "LATENT_FP8_BYTES", "quantize_latent", "dequantize_latent", "sparse_mla_fp8",
     "e4m3_table", "decode_e4m3", "decode_bf16", "encode_e4m3", "quantize_index_key",
     "new_token_positions", "cache_write", "visible_lengths",
     "physical_rows", "indexer_logits", "indexer_logits_at", "topk", "attend",
@@ -131,6 +145,32 @@ def quantize_index_key(k_bits: np.ndarray):
     scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
     x = (k / scale[..., None]).astype(np.float32)
     return encode_e4m3(x), scale
+
+
+def quantize_latent(kv_bits: np.ndarray) -> np.ndarray:
+    """Latent rows, [n, 576] bf16 bit patterns -> [n, 656] bytes: the 512
+    value dims as four 128-dim tiles of E4M3 codes (each tile quantised like
+    an index key: scale = amax / 448 in fp32), then the four fp32 scales
+    (little-endian), then the 64 rope dims' bf16 bit patterns (little-endian)."""
+    kv = np.asarray(kv_bits, dtype=np.uint16).reshape(-1, LATENT_DIM)
+    n = kv.shape[0]
+    codes, scales = quantize_index_key(kv[:, :V_DIM].reshape(n, 4, 128))
+    out = np.empty((n, LATENT_FP8_BYTES), dtype=np.uint8)
+    out[:, :V_DIM] = codes.reshape(n, V_DIM)
+    out[:, V_DIM:V_DIM + 16] = scales.astype("<f4").reshape(n, 4).view(np.uint8)
+    out[:, V_DIM + 16:] = np.ascontiguousarray(kv[:, V_DIM:]).astype("<u2").view(np.uint8)
+    return out
+
+
+def dequantize_latent(kv8: np.ndarray) -> np.ndarray:
+    """[n, 656] FP8 latent rows -> float64 [n, 576]: code x its tile's scale
+    for the value dims, the rope dims as they are."""
+    kv8 = np.asarray(kv8, dtype=np.uint8).reshape(-1, LATENT_FP8_BYTES)
+    n = kv8.shape[0]
+    scales = np.ascontiguousarray(kv8[:, V_DIM:V_DIM + 16]).view("<f4").astype(np.float64)
+    vals = decode_e4m3(kv8[:, :V_DIM]).reshape(n, 4, 128) * scales[:, :, None]
+    rope = decode_bf16(np.ascontiguousarray(kv8[:, V_DIM + 16:]).view("<u2"))
+    return np.concatenate([vals.reshape(n, V_DIM), rope], axis=1)
 
 
 # ---------------------------------------------------------------------------
@@ -300,14 +340,23 @@ def _selected_rows(idx_row, n_pos, vis_t, page_table_row):
     return physical_rows(page_table_row, ids)
 
 
+def _latent_rows(kv_bits, kv_fp8, rows):
+    """float64 latent rows of the bf16 cache, or of the FP8 cache if given."""
+    if kv_fp8 is not None:
+        return dequantize_latent(kv_fp8[rows])
+    return decode_bf16(kv_bits[rows])
+
+
 def sparse_mla(q_bits, kv_bits, idx, page_table, seqlens, q_per_req: int, sm_scale: float,
-               tokens=None):
+               tokens=None, kv_fp8=None):
     """Attention of each query row over the tokens its index row selects.
 
     q_bits [T, H, 576] and kv_bits [rows, 576] are bf16 bit patterns.  Query
     row t reads positions [0, min(k, vis_t)) of idx[t]; entries there that are
     negative or >= vis_t are skipped.  Returns (O [T, H, 512], lse [T, H]).
     ``tokens`` restricts the computation to a subset of rows (others are NaN).
+    With ``kv_fp8`` ([rows, 656], see quantize_latent) the rows are read from
+    the FP8 cache instead (kv_bits is then unused).
     """
     idx = np.asarray(idx)
     T, k = idx.shape
@@ -320,9 +369,16 @@ def sparse_mla(q_bits, kv_bits, idx, page_table, seqlens, q_per_req: int, sm_sca
         r = t // q_per_req
         rows = _selected_rows(idx[t], int(n_sel[t]), int(vis[t]), page_table[r])
         qh = decode_bf16(q_bits[t])
-        lat = decode_bf16(kv_bits[rows])
+        lat = _latent_rows(kv_bits, kv_fp8, rows)
         O[t], L[t] = _attend(qh, lat, sm_scale)
     return O, L
+
+
+def sparse_mla_fp8(q_bits, kv_fp8, idx, page_table, seqlens, q_per_req: int, sm_scale: float,
+                   tokens=None):
+    """sparse_mla over the FP8 latent cache kv_fp8 [rows, 656]."""
+    return sparse_mla(q_bits, None, idx, page_table, seqlens, q_per_req, sm_scale, tokens,
+                      kv_fp8=kv_fp8)
 
 
 def split_bounds(k: int, num_splits: int, n_pos: int):
@@ -344,9 +400,10 @@ def split_bounds(k: int, num_splits: int, n_pos: int):
 
 
 def sparse_mla_split(q_bits, kv_bits, idx, page_table, seqlens, q_per_req: int,
-                     sm_scale: float, num_splits: int, tokens=None):
+                     sm_scale: float, num_splits: int, tokens=None, kv_fp8=None):
     """Per-split partial attention: Mid_O [T, H, S, 512] (each block's output
-    normalised by its own softmax sum) and Mid_O_LogExpSum [T, H, S]."""
+    normalised by its own softmax sum) and Mid_O_LogExpSum [T, H, S].  With
+    ``kv_fp8`` the rows come from the FP8 cache."""
     idx = np.asarray(idx)
     T, k = idx.shape
     H = q_bits.shape[1]
@@ -360,7 +417,7 @@ def sparse_mla_split(q_bits, kv_bits, idx, page_table, seqlens, q_per_req: int,
         for s, (lo, hi) in enumerate(split_bounds(k, num_splits, int(n_sel[t]))):
             ids = np.asarray(idx[t, lo:hi], dtype=np.int64)
             ids = ids[(ids >= 0) & (ids < vis[t])]
-            lat = decode_bf16(kv_bits[physical_rows(page_table[r], ids)])
+            lat = _latent_rows(kv_bits, kv_fp8, physical_rows(page_table[r], ids))
             mid_o[t, :, s], mid_l[t, :, s] = _attend(qh, lat, sm_scale)
     return mid_o, mid_l
 

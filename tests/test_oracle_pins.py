@@ -418,3 +418,76 @@ def test_layer_bytes_single_query_matches_cost_model():
         assert O.layer_bytes([L], 1, 2048) == O.decode_bytes(L)
         fi, fa = O.layer_flops([L], 1, 2048, 128)
         assert fi + fa == O.decode_flops(L)
+
+
+# ---------------------------------------------------------------- FP8 latent cache
+
+def _bf16_bits(x):
+    return (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_latent_fp8_layout_and_error_bound():
+    # 656-byte rows: codes of dims 0..511, four fp32 scales, the rope bits.
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((9, 576)) * np.exp(rng.standard_normal((9, 1)) * 3)
+    x[0, :128] = 0.0                                    # a tile of zeros
+    bits = _bf16_bits(x)
+    q8 = O.quantize_latent(bits)
+    assert q8.shape == (9, 656) and q8.dtype == np.uint8
+    xv = O.decode_bf16(bits)
+    # rope: the bf16 bit patterns, little-endian, bit for bit
+    assert np.array_equal(q8[:, 528:].copy().view("<u2"), bits[:, 512:])
+    sc = q8[:, 512:528].copy().view("<f4").astype(np.float64)
+    tiles = xv[:, :512].reshape(9, 4, 128)
+    amax = np.abs(tiles).max(axis=2)
+    assert sc[0, 0] == 1.0                              # zeros: scale 1
+    np.testing.assert_allclose(sc[amax > 0], amax[amax > 0] / 448.0, rtol=1e-6)
+    # each tile's largest magnitude is code +-448 (0x7E / 0xFE)
+    for n in range(1, 9):
+        for g in range(4):
+            j = int(np.argmax(np.abs(tiles[n, g])))
+            assert q8[n, 128 * g + j] & 0x7F == 0x7E
+            assert (q8[n, 128 * g + j] >> 7) == (tiles[n, g, j] < 0)
+    # dequantised values: within half an E4M3 step of the input (relative
+    # 2^-4 for normal codes, 2^-10 x scale for subnormal ones)
+    d = O.dequantize_latent(q8)
+    assert np.array_equal(d[:, 512:], xv[:, 512:])
+    err = np.abs(d[:, :512] - xv[:, :512]).reshape(9, 4, 128)
+    bound = np.maximum(np.abs(tiles) * 2.0 ** -4, sc[:, :, None] * 2.0 ** -10) * (1 + 1e-9)
+    assert (err <= bound).all()
+    # a dims shift or transposed tile would break these: dim 200 of row 3
+    assert abs(d[3, 200] - xv[3, 200]) <= max(abs(xv[3, 200]) * 2 ** -4, sc[3, 1] * 2 ** -10)
+
+
+def test_latent_fp8_attention_equals_bf16_when_exact():
+    # Tiles made of E4M3 values times a power of two, each holding +-448 x 2^e:
+    # the scale is 2^e exactly, quantisation is lossless, and the attention
+    # over the FP8 cache equals the attention over the bf16 cache.
+    rng = np.random.default_rng(6)
+    rows = 64 * 3
+    e4 = O.e4m3_table()[:0x7F]
+    codes = rng.integers(0, 0x7F, size=(rows, 4, 128))
+    signs = rng.choice([-1.0, 1.0], size=(rows, 4, 128))
+    vals = e4[codes] * signs
+    vals[:, :, 0] = 448.0 * rng.choice([-1.0, 1.0], size=(rows, 4))
+    expo = rng.integers(-12, -6, size=(rows, 4, 1)).astype(np.float64)
+    lat = np.concatenate([(vals * 2.0 ** expo).reshape(rows, 512),
+                          rng.standard_normal((rows, 64))], axis=1)
+    kv = _bf16_bits(lat)
+    q8 = O.quantize_latent(kv)
+    assert np.array_equal(O.dequantize_latent(q8), O.decode_bf16(kv))
+    T, H = 2, 8
+    q = _bf16_bits(rng.standard_normal((T, H, 576)) * 40)
+    table = np.array([[2, 0, 1], [1, 2, 0]], dtype=np.int64)
+    seqlens = np.array([150, 192])
+    idx = np.full((T, 64), -1, dtype=np.int64)
+    idx[0, :40] = rng.choice(150, 40, replace=False)
+    idx[1, :64] = rng.choice(192, 64, replace=False)
+    o1, l1 = O.sparse_mla(q, kv, idx, table, seqlens, 1, 0.07)
+    o2, l2 = O.sparse_mla_fp8(q, q8, idx, table, seqlens, 1, 0.07)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+    # and the FP8 split partials merge to the same output
+    mo, ml = O.sparse_mla_split(q, None, idx, table, seqlens, 1, 0.07, 3, kv_fp8=q8)
+    om, lm = O.merge(mo, ml)
+    np.testing.assert_allclose(om, o1, rtol=0, atol=1e-10)
