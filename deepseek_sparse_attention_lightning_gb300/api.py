@@ -61,6 +61,14 @@ _SIGS = {
                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_void_p, c_float, c_int32, c_int32,
                                          c_void_p, c_void_p, c_size_t, c_void_p]),
+    "dsa_latent_to_fp8": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
+    "dsa_sparse_mla_decode_split_fp8": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p,
+                                                  c_void_p, c_int32, c_float, c_void_p, c_void_p,
+                                                  c_void_p]),
+    "dsa_decode_fused_fp8kv": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_float, c_int32, c_int32, c_void_p, c_void_p,
+                                         c_size_t, c_void_p]),
     "dsa_workspace_bytes": (c_size_t, [ctypes.POINTER(DecodeDesc), c_int32, c_int32]),
     "dsa_num_splits_auto": (c_int32, [ctypes.POINTER(DecodeDesc)]),
     "dsa_status_str": (ctypes.c_char_p, [c_int32]),
@@ -233,6 +241,34 @@ def dsa_decode_fused_write(desc, new_latent, new_index_k, q_fp8, q_scale, w, k_f
         _ptr(topk_out, torch.int32, "topk_out"), float(sm_scale), int(num_splits),
         int(max_seqlen), _ptr(out, torch.float32, "out"), _ptr(ws, torch.uint8, "ws"),
         ws.numel(), _stream(stream)), "dsa_decode_fused_write")
+
+
+def dsa_latent_to_fp8(kv, kv8, stream=None):
+    rows = int(kv.shape[0])
+    if kv8.shape != (rows, 656):
+        raise ValueError("kv8 must be [rows, 656]")
+    _check(lib().dsa_latent_to_fp8(_u16(kv, "kv"), rows, _ptr(kv8, torch.uint8, "kv8"),
+                                   _stream(stream)), "dsa_latent_to_fp8")
+
+
+def dsa_sparse_mla_decode_split_fp8(desc, q, kv8, topk_idx, num_splits, sm_scale, mid_o, mid_lse,
+                                    stream=None):
+    _check(lib().dsa_sparse_mla_decode_split_fp8(
+        ctypes.byref(desc), _u16(q, "q"), _ptr(kv8, torch.uint8, "kv8"),
+        _ptr(topk_idx, torch.int32, "topk_idx"), int(num_splits), float(sm_scale),
+        _ptr(mid_o, torch.float32, "mid_o"), _ptr(mid_lse, torch.float32, "mid_lse"),
+        _stream(stream)), "dsa_sparse_mla_decode_split_fp8")
+
+
+def dsa_decode_fused_fp8kv(desc, q_fp8, q_scale, w, k_fp8, k_scale, q, kv8, out, ws, max_seqlen,
+                           sm_scale, num_splits=0, topk_in=None, topk_out=None, stream=None):
+    _check(lib().dsa_decode_fused_fp8kv(
+        ctypes.byref(desc), _ptr(q_fp8, torch.uint8, "q_fp8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(w, torch.float32, "w"), _ptr(k_fp8, torch.uint8, "k_fp8"),
+        _ptr(k_scale, torch.float32, "k_scale"), _u16(q, "q"), _ptr(kv8, torch.uint8, "kv8"),
+        _ptr(topk_in, torch.int32, "topk_in"), _ptr(topk_out, torch.int32, "topk_out"),
+        float(sm_scale), int(num_splits), int(max_seqlen), _ptr(out, torch.float32, "out"),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "dsa_decode_fused_fp8kv")
 
 
 def dsa_get_device_error(stream=None) -> int:

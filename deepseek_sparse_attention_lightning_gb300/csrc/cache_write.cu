@@ -27,7 +27,8 @@ DSA_DEFINE_ERROR_WORD(cache)
 namespace dsa {
 namespace {
 
-constexpr int kWarps = 8;   // tokens per CTA
+constexpr int kWarps = 8;   // tokens (rows) per CTA
+constexpr int kF8LatentBytes = 656;
 
 // Writes new token t (one warp).
 __device__ __forceinline__ void write_token(const CacheWriteLaunch& p, int t, int lane) {
@@ -86,7 +87,55 @@ __global__ void __launch_bounds__(kWarps * 32) cache_write_kernel(const CacheWri
     p.clear[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Latent rows in FP8 (656 bytes: the 512 value dims as four 128-dim tiles of
+// E4M3 codes, each with an fp32 scale amax / 448 -- the fine-grained 1 x 128
+// tiles of "Deepseek Details", section "FP8 Training" -- then the four
+// scales, then the 64 rope dims as bf16).  One warp per row: lane l holds
+// dims 16 l .. 16 l + 15 (tile l / 8), eight lanes reduce a tile's amax.
+__global__ void __launch_bounds__(kWarps * 32) latent_fp8_kernel(const uint16_t* __restrict__ kv,
+                                                                 long long rows,
+                                                                 uint8_t* __restrict__ kv8) {
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const uint4* src = reinterpret_cast<const uint4*>(kv + row * kLatentDim);
+  const uint4 v0 = __ldg(src + 2 * lane), v1 = __ldg(src + 2 * lane + 1);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float x[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    x[2 * e] = bf16lo_to_f32(w[e]);
+    x[2 * e + 1] = bf16hi_to_f32(w[e]);
+    amax = fmaxf(amax, fmaxf(fabsf(x[2 * e]), fabsf(x[2 * e + 1])));
+  }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = amax > 0.f ? amax / 448.f : 1.f;
+  uint32_t codes[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    codes[e >> 2] |=
+        static_cast<uint32_t>(__nv_cvt_float_to_fp8(x[e] / scale, __NV_SATFINITE, __NV_E4M3))
+        << (8 * (e & 3));
+  uint8_t* dst = kv8 + row * kF8LatentBytes;
+  reinterpret_cast<uint4*>(dst)[lane] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+  if ((lane & 7) == 0) reinterpret_cast<float*>(dst + 512)[lane >> 3] = scale;
+  if (lane < 8)
+    reinterpret_cast<uint4*>(dst + 528)[lane] = __ldg(src + (512 * 2) / 16 + lane);
+}
+
 }  // namespace
+
+cudaError_t launch_latent_fp8(const uint16_t* kv, long long rows, uint8_t* kv8,
+                              cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const long long grid = (rows + kWarps - 1) / kWarps;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  latent_fp8_kernel<<<dim3(static_cast<unsigned>(grid)), dim3(kWarps * 32), 0, stream>>>(kv, rows,
+                                                                                        kv8);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_cache_write(const CacheWriteLaunch& a, cudaStream_t stream) {
   const int T = a.batch * a.nq;

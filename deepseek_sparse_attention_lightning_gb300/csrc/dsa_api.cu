@@ -233,25 +233,53 @@ dsa_status dsa_topk(const dsa_decode_desc* d, const float* logits, int64_t ld, i
   return cuda_status(dsa::launch_topk(a, s));
 }
 
-dsa_status dsa_sparse_mla_decode_split(const dsa_decode_desc* d, const uint16_t* q,
-                                       const uint16_t* kv, const int32_t* topk_idx,
-                                       int32_t num_splits, float sm_scale, float* mid_o,
-                                       float* mid_lse, void* stream) {
+namespace {
+
+// The attention stage over the bf16 cache kv, or over the FP8 cache kv8.
+dsa_status mla_split(const dsa_decode_desc* d, const uint16_t* q, const uint16_t* kv,
+                     const uint8_t* kv8, const int32_t* topk_idx, int32_t num_splits,
+                     float sm_scale, float* mid_o, float* mid_lse, void* stream) {
   dsa_status st = check_desc(d);
   if (st != DSA_OK) return st;
-  if (!q || !kv || !topk_idx || !mid_o || !mid_lse) return DSA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(mid_o, 16) || !aligned(topk_idx, 4) ||
-      !aligned(mid_lse, 4))
+  if (!q || (!kv && !kv8) || !topk_idx || !mid_o || !mid_lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || (kv && !aligned(kv, 16)) || (kv8 && !aligned(kv8, 16)) ||
+      !aligned(mid_o, 16) || !aligned(topk_idx, 4) || !aligned(mid_lse, 4))
     return DSA_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
   const int splits = resolve_splits(d, num_splits);
   if (splits < 1 || splits > max_splits(d)) return DSA_ERR_INVALID_ARG;
   dsa::MlaLaunch a{};
-  a.q = q; a.kv = kv; a.topk_idx = topk_idx; a.seqlens = d->seqlens; a.page_table = d->page_table;
+  a.q = q; a.kv = kv; a.kv8 = kv8; a.topk_idx = topk_idx; a.seqlens = d->seqlens;
+  a.page_table = d->page_table;
   a.mid_o = mid_o; a.mid_lse = mid_lse; a.batch = d->batch; a.nq = d->q_per_req;
   a.heads = d->num_heads; a.k = d->topk; a.max_pages = d->max_pages; a.num_pages = d->num_pages;
   a.num_splits = splits; a.sm_scale = sm_scale;
   return cuda_status(dsa::launch_sparse_mla(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+dsa_status dsa_sparse_mla_decode_split(const dsa_decode_desc* d, const uint16_t* q,
+                                       const uint16_t* kv, const int32_t* topk_idx,
+                                       int32_t num_splits, float sm_scale, float* mid_o,
+                                       float* mid_lse, void* stream) {
+  if (!kv) return DSA_ERR_INVALID_ARG;
+  return mla_split(d, q, kv, nullptr, topk_idx, num_splits, sm_scale, mid_o, mid_lse, stream);
+}
+
+dsa_status dsa_sparse_mla_decode_split_fp8(const dsa_decode_desc* d, const uint16_t* q,
+                                           const uint8_t* kv8, const int32_t* topk_idx,
+                                           int32_t num_splits, float sm_scale, float* mid_o,
+                                           float* mid_lse, void* stream) {
+  if (!kv8) return DSA_ERR_INVALID_ARG;
+  return mla_split(d, q, nullptr, kv8, topk_idx, num_splits, sm_scale, mid_o, mid_lse, stream);
+}
+
+dsa_status dsa_latent_to_fp8(const uint16_t* kv, int64_t rows, uint8_t* kv8, void* stream) {
+  if (rows < 0) return DSA_ERR_INVALID_ARG;
+  if (rows == 0) return DSA_OK;
+  if (!kv || !kv8 || !aligned(kv, 16) || !aligned(kv8, 16)) return DSA_ERR_INVALID_ARG;
+  return cuda_status(dsa::launch_latent_fp8(kv, rows, kv8, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status dsa_merge(int32_t num_rows, int32_t num_splits, const float* mid_o, const float* mid_lse,
@@ -308,12 +336,14 @@ namespace {
 dsa_status fused_layer(const dsa_decode_desc* d, const dsa::CacheWriteLaunch* cw,
                        const uint8_t* q_fp8, const float* q_scale, const float* w,
                        const uint8_t* k_fp8, const float* k_scale, const uint16_t* q,
-                       const uint16_t* kv, const int32_t* topk_in, int32_t* topk_out,
+                       const uint16_t* kv, const uint8_t* kv8, const int32_t* topk_in,
+                       int32_t* topk_out,
                        float sm_scale, int32_t num_splits, int32_t max_seqlen, float* out,
                        void* ws, size_t ws_bytes, void* stream, void* const* stage_events) {
   dsa_status st = check_desc(d);
   if (st != DSA_OK) return st;
-  if (!q || !kv || !out || !aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16))
+  if (!q || (!kv && !kv8) || !out || !aligned(q, 16) || (kv && !aligned(kv, 16)) ||
+      (kv8 && !aligned(kv8, 16)) || !aligned(out, 16))
     return DSA_ERR_INVALID_ARG;
   if (!topk_in && (!q_fp8 || !q_scale || !w || !k_fp8 || !k_scale || !aligned(q_fp8, 16) ||
                    !aligned(k_fp8, 16) || !aligned(q_scale, 4) || !aligned(w, 4) ||
@@ -385,7 +415,7 @@ dsa_status fused_layer(const dsa_decode_desc* d, const dsa::CacheWriteLaunch* cw
   }
   if (!mark(2)) return DSA_ERR_CUDA;
   dsa::MlaLaunch ma{};
-  ma.q = q; ma.kv = kv; ma.topk_idx = idx; ma.seqlens = d->seqlens; ma.page_table = d->page_table;
+  ma.q = q; ma.kv = kv; ma.kv8 = kv8; ma.topk_idx = idx; ma.seqlens = d->seqlens; ma.page_table = d->page_table;
   ma.mid_o = splits > 1 ? reinterpret_cast<float*>(base + lay.mid_o) : out;
   ma.mid_lse = reinterpret_cast<float*>(base + lay.mid_lse);
   ma.batch = d->batch; ma.nq = d->q_per_req; ma.heads = d->num_heads; ma.k = d->topk;
@@ -415,8 +445,9 @@ dsa_status dsa_decode_fused_timed(const dsa_decode_desc* d, const uint8_t* q_fp8
                                   const int32_t* topk_in, int32_t* topk_out, float sm_scale,
                                   int32_t num_splits, int32_t max_seqlen, float* out, void* ws,
                                   size_t ws_bytes, void* stream, void* const* stage_events) {
-  return fused_layer(d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, topk_in, topk_out,
-                     sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream, stage_events);
+  return fused_layer(d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, nullptr, topk_in,
+                     topk_out, sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream,
+                     stage_events);
 }
 
 dsa_status dsa_decode_fused_write(const dsa_decode_desc* d, const uint16_t* new_latent,
@@ -436,8 +467,19 @@ dsa_status dsa_decode_fused_write(const dsa_decode_desc* d, const uint16_t* new_
   c.new_latent = new_latent; c.new_index_k = new_index_k; c.kv = kv; c.k_fp8 = k_fp8;
   c.k_scale = k_scale; c.seqlens = d->seqlens; c.page_table = d->page_table;
   c.batch = d->batch; c.nq = d->q_per_req; c.max_pages = d->max_pages; c.num_pages = d->num_pages;
-  return fused_layer(d, &c, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, topk_in, topk_out, sm_scale,
-                     num_splits, max_seqlen, out, ws, ws_bytes, stream, nullptr);
+  return fused_layer(d, &c, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, nullptr, topk_in, topk_out,
+                     sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream, nullptr);
+}
+
+dsa_status dsa_decode_fused_fp8kv(const dsa_decode_desc* d, const uint8_t* q_fp8,
+                                  const float* q_scale, const float* w, const uint8_t* k_fp8,
+                                  const float* k_scale, const uint16_t* q, const uint8_t* kv8,
+                                  const int32_t* topk_in, int32_t* topk_out, float sm_scale,
+                                  int32_t num_splits, int32_t max_seqlen, float* out, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  if (!kv8) return DSA_ERR_INVALID_ARG;
+  return fused_layer(d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, nullptr, kv8, topk_in,
+                     topk_out, sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream, nullptr);
 }
 
 dsa_status dsa_get_device_error(void* stream) {

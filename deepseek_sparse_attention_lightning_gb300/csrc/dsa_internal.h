@@ -71,6 +71,7 @@ struct CacheWriteLaunch {
 struct MlaLaunch {
   const uint16_t* q;
   const uint16_t* kv;
+  const uint8_t* kv8;   // non-null: the latent cache in FP8 rows of 656 bytes (kv unused)
   const int32_t* topk_idx;
   const int32_t* seqlens;
   const int32_t* page_table;
@@ -85,6 +86,7 @@ cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s);
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t s);
 cudaError_t launch_cache_write(const CacheWriteLaunch& a, cudaStream_t s);
+cudaError_t launch_latent_fp8(const uint16_t* kv, long long rows, uint8_t* kv8, cudaStream_t s);
 cudaError_t launch_merge(int rows, int splits, const float* mid_o, const float* mid_lse,
                          float* out, float* out_lse, cudaStream_t s, bool pdl = false);
 

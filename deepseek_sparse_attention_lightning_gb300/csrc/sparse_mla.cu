@@ -45,6 +45,9 @@
 // each) but the warps' in parallel.  Warp 1 issues the MMAs and owns TMEM;
 // warps 4-7 and 12-15 run the softmax and the epilogue (Mid_O written by
 // 128B-swizzled tensor stores of 32 heads x 32 dims).
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
 
@@ -66,8 +69,10 @@ constexpr int kMaxPos = 2048;                            // positions of one spl
 constexpr int kOffRows = kOffStage + 2 * kStageBytes;    // cache row of every position
 constexpr int kOffMask = kOffRows + kMaxPos * 4;         // validity bits, 32 per word
 constexpr int kOffXchg = kOffMask + (kMaxPos / 32) * 4;    // softmax groups' exchange, 2 KB
-constexpr int kOffBar = kOffXchg + 2 * 2 * 128 * 4;
-constexpr int kNumBars = 12;
+constexpr int kOffSc = kOffXchg + 2 * 2 * 128 * 4;         // FP8 rows' tile scales, 2 stages
+constexpr int kScStageBytes = (kBN / 4) * 128;             // 4 rows x 16 B per 128-byte slot
+constexpr int kOffBar = kOffSc + 2 * kScStageBytes;
+constexpr int kNumBars = 14;
 constexpr int kQStageAtoms = 4;                            // q dims [0, 256) via stage 1
 constexpr int kOffSlot = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;
@@ -83,16 +88,55 @@ constexpr int kOBoxBytes = 32 * 128;                       // Mid_O box: 32 head
 constexpr int kOChunkBytes = 4 * kOBoxBytes;               // the 4 warps' boxes of a chunk
 static_assert(8 * kOChunkBytes <= 2 * kStageBytes, "Mid_O staging fits in the key stages");
 constexpr float kRescaleLog2 = 8.0f;
+// FP8 latent rows: 512 E4M3 codes (four 128-dim tiles), the 4 tiles' fp32
+// scales, the 64 rope dims in bf16 -- 656 bytes.
+constexpr int kF8RowBytes = 656;
+constexpr int kF8Copies = (kBN / 4) * 6;                   // 4 code tiles + rope + scales per 4 rows
+constexpr int kF8Issuers = kF8Copies / 2;                  // 48 per CTA (warps 0, 2, 3)
+constexpr int kF8TileBytes = kBN * (512 + 128 + 16);       // bytes landing per tile per CTA
+constexpr int kF8Rem = kF8TileBytes - kF8Issuers * (kF8TileBytes / kF8Issuers);
+constexpr int kRawOff = 4 * kAtomBytes;                    // codes land in stage atoms 4..7
+constexpr int kConvThreads = 128;                          // warps 8-11 dequantise
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// Dequantises code tile a's 16-code chunk c of key row j (scale sc) into the
+// bf16 atoms of the stage, in the 128B-swizzled layout the MMAs read: dims
+// 128 a + 16 c .. + 15 are atom 2a + c / 4, 16-byte chunks 2 (c % 4) and
+// 2 (c % 4) + 1 of row j.
+__device__ __forceinline__ void dequant_chunk(uint8_t* stage, int a, int j, int c, uint4 raw,
+                                              float sc) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2_raw h01 =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[q] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw h23 =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[q] >> 16), __NV_E4M3);
+    const float2 f01 = __half22float2(__half2(h01));
+    const float2 f23 = __half22float2(__half2(h23));
+    o[2 * q] = pack_bf16x2(f01.x * sc, f01.y * sc);
+    o[2 * q + 1] = pack_bf16x2(f23.x * sc, f23.y * sc);
+  }
+  uint8_t* atom = stage + (2 * a + (c >> 2)) * kAtomBytes + j * 128;
+  const int cb = 2 * (c & 3);
+  *reinterpret_cast<uint4*>(atom + ((cb ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(atom + (((cb + 1) ^ (j & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// kFp8: the latent cache holds FP8 rows (kF8RowBytes); tmap_kv then maps its
+// bytes with 128-byte boxes (code tiles, rope) and tmap_sc with 16-byte boxes
+// (the scales).  Otherwise tmap_kv maps the bf16 cache and tmap_sc is unused.
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_kv,
-                      const __grid_constant__ CUtensorMap tmap_o, const MlaLaunch p) {
+                      const __grid_constant__ CUtensorMap tmap_o,
+                      const __grid_constant__ CUtensorMap tmap_sc, const MlaLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   const int split = blockIdx.x >> 1, half = blockIdx.x & 1, t = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint16_t kBoth = 0x3;
 #define KV_FULL(s) (bar0 + 48u + 8u * (s))
 #define KV_EMPTY(s) (bar0 + 64u + 8u * (s))
+#define KV_CONV(s) (bar0 + 96u + 8u * (s))
 
   if (threadIdx.x == 0) {
     mbar_init(Q_FULL, 1);
@@ -147,8 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(Q_STAGE, 1);
     mbar_init(Q_PEER, 1);                         // the peer's softmax read its q staging
     for (int s = 0; s < 2; ++s) {
-      mbar_init(KV_FULL(s), kIssuers);            // one expect-tx arrive per issuing thread
+      mbar_init(KV_FULL(s), kFp8 ? kF8Issuers : kIssuers);   // one expect-tx arrive per issuer
       mbar_init(KV_EMPTY(s), 2);                  // both CTAs' MMAs done with the stage
+      mbar_init(KV_CONV(s), kConvThreads);        // FP8: the stage dequantised
     }
     fence_mbar_init();
   }
@@ -180,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmap_q);
       prefetch_tmap(&tmap_kv);
       prefetch_tmap(&tmap_o);
+      if (kFp8) prefetch_tmap(&tmap_sc);
       mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
       mbar_expect_tx(Q_STAGE, kQStageAtoms * kQAtomBytes);
       const uint64_t pol_q = policy_evict_last();
@@ -230,6 +277,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(1, kLoaderWarps * 32);   // rows_s / mask_s complete
     const uint64_t pol_kv = policy_evict_last();   // the sibling half reads the same rows
     int issued = 0;
+    if constexpr (kFp8) {
+      if (lw < 3) {
+        // Warps 0, 2, 3 gather: per tile 96 copies of 4 rows each (per row
+        // group: the four code tiles into stage atoms 4..7, the rope dims
+        // into atom 8, the scales into the scale area); this CTA issues
+        // c = crank mod 2, one per thread, announcing its share of the
+        // 41984 bytes that land in each CTA.
+        const int g8 = lane * 3 + lw;
+        for (int it = 0; it < ntiles && g8 < kF8Issuers; ++it) {
+          const int st = it & 1;
+          if (it >= 2 && !mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1)) {
+            raise_error(kErrTimeout);
+            break;
+          }
+          if (it == 1 && !(mbar_wait(Q_TMEM, 0) && mbar_wait(Q_PEER, 0))) {
+            raise_error(kErrTimeout);
+            break;
+          }
+          const uint32_t dst = sbase + kOffStage + st * kStageBytes;
+          const int* rows = rows_s + it * kBN;
+          mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(kF8TileBytes / kF8Issuers +
+                                                             (g8 < kF8Rem ? 1 : 0)));
+          const int c = 2 * g8 + static_cast<int>(crank);
+          if (c < 64) {
+            const int g = c >> 2, a = c & 3;
+            const int* r4 = rows + 4 * g;
+            tma_gather4_mc(dst + kRawOff + a * kAtomBytes + g * 512, &tmap_kv, 128 * a, r4[0], r4[1],
+                           r4[2], r4[3], KV_FULL(st), kBoth, pol_kv);
+          } else if (c < 80) {
+            const int* r4 = rows + 4 * (c - 64);
+            tma_gather4_mc(dst + 8 * kAtomBytes + (c - 64) * 512, &tmap_kv, 528, r4[0], r4[1], r4[2],
+                           r4[3], KV_FULL(st), kBoth, pol_kv);
+          } else {
+            const int* r4 = rows + 4 * (c - 80);
+            // (a tensor copy's shared-memory destination is 128-byte aligned)
+            tma_gather4_mc(sbase + kOffSc + st * kScStageBytes + (c - 80) * 128, &tmap_sc, 512, r4[0],
+                           r4[1], r4[2], r4[3], KV_FULL(st), kBoth, pol_kv);
+          }
+          issued = it + 1;
+        }
+      } else {
+        // Warps 8-11 dequantise each landed stage in place: code tiles 0, 1
+        // (stage bytes 32-48 KB) become bf16 atoms 0-3 (0-32 KB); tiles 2, 3
+        // are read into registers first, because their bf16 atoms 4-7 cover
+        // the codes themselves.
+        const int ctid = (lw - 3) * 32 + lane;
+        for (int it = 0; it < ntiles; ++it) {
+          const int st = it & 1;
+          if (!mbar_wait(KV_FULL(st), (it >> 1) & 1)) {
+            raise_error(kErrTimeout);
+            break;
+          }
+          uint8_t* stg = smem + kOffStage + st * kStageBytes;
+          const float* scs = reinterpret_cast<const float*>(smem + kOffSc + st * kScStageBytes);
+          uint4 keep[8];
+          float ksc[8];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int item = ctid + kConvThreads * u;
+            const int a = u >> 2, j = (item >> 3) & (kBN - 1), c = item & 7;
+            const uint4 raw = *reinterpret_cast<const uint4*>(stg + kRawOff + a * kAtomBytes + j * 128 +
+                                                              ((c ^ (j & 7)) << 4));
+            const float sc = scs[(j >> 2) * 32 + (j & 3) * 4 + a];
+            if (u < 8) {
+              dequant_chunk(stg, a, j, c, raw, sc);
+            } else {
+              keep[u - 8] = raw;
+              ksc[u - 8] = sc;
+            }
+          }
+          named_bar_sync(4, kConvThreads);
+#pragma unroll
+          for (int u = 8; u < 16; ++u) {
+            const int item = ctid + kConvThreads * u;
+            dequant_chunk(stg, u >> 2, (item >> 3) & (kBN - 1), item & 7, keep[u - 8], ksc[u - 8]);
+          }
+          fence_proxy_async_smem();   // generic-proxy writes -> the MMAs' reads
+          mbar_arrive(KV_CONV(st));
+        }
+      }
+    } else {
     for (int it = 0; it < ntiles && gi < kIssuers; ++it) {
       const int st = it & 1;
       if (it >= 2 && !mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1)) {
@@ -255,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_gather4_mc(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r4[0], r4[1], r4[2], r4[3],
                      KV_FULL(st), kBoth, pol_kv);
       issued = it + 1;
+    }
     }
     // No copy may still be in flight when the CTA exits: the last phase of
     // each stage completes only once every byte (both CTAs' copies) landed.
@@ -301,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_pv();
             continue;
           }
-          if (mbar_test_wait(KV_FULL(st), (it >> 1) & 1) &&
+          if (mbar_test_wait(kFp8 ? KV_CONV(st) : KV_FULL(st), (it >> 1) & 1) &&
               (it == 0 || mbar_test_wait(S_FREE, (it - 1) & 1)))
             break;
           if (clock64() - t0 > kWaitCycles) {
@@ -510,21 +639,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 #undef KV_FULL
 #undef KV_EMPTY
+#undef KV_CONV
 }
 
 }  // namespace
 
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
-  CUtensorMap tq, tkv;
+  const bool fp8 = a.kv8 != nullptr;
+  CUtensorMap tq, tkv, tsc;
   const uint64_t qrows = static_cast<uint64_t>(a.batch) * a.nq * a.heads;
+  const uint64_t cache_rows = static_cast<uint64_t>(a.num_pages) * kPage;
   if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kLatentDim, qrows,
                       kLatentDim * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // One latent row per box row; gather4 takes four row coordinates per copy.
-  if (!encode_tmap_2d(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kLatentDim,
-                      static_cast<uint64_t>(a.num_pages) * kPage, kLatentDim * 2, 64, 1,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  if (fp8) {
+    // The FP8 rows as bytes: 128-byte boxes (a code tile or the rope dims,
+    // 128B-swizzled like the bf16 atoms) and 16-byte boxes (the scales).
+    if (!encode_tmap_2d(&tkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv8, kF8RowBytes, cache_rows,
+                        kF8RowBytes, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tsc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv8, kF8RowBytes, cache_rows,
+                        kF8RowBytes, 16, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    // One latent row per box row; gather4 takes four row coordinates per copy.
+    if (!encode_tmap_2d(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kLatentDim, cache_rows,
+                        kLatentDim * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    tsc = tkv;
+  }
   // Mid_O [T][H][S][512] fp32 as a 4-D map; a box is 32 dims x 1 split x 32
   // heads x 1 row, 128B-swizzled.
   CUtensorMap to;
@@ -537,12 +679,12 @@ cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
                         CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kern = fp8 ? sparse_mla_kernel<true> : sparse_mla_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.num_splits, a.batch * a.nq);
-  return launch_kernel(sparse_mla_kernel, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0,
-                       2, tq, tkv, to, a);
+  return launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0, 2, tq, tkv, to,
+                       tsc, a);
 }
 
 }  // namespace dsa

@@ -296,6 +296,48 @@ dsa_status dsa_decode_fused_write(const dsa_decode_desc* desc, const uint16_t* n
                                   float sm_scale, int32_t num_splits, int32_t max_seqlen,
                                   float* out, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * FP8 latent cache ("[SGLang] NSA (Narrow Sparse Attention)", its module
+ * list: quant_k_cache / dequant_k_cache, the NSA cache's own FP8
+ * quantisation, read as FP8 by the attention to save bandwidth; "Deepseek
+ * Details", section "FP8 Training": E4M3 with one scale per 1 x 128 tile).
+ * Row layout, 656 bytes: bytes 0..511 the value dims 0..511 as E4M3 codes in
+ * four 128-dim tiles, tile scale = amax / 448 in fp32 (a tile of zeros:
+ * scale 1), codes = E4M3(x / scale) rounded to nearest even and saturated;
+ * bytes 512..527 the four fp32 scales; bytes 528..655 the 64 rope dims as
+ * bf16, unchanged.  The attention over such rows is the attention over their
+ * dequantised values (code x scale).
+ */
+
+/*
+ * Quantises `rows` bf16 latent rows kv [rows, 576] (16-byte aligned) into
+ * FP8 rows kv8 [rows, 656] (16-byte aligned, written).  Both [dev].
+ */
+dsa_status dsa_latent_to_fp8(const uint16_t* kv, int64_t rows, uint8_t* kv8, void* stream);
+
+/*
+ * dsa_sparse_mla_decode_split over the FP8 latent cache kv8 [num_pages * 64,
+ * 656] (16-byte aligned): the selected rows are gathered as FP8 and
+ * dequantised in shared memory to bf16 for the tensor cores (each value
+ * rounded once to bf16).  Other arguments, outputs and errors as there.
+ */
+dsa_status dsa_sparse_mla_decode_split_fp8(const dsa_decode_desc* desc, const uint16_t* q,
+                                           const uint8_t* kv8, const int32_t* topk_idx,
+                                           int32_t num_splits, float sm_scale, float* mid_o,
+                                           float* mid_lse, void* stream);
+
+/*
+ * dsa_decode_fused with the latent cache in FP8 rows (kv8 as in
+ * dsa_sparse_mla_decode_split_fp8); every other argument as there.
+ */
+dsa_status dsa_decode_fused_fp8kv(const dsa_decode_desc* desc,
+                                  const uint8_t* q_fp8, const float* q_scale, const float* w,
+                                  const uint8_t* k_fp8, const float* k_scale,
+                                  const uint16_t* q, const uint8_t* kv8,
+                                  const int32_t* topk_in, int32_t* topk_out,
+                                  float sm_scale, int32_t num_splits, int32_t max_seqlen,
+                                  float* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes dsa_decode_fused needs (num_splits 0 = auto). */
 size_t dsa_workspace_bytes(const dsa_decode_desc* desc, int32_t max_seqlen,
                            int32_t num_splits);

@@ -69,7 +69,7 @@ LATENT_FP8_BYTES = 656   # 512 E4M3 codes + 4 fp32 scales + 64 bf16 rope values
 
 __all__ = [
     "PAGE_SIZE", "INDEX_HEADS", "INDEX_DIM", "LATENT_DIM", "V_DIM",
-    "LATENT_FP8_BYTES", "quantize_latent", "dequantize_latent", "sparse_mla_fp8",
+    "LATENT_FP8_BYTES", "quantize_latent", "dequantize_latent", "sparse_mla_fp8", "attend_fp8",
     "e4m3_table", "decode_e4m3", "decode_bf16", "encode_e4m3", "quantize_index_key",
     "new_token_positions", "cache_write", "visible_lengths",
     "physical_rows", "indexer_logits", "indexer_logits_at", "topk", "attend",
@@ -330,6 +330,11 @@ def attend(q_bits_t, lat_bits, sm_scale):
     """Attention of one query row (bf16 bits [H, 576]) over the given latent
     rows (bf16 bits [n, 576]): the per-query step of ``sparse_mla``."""
     return _attend(decode_bf16(q_bits_t), decode_bf16(lat_bits).reshape(-1, LATENT_DIM), sm_scale)
+
+
+def attend_fp8(q_bits_t, kv8_rows, sm_scale):
+    """``attend`` over FP8 latent rows ([n, 656] bytes, see quantize_latent)."""
+    return _attend(decode_bf16(q_bits_t), dequantize_latent(kv8_rows), sm_scale)
 
 
 def _selected_rows(idx_row, n_pos, vis_t, page_table_row):

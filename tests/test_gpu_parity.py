@@ -525,3 +525,112 @@ def test_workload_sized_sampled(name):
     _sampled_checks(wl, wl, sel, out, logits, check)
     del wl
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- FP8 latent cache
+
+def _fp8_cache(g, layer=0):
+    kv = g.layers[layer].kv
+    kv8 = torch.empty((kv.shape[0], 656), dtype=torch.uint8, device="cuda")
+    api.dsa_latent_to_fp8(kv, kv8)
+    return kv8
+
+
+def test_latent_to_fp8_bit_exact():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((1000, 576)) * np.exp(rng.standard_normal((1000, 1)) * 3)
+    x[0, :128] = 0.0                       # a tile of zeros: scale 1
+    x[1, 128:256] *= 1e30                  # large magnitudes
+    x[2, 300] *= -1e3                      # one outlier in a tile
+    bits = (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kv = torch.from_numpy(bits.view(np.int16)).cuda()
+    kv8 = torch.empty((1000, 656), dtype=torch.uint8, device="cuda")
+    api.dsa_latent_to_fp8(kv, kv8)
+    torch.cuda.synchronize()
+    assert np.array_equal(kv8.cpu().numpy(), O.quantize_latent(bits))
+
+
+@pytest.mark.parametrize("splits", [1, 3, 0])
+@pytest.mark.parametrize("case", MLA_CASES, ids=lambda c: f"{c['base']}-H{c['num_heads']}-k{c['topk']}")
+def test_sparse_mla_fp8_split_and_merge_match_oracle(case, splits):
+    case = dict(case)
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    wl, g = _gpu_wl(base, seqlens=seqlens, heavy="none", **case)
+    a, idx = _oracle_indices(wl)
+    kv8 = _fp8_cache(g)
+    kv8_h = kv8.cpu().numpy()
+    assert np.array_equal(kv8_h, O.quantize_latent(a["kv"]))
+    desc = api.workload_desc(g)
+    S = api.dsa_num_splits_auto(desc) if splits == 0 else splits
+    T, H = wl.spec.num_tokens, wl.spec.num_heads
+    mid_o = torch.empty((T, H, S, 512), dtype=torch.float32, device="cuda")
+    mid_lse = torch.empty((T, H, S), dtype=torch.float32, device="cuda")
+    api.dsa_sparse_mla_decode_split_fp8(desc, g.layers[0].q, kv8,
+                                        torch.from_numpy(idx.astype(np.int32)).cuda(), S,
+                                        wl.spec.sm_scale, mid_o, mid_lse)
+    out, lse = api.run_merge(mid_o, mid_lse)
+    _assert_no_device_error()
+    mo, ml = O.sparse_mla_split(a["q"], None, idx, a["page_table"], a["seqlens"], a["q_per_req"],
+                                a["sm_scale"], S, kv_fp8=kv8_h)
+    _assert_close_att(mid_o.cpu().numpy(), mo, "Mid_O")
+    _assert_close_att(mid_lse.cpu().numpy(), ml, "Mid_LSE")
+    o, l = O.sparse_mla_fp8(a["q"], kv8_h, idx, a["page_table"], a["seqlens"], a["q_per_req"],
+                            a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "O")
+    _assert_close_att(lse.cpu().numpy(), l, "LSE")
+
+
+@pytest.mark.parametrize("case", [c for c in FUSED_CASES if c["base"] != "short_dense"],
+                         ids=lambda c: c["base"])
+def test_fused_layer_fp8_latent(case):
+    """The layer over the FP8 latent cache: the same selection as the bf16
+    layer (the indexer and top-k do not read the latent cache), and the
+    attention over the dequantised rows."""
+    case = dict(case)
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    wl, g = _gpu_wl(base, seqlens=seqlens, **case)
+    T, k, H = wl.spec.num_tokens, wl.spec.topk, wl.spec.num_heads
+    kv8 = _fp8_cache(g)
+    sel16 = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    api.run_decode(g, topk_out=sel16)
+    sel8 = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, H, 512), dtype=torch.float32, device="cuda")
+    lc = g.layers[0]
+    api.dsa_decode_fused_fp8kv(api.workload_desc(g), g.q_fp8, g.q_scale, g.w, lc.k_fp8, lc.k_scale,
+                               lc.q, kv8, out, api.alloc_workspace(g), g.max_seqlen,
+                               wl.spec.sm_scale, topk_out=sel8)
+    torch.cuda.synchronize()
+    _assert_no_device_error()
+    assert torch.equal(sel8, sel16)
+    a = W.host_arrays(wl)
+    o, _ = O.sparse_mla_fp8(a["q"], kv8.cpu().numpy(), sel8.cpu().numpy(), a["page_table"],
+                            a["seqlens"], a["q_per_req"], a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "O")
+
+
+@pytest.mark.parametrize("name", ["long_128k", "mtp_32k"])
+def test_fused_layer_fp8_latent_workload_sized(name):
+    wl = W.make_workload(name, device="cuda")
+    T, k, H = wl.spec.num_tokens, wl.spec.topk, wl.spec.num_heads
+    kv8 = _fp8_cache(wl)
+    sel = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    out = torch.empty((T, H, 512), dtype=torch.float32, device="cuda")
+    lc = wl.layers[0]
+    api.dsa_decode_fused_fp8kv(api.workload_desc(wl), wl.q_fp8, wl.q_scale, wl.w, lc.k_fp8,
+                               lc.k_scale, lc.q, kv8, out, api.alloc_workspace(wl), wl.max_seqlen,
+                               wl.spec.sm_scale, topk_out=sel)
+    torch.cuda.synchronize()
+    _assert_no_device_error()
+    table = wl.page_table.cpu().numpy()
+    sel_np = sel.cpu().numpy()
+    for t in sorted({0, T // 2, T - 1}):
+        r = t // wl.spec.q_per_req
+        chosen = sel_np[t][sel_np[t] >= 0]
+        rows = torch.from_numpy(O.physical_rows(table[r], chosen)).cuda()
+        # spot-check the stored rows against the oracle's quantisation
+        assert np.array_equal(kv8[rows[:64]].cpu().numpy(),
+                              O.quantize_latent(W.bf16_bits(lc.kv[rows[:64]])))
+        o, _ = O.attend_fp8(W.bf16_bits(lc.q[t]), kv8[rows].cpu().numpy(), wl.spec.sm_scale)
+        _assert_close_att(out[t].cpu().numpy(), o, f"row {t}")
+    del wl
+    torch.cuda.empty_cache()
