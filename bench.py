@@ -397,7 +397,8 @@ def measure_configs(torch, api, W, dev, steps):
     and mli_195k's two layers serial vs with the second layer's indexer +
     top-k on a second stream while its attention reuses the first layer's
     selection; the new tokens' cache write alone (*_cache_write) and fused
-    in front of the layer (*_with_cache_write)."""
+    in front of the layer (*_with_cache_write); long_128k and mtp_32k with
+    the latent cache in FP8 (*_fp8_latent)."""
     res = {}
 
     def timed(make_fn, wls, n):
@@ -546,6 +547,45 @@ def measure_configs(torch, api, W, dev, steps):
         else:
             record(name, wl, timed(plain, copies, n))
         del wl, copies, ws0, out0
+        torch.cuda.empty_cache()
+    # The layer over an FP8 latent cache (656-byte rows: dsa_decode_fused_fp8kv)
+    # on the long-context workloads; the bf16 layer of the same workload is
+    # the headline (long_128k) or the entry above (mtp_32k).
+    for name in ("long_128k", "mtp_32k"):
+        wl = W.make_workload(name, device=dev)
+        copies = [wl] + [clone_workload(W, wl) for _ in range(NCOPY - 1)]
+        ws0 = api.alloc_workspace(wl, api.dsa_num_splits_auto(api.workload_desc(wl)))
+        out0 = torch.empty((wl.spec.num_tokens, wl.spec.num_heads, 512), dtype=torch.float32,
+                           device=dev)
+        kv8s = []
+        for c in copies:
+            kv = c.layers[0].kv
+            kv8 = torch.empty((kv.shape[0], 656), dtype=torch.uint8, device=dev)
+            api.dsa_latent_to_fp8(kv, kv8)
+            kv8s.append(kv8)
+
+        def fp8_layer(i):
+            c, kv8, spec = copies[i], kv8s[i], copies[i].spec
+            cdesc = api.workload_desc(c)
+            splits = api.dsa_num_splits_auto(cdesc)
+            lc, msl = c.layers[0], c.max_seqlen
+
+            def fn():
+                api.dsa_decode_fused_fp8kv(cdesc, c.q_fp8, c.q_scale, c.w, lc.k_fp8, lc.k_scale,
+                                           lc.q, kv8, out0, ws0, msl, spec.sm_scale, splits,
+                                           stream=torch.cuda.current_stream())
+            return fn
+
+        t = timed(fp8_layer, list(range(len(copies))), n)
+        u = accounting(wl.spec, wl.seqlens.cpu().tolist())
+        fp8_bytes = u["indexer_bytes"] + (u["attention_bytes"] // 1152) * 656
+        us = t["us_per_step"]
+        t.update(query_tokens_per_s=u["query_tokens"] / (us * 1e-6), layer_bytes=fp8_bytes,
+                 layer_gbs=fp8_bytes / (us * 1e-6) / 1e9,
+                 frac_of_8tbs=fp8_bytes / (us * 1e-6) / 1e9 / TARGET_HBM_GBS,
+                 note="latent cache in FP8 rows of 656 B (gathered bytes 656 per selected token)")
+        res[name + "_fp8_latent"] = t
+        del copies, kv8s, wl
         torch.cuda.empty_cache()
     return res
 

@@ -72,7 +72,7 @@ constexpr int kOffXchg = kOffMask + (kMaxPos / 32) * 4;    // softmax groups' ex
 constexpr int kOffSc = kOffXchg + 2 * 2 * 128 * 4;         // FP8 rows' tile scales, 2 stages
 constexpr int kScStageBytes = (kBN / 4) * 128;             // 4 rows x 16 B per 128-byte slot
 constexpr int kOffBar = kOffSc + 2 * kScStageBytes;
-constexpr int kNumBars = 14;
+constexpr int kNumBars = 16;
 constexpr int kQStageAtoms = 4;                            // q dims [0, 256) via stage 1
 constexpr int kOffSlot = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;
@@ -91,11 +91,12 @@ constexpr float kRescaleLog2 = 8.0f;
 // FP8 latent rows: 512 E4M3 codes (four 128-dim tiles), the 4 tiles' fp32
 // scales, the 64 rope dims in bf16 -- 656 bytes.
 constexpr int kF8RowBytes = 656;
-constexpr int kF8Copies = (kBN / 4) * 6;                   // 4 code tiles + rope + scales per 4 rows
-constexpr int kF8Issuers = kF8Copies / 2;                  // 48 per CTA (warps 0, 2, 3)
+constexpr int kF8Copies = (kBN / 4) * 4;                   // 2 code halves + rope + scales per 4 rows
+constexpr int kF8Issuers = kF8Copies / 2;                  // 32 per CTA (warps 0, 2, 3)
+constexpr int kRawHalfBytes = kBN * 256;                   // codes 0..255 / 256..511 of 64 rows
 constexpr int kF8TileBytes = kBN * (512 + 128 + 16);       // bytes landing per tile per CTA
 constexpr int kF8Rem = kF8TileBytes - kF8Issuers * (kF8TileBytes / kF8Issuers);
-constexpr int kRawOff = 4 * kAtomBytes;                    // codes land in stage atoms 4..7
+constexpr int kRawOff = 4 * kAtomBytes;                    // codes land in stage bytes 32..64 KB
 constexpr int kConvThreads = 128;                          // warps 8-11 dequantise
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -129,14 +130,16 @@ __device__ __forceinline__ void dequant_chunk(uint8_t* stage, int a, int j, int 
 }
 
 // kFp8: the latent cache holds FP8 rows (kF8RowBytes); tmap_kv then maps its
-// bytes with 128-byte boxes (code tiles, rope) and tmap_sc with 16-byte boxes
-// (the scales).  Otherwise tmap_kv maps the bf16 cache and tmap_sc is unused.
+// bytes with plain 256-byte boxes (codes), tmap_rope with 128B-swizzled
+// 128-byte boxes (the rope dims) and tmap_sc with 16-byte boxes (the
+// scales).  Otherwise tmap_kv maps the bf16 cache and the others are unused.
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_kv,
                       const __grid_constant__ CUtensorMap tmap_o,
-                      const __grid_constant__ CUtensorMap tmap_sc, const MlaLaunch p) {
+                      const __grid_constant__ CUtensorMap tmap_sc,
+                      const __grid_constant__ CUtensorMap tmap_rope, const MlaLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   const int split = blockIdx.x >> 1, half = blockIdx.x & 1, t = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -181,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define KV_FULL(s) (bar0 + 48u + 8u * (s))
 #define KV_EMPTY(s) (bar0 + 64u + 8u * (s))
 #define KV_CONV(s) (bar0 + 96u + 8u * (s))
+#define KV_CONV_A(s) (bar0 + 112u + 8u * (s))
 
   if (threadIdx.x == 0) {
     mbar_init(Q_FULL, 1);
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(KV_FULL(s), kFp8 ? kF8Issuers : kIssuers);   // one expect-tx arrive per issuer
       mbar_init(KV_EMPTY(s), 2);                  // both CTAs' MMAs done with the stage
       mbar_init(KV_CONV(s), kConvThreads);        // FP8: the stage dequantised
+      mbar_init(KV_CONV_A(s), kConvThreads);      // FP8: its bf16 atoms 0-3 (dims 0..255)
     }
     fence_mbar_init();
   }
@@ -226,7 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmap_q);
       prefetch_tmap(&tmap_kv);
       prefetch_tmap(&tmap_o);
-      if (kFp8) prefetch_tmap(&tmap_sc);
+      if (kFp8) {
+        prefetch_tmap(&tmap_sc);
+        prefetch_tmap(&tmap_rope);
+      }
       mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
       mbar_expect_tx(Q_STAGE, kQStageAtoms * kQAtomBytes);
       const uint64_t pol_q = policy_evict_last();
@@ -279,11 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0;
     if constexpr (kFp8) {
       if (lw < 3) {
-        // Warps 0, 2, 3 gather: per tile 96 copies of 4 rows each (per row
-        // group: the four code tiles into stage atoms 4..7, the rope dims
-        // into atom 8, the scales into the scale area); this CTA issues
-        // c = crank mod 2, one per thread, announcing its share of the
-        // 41984 bytes that land in each CTA.
+        // Warps 0, 2, 3 gather: per tile 64 copies of 4 rows each (per row
+        // group: codes 0..255 and 256..511 as plain 256-byte rows into the
+        // raw halves at stage bytes 32 KB and 48 KB, the rope dims 128B-
+        // swizzled into atom 8, the scales into the scale area); this CTA
+        // issues c = crank mod 2, one per thread, announcing its share of
+        // the 41984 bytes that land in each CTA.
         const int g8 = lane * 3 + lw;
         for (int it = 0; it < ntiles && g8 < kF8Issuers; ++it) {
           const int st = it & 1;
@@ -300,29 +309,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(kF8TileBytes / kF8Issuers +
                                                              (g8 < kF8Rem ? 1 : 0)));
           const int c = 2 * g8 + static_cast<int>(crank);
-          if (c < 64) {
-            const int g = c >> 2, a = c & 3;
+          if (c < 32) {
+            const int g = c >> 1, h = c & 1;
             const int* r4 = rows + 4 * g;
-            tma_gather4_mc(dst + kRawOff + a * kAtomBytes + g * 512, &tmap_kv, 128 * a, r4[0], r4[1],
+            tma_gather4_mc(dst + kRawOff + h * kRawHalfBytes + g * 1024, &tmap_kv, 256 * h, r4[0],
+                           r4[1], r4[2], r4[3], KV_FULL(st), kBoth, pol_kv);
+          } else if (c < 48) {
+            const int* r4 = rows + 4 * (c - 32);
+            tma_gather4_mc(dst + 8 * kAtomBytes + (c - 32) * 512, &tmap_rope, 528, r4[0], r4[1],
                            r4[2], r4[3], KV_FULL(st), kBoth, pol_kv);
-          } else if (c < 80) {
-            const int* r4 = rows + 4 * (c - 64);
-            tma_gather4_mc(dst + 8 * kAtomBytes + (c - 64) * 512, &tmap_kv, 528, r4[0], r4[1], r4[2],
-                           r4[3], KV_FULL(st), kBoth, pol_kv);
           } else {
-            const int* r4 = rows + 4 * (c - 80);
+            const int* r4 = rows + 4 * (c - 48);
             // (a tensor copy's shared-memory destination is 128-byte aligned)
-            tma_gather4_mc(sbase + kOffSc + st * kScStageBytes + (c - 80) * 128, &tmap_sc, 512, r4[0],
+            tma_gather4_mc(sbase + kOffSc + st * kScStageBytes + (c - 48) * 128, &tmap_sc, 512, r4[0],
                            r4[1], r4[2], r4[3], KV_FULL(st), kBoth, pol_kv);
           }
           issued = it + 1;
         }
       } else {
         // Warps 8-11 dequantise each landed stage in place: code tiles 0, 1
-        // (stage bytes 32-48 KB) become bf16 atoms 0-3 (0-32 KB); tiles 2, 3
-        // are read into registers first, because their bf16 atoms 4-7 cover
-        // the codes themselves.
+        // (raw half 0) become bf16 atoms 0-3 (0-32 KB); tiles 2, 3 are read
+        // into registers first, because their bf16 atoms 4-7 cover the codes
+        // themselves.  The eight lanes of a quarter warp take rows j0, j0 + 1
+        // (j0 even) and the chunks c of one row in 0..3, of the other in 4..7,
+        // so that each quarter warp's 16-byte reads and writes fall on eight
+        // distinct bank groups.
         const int ctid = (lw - 3) * 32 + lane;
+        const int l8 = ctid & 7, qw = ctid >> 3;
         for (int it = 0; it < ntiles; ++it) {
           const int st = it & 1;
           if (!mbar_wait(KV_FULL(st), (it >> 1) & 1)) {
@@ -335,10 +348,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           float ksc[8];
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
-            const int item = ctid + kConvThreads * u;
-            const int a = u >> 2, j = (item >> 3) & (kBN - 1), c = item & 7;
-            const uint4 raw = *reinterpret_cast<const uint4*>(stg + kRawOff + a * kAtomBytes + j * 128 +
-                                                              ((c ^ (j & 7)) << 4));
+            const int a = u >> 2, v = u & 1, rp = (u >> 1) & 1;
+            const int j = 2 * (qw + 16 * rp) + (l8 >> 2);
+            const int c = (l8 & 3) + 4 * ((l8 >> 2) ^ v);
+            const uint4 raw = *reinterpret_cast<const uint4*>(
+                stg + kRawOff + (a >> 1) * kRawHalfBytes + j * 256 + (a & 1) * 128 + c * 16);
             const float sc = scs[(j >> 2) * 32 + (j & 3) * 4 + a];
             if (u < 8) {
               dequant_chunk(stg, a, j, c, raw, sc);
@@ -347,11 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               ksc[u - 8] = sc;
             }
           }
+          // Atoms 0-3 are ready: the Q K^T MMAs on dims 0..255 may start.
+          fence_proxy_async_smem();
+          mbar_arrive(KV_CONV_A(st));
           named_bar_sync(4, kConvThreads);
 #pragma unroll
           for (int u = 8; u < 16; ++u) {
-            const int item = ctid + kConvThreads * u;
-            dequant_chunk(stg, u >> 2, (item >> 3) & (kBN - 1), item & 7, keep[u - 8], ksc[u - 8]);
+            const int v = u & 1, rp = (u >> 1) & 1;
+            dequant_chunk(stg, u >> 2, 2 * (qw + 16 * rp) + (l8 >> 2), (l8 & 3) + 4 * ((l8 >> 2) ^ v),
+                          keep[u - 8], ksc[u - 8]);
           }
           fence_proxy_async_smem();   // generic-proxy writes -> the MMAs' reads
           mbar_arrive(KV_CONV(st));
@@ -430,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_pv();
             continue;
           }
-          if (mbar_test_wait(kFp8 ? KV_CONV(st) : KV_FULL(st), (it >> 1) & 1) &&
+          if (mbar_test_wait(kFp8 ? KV_CONV_A(st) : KV_FULL(st), (it >> 1) & 1) &&
               (it == 0 || mbar_test_wait(S_FREE, (it - 1) & 1)))
             break;
           if (clock64() - t0 > kWaitCycles) {
@@ -443,10 +461,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage = sbase + kOffStage + st * kStageBytes;
 #pragma unroll
         for (int j = 0; j < kQTmemDims / 16; ++j) {
+          if (kFp8 && j == 16) {
+            // FP8: dims 256..575 (atoms 4-7; atom 8 came with the copies)
+            // once the second half of the stage is dequantised.
+            const long long t1 = clock64();
+            while (!mbar_test_wait(KV_CONV(st), (it >> 1) & 1)) {
+              if (pv_ready(it)) issue_pv();
+              if (clock64() - t1 > kWaitCycles) {
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
+            tc_fence_after();
+          }
           mma_f16_ts(tS, tQ + 8 * j, smem_desc_sw128(stage + (j >> 2) * kAtomBytes + (j & 3) * 32, 16, 1024),
                      idesc_qk, j > 0 ? 1u : 0u);
           if ((j & 7) == 7 && pv_ready(it)) issue_pv();
         }
+        if (!ok) break;
 #pragma unroll
         for (int j = kQTmemDims / 16; j < kLatentDim / 16; ++j) {
           const int jq = j - kQTmemDims / 16;
@@ -640,22 +673,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef KV_FULL
 #undef KV_EMPTY
 #undef KV_CONV
+#undef KV_CONV_A
 }
 
 }  // namespace
 
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
   const bool fp8 = a.kv8 != nullptr;
-  CUtensorMap tq, tkv, tsc;
+  CUtensorMap tq, tkv, tsc, trope;
   const uint64_t qrows = static_cast<uint64_t>(a.batch) * a.nq * a.heads;
   const uint64_t cache_rows = static_cast<uint64_t>(a.num_pages) * kPage;
   if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kLatentDim, qrows,
                       kLatentDim * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (fp8) {
-    // The FP8 rows as bytes: 128-byte boxes (a code tile or the rope dims,
-    // 128B-swizzled like the bf16 atoms) and 16-byte boxes (the scales).
+    // The FP8 rows as bytes: plain 256-byte boxes (codes), 128B-swizzled
+    // 128-byte boxes (the rope dims, laid out like a bf16 atom) and 16-byte
+    // boxes (the scales).
     if (!encode_tmap_2d(&tkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv8, kF8RowBytes, cache_rows,
+                        kF8RowBytes, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_2d(&trope, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv8, kF8RowBytes, cache_rows,
                         kF8RowBytes, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&tsc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv8, kF8RowBytes, cache_rows,
                         kF8RowBytes, 16, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -666,6 +703,7 @@ cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
                         kLatentDim * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     tsc = tkv;
+    trope = tkv;
   }
   // Mid_O [T][H][S][512] fp32 as a 4-D map; a box is 32 dims x 1 split x 32
   // heads x 1 row, 128B-swizzled.
@@ -684,7 +722,7 @@ cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.num_splits, a.batch * a.nq);
   return launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0, 2, tq, tkv, to,
-                       tsc, a);
+                       tsc, trope, a);
 }
 
 }  // namespace dsa
