@@ -35,6 +35,12 @@ class DecodeDesc(ctypes.Structure):
                 ("num_pages", c_int32), ("seqlens", c_void_p), ("page_table", c_void_p)]
 
 
+class StepLayout(ctypes.Structure):
+    """Byte offsets of a decode step's inputs in one host/device block."""
+    _fields_ = [("q_fp8", c_size_t), ("q_scale", c_size_t), ("w", c_size_t), ("q", c_size_t),
+                ("seqlens", c_size_t), ("page_table", c_size_t), ("bytes", c_size_t)]
+
+
 _SIGS = {
     "dsa_indexer_logits": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_void_p, c_int64, c_void_p]),
@@ -69,6 +75,11 @@ _SIGS = {
                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_float, c_int32, c_int32, c_void_p, c_void_p,
                                          c_size_t, c_void_p]),
+    "dsa_step_layout_get": (c_int32, [c_int32, c_int32, c_int32, c_int32,
+                                      ctypes.POINTER(StepLayout)]),
+    "dsa_decode_step_host": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
+                                       c_void_p, c_void_p, c_float, c_int32, c_int32, c_void_p,
+                                       c_void_p, c_void_p, c_size_t, c_void_p]),
     "dsa_workspace_bytes": (c_size_t, [ctypes.POINTER(DecodeDesc), c_int32, c_int32]),
     "dsa_num_splits_auto": (c_int32, [ctypes.POINTER(DecodeDesc)]),
     "dsa_status_str": (ctypes.c_char_p, [c_int32]),
@@ -269,6 +280,62 @@ def dsa_decode_fused_fp8kv(desc, q_fp8, q_scale, w, k_fp8, k_scale, q, kv8, out,
         _ptr(topk_in, torch.int32, "topk_in"), _ptr(topk_out, torch.int32, "topk_out"),
         float(sm_scale), int(num_splits), int(max_seqlen), _ptr(out, torch.float32, "out"),
         _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "dsa_decode_fused_fp8kv")
+
+
+def dsa_step_layout_get(batch, q_per_req, num_heads, max_pages) -> StepLayout:
+    lay = StepLayout()
+    _check(lib().dsa_step_layout_get(int(batch), int(q_per_req), int(num_heads), int(max_pages),
+                                     ctypes.byref(lay)), "dsa_step_layout_get")
+    return lay
+
+
+def step_views(block: torch.Tensor, layout: StepLayout, batch, q_per_req, num_heads, max_pages):
+    """Typed views of each step input inside a uint8 block (host or device)
+    laid out by ``dsa_step_layout_get``."""
+    if block.dtype != torch.uint8 or block.dim() != 1 or block.numel() < layout.bytes:
+        raise ValueError("block must be a 1-D uint8 tensor of at least layout.bytes")
+    T = int(batch) * int(q_per_req)
+    parts = (("q_fp8", torch.uint8, (T, 64, 128)), ("q_scale", torch.float32, (T,)),
+             ("w", torch.float32, (T, 64)), ("q", torch.bfloat16, (T, int(num_heads), 576)),
+             ("seqlens", torch.int32, (int(batch),)),
+             ("page_table", torch.int32, (int(batch), int(max_pages))))
+    views = {}
+    for name, dtype, shape in parts:
+        off = getattr(layout, name)
+        n = 1
+        for x in shape:
+            n *= x
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        views[name] = block[off:off + nbytes].view(dtype).view(shape)
+    return views
+
+
+def _host_ptr(t, dtype, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.is_cuda:
+        raise ValueError(f"{name}: expected a host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def dsa_decode_step_host(desc, host_in, dev_in, k_fp8, k_scale, kv, out, host_out, ws, max_seqlen,
+                         sm_scale, num_splits=0, stream=None):
+    """One decode layer from a host input block to a host output (see
+    include/dsa.h): one host-to-device copy, the fused layer, one
+    device-to-host copy, all queued on ``stream``."""
+    _check(lib().dsa_decode_step_host(
+        ctypes.byref(desc), _host_ptr(host_in, torch.uint8, "host_in"),
+        _ptr(dev_in, torch.uint8, "dev_in"), _ptr(k_fp8, torch.uint8, "k_fp8"),
+        _ptr(k_scale, torch.float32, "k_scale"), _u16(kv, "kv"), float(sm_scale),
+        int(num_splits), int(max_seqlen), _ptr(out, torch.float32, "out"),
+        _host_ptr(host_out, torch.float32, "host_out"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        _stream(stream)), "dsa_decode_step_host")
 
 
 def dsa_get_device_error(stream=None) -> int:

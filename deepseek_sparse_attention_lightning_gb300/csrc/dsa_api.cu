@@ -339,7 +339,8 @@ dsa_status fused_layer(const dsa_decode_desc* d, const dsa::CacheWriteLaunch* cw
                        const uint16_t* kv, const uint8_t* kv8, const int32_t* topk_in,
                        int32_t* topk_out,
                        float sm_scale, int32_t num_splits, int32_t max_seqlen, float* out,
-                       void* ws, size_t ws_bytes, void* stream, void* const* stage_events) {
+                       void* ws, size_t ws_bytes, void* stream, void* const* stage_events,
+                       bool check_only = false) {
   dsa_status st = check_desc(d);
   if (st != DSA_OK) return st;
   if (!q || (!kv && !kv8) || !out || !aligned(q, 16) || (kv && !aligned(kv, 16)) ||
@@ -361,6 +362,7 @@ dsa_status fused_layer(const dsa_decode_desc* d, const dsa::CacheWriteLaunch* cw
   if (splits > 32) return DSA_ERR_UNSUPPORTED;
   const FusedWs lay = fused_ws_layout(d, max_seqlen, splits);
   if (!ws || !aligned(ws, 256) || ws_bytes < lay.total) return DSA_ERR_WORKSPACE;
+  if (check_only) return DSA_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int T = rows_of(d);
@@ -480,6 +482,76 @@ dsa_status dsa_decode_fused_fp8kv(const dsa_decode_desc* d, const uint8_t* q_fp8
   if (!kv8) return DSA_ERR_INVALID_ARG;
   return fused_layer(d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, nullptr, kv8, topk_in,
                      topk_out, sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream, nullptr);
+}
+
+namespace {
+
+size_t step_layout(int32_t batch, int32_t q_per_req, int32_t num_heads, int32_t max_pages,
+                   dsa_step_layout* L) {
+  const size_t T = static_cast<size_t>(batch) * q_per_req;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  L->q_fp8 = take(T * DSA_INDEX_HEADS * DSA_INDEX_DIM);
+  L->q_scale = take(T * 4);
+  L->w = take(T * DSA_INDEX_HEADS * 4);
+  L->q = take(T * static_cast<size_t>(num_heads) * DSA_LATENT_DIM * 2);
+  L->seqlens = take(static_cast<size_t>(batch) * 4);
+  L->page_table = take(static_cast<size_t>(batch) * max_pages * 4);
+  L->bytes = off;
+  return off;
+}
+
+}  // namespace
+
+dsa_status dsa_step_layout_get(int32_t batch, int32_t q_per_req, int32_t num_heads,
+                               int32_t max_pages, dsa_step_layout* layout) {
+  if (!layout || batch < 1 || q_per_req < 1 || num_heads < 1 || max_pages < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (batch > DSA_MAX_BATCH || q_per_req > DSA_MAX_Q_PER_REQ || num_heads > 128)
+    return DSA_ERR_UNSUPPORTED;
+  step_layout(batch, q_per_req, num_heads, max_pages, layout);
+  return DSA_OK;
+}
+
+dsa_status dsa_decode_step_host(const dsa_decode_desc* desc, const void* host_in, void* dev_in,
+                                const uint8_t* k_fp8, const float* k_scale, const uint16_t* kv,
+                                float sm_scale, int32_t num_splits, int32_t max_seqlen,
+                                float* out, float* host_out, void* ws, size_t ws_bytes,
+                                void* stream) {
+  if (!desc || !host_in || !dev_in || !aligned(dev_in, 256)) return DSA_ERR_INVALID_ARG;
+  dsa_step_layout L;
+  dsa_status st = dsa_step_layout_get(desc->batch, desc->q_per_req, desc->num_heads,
+                                      desc->max_pages, &L);
+  if (st != DSA_OK) return st;
+  uint8_t* in = static_cast<uint8_t*>(dev_in);
+  dsa_decode_desc d = *desc;
+  d.seqlens = reinterpret_cast<const int32_t*>(in + L.seqlens);
+  d.page_table = reinterpret_cast<const int32_t*>(in + L.page_table);
+  const uint8_t* q_fp8 = in + L.q_fp8;
+  const float* q_scale = reinterpret_cast<const float*>(in + L.q_scale);
+  const float* w = reinterpret_cast<const float*>(in + L.w);
+  const uint16_t* q = reinterpret_cast<const uint16_t*>(in + L.q);
+  // Every argument is checked before the first copy is queued.
+  st = fused_layer(&d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, nullptr, nullptr,
+                   nullptr, sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream, nullptr,
+                   /*check_only=*/true);
+  if (st != DSA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dev_in, host_in, L.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  st = fused_layer(&d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, nullptr, nullptr,
+                   nullptr, sm_scale, num_splits, max_seqlen, out, ws, ws_bytes, stream, nullptr);
+  if (st != DSA_OK) return st;
+  if (host_out) {
+    const size_t ob = static_cast<size_t>(rows_of(&d)) * d.num_heads * DSA_V_DIM * sizeof(float);
+    if (cudaMemcpyAsync(host_out, out, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
 }
 
 dsa_status dsa_get_device_error(void* stream) {

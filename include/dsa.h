@@ -338,6 +338,53 @@ dsa_status dsa_decode_fused_fp8kv(const dsa_decode_desc* desc,
                                   float sm_scale, int32_t num_splits, int32_t max_seqlen,
                                   float* out, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * A decode step whose inputs start in host memory and whose output ends
+ * there.  What changes from one step to the next (index queries and their
+ * scales, head weights, MLA queries, seqlens, page table) is packed in one
+ * block, so that it crosses the host link in one copy; the caches and the
+ * workspace stay in device memory (model state and scratch).  The pages
+ * give no host interface; this packing is the library's.
+ *
+ * dsa_step_layout_get: byte offsets of each input in the block, for
+ * B = batch requests, T = B * q_per_req rows, H = num_heads:
+ *   q_fp8      uint8 [T, 64, 128]        q_scale  float [T]
+ *   w          float [T, 64]             q        bf16  [T, H, 576]
+ *   seqlens    int32 [B]                 page_table int32 [B, max_pages]
+ * Every offset is a multiple of 256; `bytes` is the block size.
+ * DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED for sizes the decode calls reject.
+ */
+typedef struct dsa_step_layout {
+  size_t q_fp8, q_scale, w, q, seqlens, page_table;
+  size_t bytes;
+} dsa_step_layout;
+
+dsa_status dsa_step_layout_get(int32_t batch, int32_t q_per_req, int32_t num_heads,
+                               int32_t max_pages, dsa_step_layout* layout);
+
+/*
+ * One decode layer from host buffers, queued on `stream`:
+ *   1. host_in -> dev_in, one copy of layout.bytes;
+ *   2. dsa_decode_fused over the inputs in dev_in (the seqlens and page_table
+ *      fields of desc are ignored: they are taken from dev_in);
+ *   3. out -> host_out, one copy of T * H * 512 floats (skipped if host_out
+ *      is NULL).
+ *   host_in   [host] the block laid out by dsa_step_layout_get(desc's sizes).
+ *             Page-locked memory (cudaHostAlloc, cudaHostRegister) keeps the
+ *             copies asynchronous; with pageable memory they still happen but
+ *             the call may block until they are done.
+ *   dev_in    [dev]  layout.bytes, 256-byte aligned; overwritten by the copy.
+ *   host_out  [host] float [T, H, 512]; valid once `stream` has passed the call.
+ * k_fp8, k_scale, kv, sm_scale, num_splits, max_seqlen, out, ws and ws_bytes
+ * as in dsa_decode_fused.  Every argument is checked before the first copy
+ * is queued; the errors are those of dsa_decode_fused.
+ */
+dsa_status dsa_decode_step_host(const dsa_decode_desc* desc, const void* host_in, void* dev_in,
+                                const uint8_t* k_fp8, const float* k_scale, const uint16_t* kv,
+                                float sm_scale, int32_t num_splits, int32_t max_seqlen,
+                                float* out, float* host_out, void* ws, size_t ws_bytes,
+                                void* stream);
+
 /* Workspace bytes dsa_decode_fused needs (num_splits 0 = auto). */
 size_t dsa_workspace_bytes(const dsa_decode_desc* desc, int32_t max_seqlen,
                            int32_t num_splits);

@@ -9,6 +9,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from deepseek_sparse_attention_lightning_gb300 import api, build
 
@@ -100,6 +101,41 @@ def test_workspace_checks(L):
                                     None, None, 0.07, 1, 256, FAKE, FAKE, n1, None) == 1
     assert L.dsa_decode_fused_write(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                     None, None, 0.07, 1, 256, FAKE, FAKE, n1 - 1, None) == 3
+
+
+def test_step_layout(L):
+    B, nq, H, mp = 3, 2, 128, 5
+    lay = api.dsa_step_layout_get(B, nq, H, mp)
+    T = B * nq
+    need = [("q_fp8", T * 64 * 128), ("q_scale", T * 4), ("w", T * 64 * 4),
+            ("q", T * H * 576 * 2), ("seqlens", B * 4), ("page_table", B * mp * 4)]
+    end = 0
+    for name, nbytes in need:
+        off = getattr(lay, name)
+        assert off % 256 == 0 and off >= end, name      # aligned, in order, no overlap
+        end = off + nbytes
+    assert lay.bytes >= end and lay.bytes % 256 == 0
+    views = api.step_views(torch.zeros(lay.bytes, dtype=torch.uint8),
+                           lay, B, nq, H, mp)
+    assert views["q"].shape == (T, H, 576) and views["page_table"].shape == (B, mp)
+    out = api.StepLayout()
+    assert L.dsa_step_layout_get(0, 1, 128, 4, ctypes.byref(out)) == 1
+    assert L.dsa_step_layout_get(2, 5, 128, 4, ctypes.byref(out)) == 2
+    assert L.dsa_step_layout_get(2, 1, 128, 4, None) == 1
+
+
+def test_host_step_rejects_bad_arguments_before_any_copy(L):
+    d = ctypes.byref(_fake_desc())
+    n1 = L.dsa_workspace_bytes(d, 256, 1)
+    call = lambda hin, din, ws_bytes, scale=0.07: L.dsa_decode_step_host(
+        d, hin, din, FAKE, FAKE, FAKE, scale, 1, 256, FAKE, FAKE, FAKE, ws_bytes, None)
+    assert call(None, FAKE, n1) == 1                     # no host block
+    assert call(FAKE, None, n1) == 1                     # no device block
+    assert call(FAKE, FAKE + 16, n1) == 1                # device block not 256-byte aligned
+    assert call(FAKE, FAKE, n1 - 1) == 3                 # short workspace
+    assert call(FAKE, FAKE, n1, scale=-1.0) == 1         # bad softmax scale
+    assert L.dsa_decode_step_host(ctypes.byref(_fake_desc(q_per_req=5)), FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, 0.07, 1, 256, FAKE, FAKE, FAKE, n1, None) == 2
 
 
 def test_merge_validation(L):

@@ -268,6 +268,42 @@ def test_fused_decode_layer(case):
     _assert_close_att(out.cpu().numpy(), o, "O")
 
 
+@pytest.mark.parametrize("case", FUSED_CASES[:2], ids=lambda c: c["base"])
+def test_host_step_equals_fused_layer(case):
+    # dsa_decode_step_host: the step's inputs packed in one pinned host block,
+    # one copy in, the fused layer, one copy out.  Same kernels on the same
+    # inputs, so the output must equal dsa_decode_fused's bit for bit; two
+    # calls in a row, the second on other queries, check that nothing of the
+    # first call's block or output is reused.
+    case = dict(case)
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    wl, g = _gpu_wl(base, seqlens=seqlens, **case)
+    spec = wl.spec
+    B, nq, H, mp = spec.batch, spec.q_per_req, spec.num_heads, g.max_pages
+    lay = api.dsa_step_layout_get(B, nq, H, mp)
+    host_in = torch.zeros(lay.bytes, dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty(lay.bytes, dtype=torch.uint8, device="cuda")
+    hv = api.step_views(host_in, lay, B, nq, H, mp)
+    desc = api.workload_desc(g)
+    ws = api.alloc_workspace(g)
+    out = torch.empty((spec.num_tokens, H, 512), dtype=torch.float32, device="cuda")
+    host_out = torch.full((spec.num_tokens, H, 512), float("nan")).pin_memory()
+    for call in range(2):
+        if call == 1:     # new MLA queries for the second step
+            g.layers[0].q.copy_(torch.randn(g.layers[0].q.shape, generator=torch.Generator().manual_seed(7))
+                                .to(torch.bfloat16))
+        for name in ("q_fp8", "q_scale", "w", "seqlens", "page_table"):
+            hv[name].copy_(getattr(g, name).cpu())
+        hv["q"].copy_(g.layers[0].q.cpu())
+        want = api.run_decode(g)
+        api.dsa_decode_step_host(desc, host_in, dev_in, g.k_fp8, g.k_scale, g.kv, out, host_out, ws,
+                                 g.max_seqlen, spec.sm_scale)
+        torch.cuda.synchronize()
+        _assert_no_device_error()
+        assert torch.equal(host_out, want.cpu()), f"call {call}"
+        assert torch.equal(out, want), f"call {call}"
+
+
 def test_fused_reuses_given_selection_on_second_stream():
     # Multi-layer-indexer schedule: layer 2 attends layer 1's selection while
     # layer 2's own indexer + top-k run on another stream.
