@@ -394,9 +394,9 @@ def measure_configs(torch, api, W, dev, steps):
     tiny_4k cold and warm (warm: one copy, so its inputs stay in L2),
     mtp_32k, long_varlen, short_dense as the DSA layer and as the dense path
     (the same attention over every visible token, given as the selection),
-    and mli_195k's two layers serial vs with the second layer's indexer +
-    top-k on a second stream while its attention reuses the first layer's
-    selection; the new tokens' cache write alone (*_cache_write) and fused
+    and mli_195k's two layers serial vs the second layer through
+    dsa_decode_mli (its attention reuses the first layer's selection while
+    its own indexer + top-k run beside it); the new tokens' cache write alone (*_cache_write) and fused
     in front of the layer (*_with_cache_write); long_128k and mtp_32k with
     the latent cache in FP8 (*_fp8_latent)."""
     res = {}
@@ -509,11 +509,6 @@ def measure_configs(torch, api, W, dev, steps):
             T, k = wl.spec.num_tokens, wl.spec.topk
             sel1 = torch.empty((T, k), dtype=torch.int32, device=dev)
             sel2 = torch.empty((T, k), dtype=torch.int32, device=dev)
-            desc0 = api.workload_desc(wl)
-            ld = api.logits_ld(wl)
-            logits2 = torch.empty((T, ld), dtype=torch.float32, device=dev)
-            tws = torch.empty(api.dsa_topk_workspace_bytes(desc0, ld), dtype=torch.uint8, device=dev)
-            side = torch.cuda.Stream()
 
             def serial(c):
                 f1, f2 = plain(c, layer=0, topk_out=sel1), plain(c, layer=1)
@@ -524,19 +519,18 @@ def measure_configs(torch, api, W, dev, steps):
                 return fn
 
             def overlapped(c):
-                f1, f2_reuse = plain(c, layer=0, topk_out=sel1), plain(c, layer=1, topk_in=sel1)
-                desc, lc2 = api.workload_desc(c), c.layers[1]
+                # layer 1 as usual; layer 2 through dsa_decode_mli: its
+                # attention over layer 1's selection, its own indexer + top-k
+                # on the SMs the attention leaves free
+                f1 = plain(c, layer=0, topk_out=sel1)
+                desc, lc2, spec = api.workload_desc(c), c.layers[1], c.spec
+                msl = c.max_seqlen
 
                 def fn():
                     f1()
-                    main = torch.cuda.current_stream()
-                    side.wait_stream(main)
-                    with torch.cuda.stream(side):
-                        api.dsa_indexer_logits(desc, c.q_fp8, c.q_scale, c.w, lc2.k_fp8, lc2.k_scale,
-                                               logits2, ld, side)
-                        api.dsa_topk(desc, logits2, sel2, tws, ld, side)
-                    f2_reuse()
-                    main.wait_stream(side)
+                    api.dsa_decode_mli(desc, c.q_fp8, c.q_scale, c.w, lc2.k_fp8, lc2.k_scale,
+                                       lc2.q, lc2.kv, sel1, sel2, out0, ws0, msl, spec.sm_scale,
+                                       stream=torch.cuda.current_stream())
                 return fn
 
             a = timed(serial, copies, n)

@@ -75,6 +75,11 @@ _SIGS = {
                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_float, c_int32, c_int32, c_void_p, c_void_p,
                                          c_size_t, c_void_p]),
+    "dsa_decode_mli": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_float, c_int32, c_int32, c_void_p, c_void_p, c_size_t,
+                                 c_void_p]),
+    "dsa_num_splits_mli": (c_int32, [ctypes.POINTER(DecodeDesc)]),
     "dsa_step_layout_get": (c_int32, [c_int32, c_int32, c_int32, c_int32,
                                       ctypes.POINTER(StepLayout)]),
     "dsa_decode_step_host": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
@@ -280,6 +285,24 @@ def dsa_decode_fused_fp8kv(desc, q_fp8, q_scale, w, k_fp8, k_scale, q, kv8, out,
         _ptr(topk_in, torch.int32, "topk_in"), _ptr(topk_out, torch.int32, "topk_out"),
         float(sm_scale), int(num_splits), int(max_seqlen), _ptr(out, torch.float32, "out"),
         _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "dsa_decode_fused_fp8kv")
+
+
+def dsa_decode_mli(desc, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, topk_prev, topk_next, out, ws,
+                   max_seqlen, sm_scale, num_splits=0, stream=None):
+    """One layer of the Multi-layer Indexer schedule: attention over
+    ``topk_prev`` while this layer's indexer and top-k write ``topk_next``
+    (see include/dsa.h)."""
+    _check(lib().dsa_decode_mli(
+        ctypes.byref(desc), _ptr(q_fp8, torch.uint8, "q_fp8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(w, torch.float32, "w"), _ptr(k_fp8, torch.uint8, "k_fp8"),
+        _ptr(k_scale, torch.float32, "k_scale"), _u16(q, "q"), _u16(kv, "kv"),
+        _ptr(topk_prev, torch.int32, "topk_prev"), _ptr(topk_next, torch.int32, "topk_next"),
+        float(sm_scale), int(num_splits), int(max_seqlen), _ptr(out, torch.float32, "out"),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "dsa_decode_mli")
+
+
+def dsa_num_splits_mli(desc) -> int:
+    return int(lib().dsa_num_splits_mli(ctypes.byref(desc)))
 
 
 def dsa_step_layout_get(batch, q_per_req, num_heads, max_pages) -> StepLayout:

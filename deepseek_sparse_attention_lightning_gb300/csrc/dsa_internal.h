@@ -40,6 +40,9 @@ struct IndexerLaunch {
   int pdl;              // 1: launched as a programmatic dependent of the workspace clear
   int wait_tail;        // 1: that kernel also writes new tokens' keys: each request's last
                         //    two tiles are read only after it completed
+  int max_ctas;         // > 0: at most this many CTAs (one per SM), else one per SM
+  int no_flush_wait;    // 1: the histogram was zeroed by a kernel that completed before
+                        //    the kernel this one depends on started: flush without waiting
 };
 
 struct TopkLaunch {

@@ -339,6 +339,40 @@ dsa_status dsa_decode_fused_fp8kv(const dsa_decode_desc* desc,
                                   float* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * One layer of the Multi-layer Indexer schedule ("Multi-layer Indexer:
+ * Overlapping Selection and Attention in DeepSeek Sparse Attention",
+ * abstract; "MTP and sparse attention: NSA and DSA", section "New demands on
+ * inference engines", reusing selections): the layer's attention runs over
+ * an earlier layer's selection (topk_prev) while the layer's own indexer and
+ * top-k run at the same time and write the selection a later layer reuses
+ * (topk_next).  On one stream: the workspace clear; the attention over
+ * topk_prev with num_splits splits (0: dsa_num_splits_mli), i.e. on
+ * 2 * T * splits SMs; the indexer launched as the attention's programmatic
+ * dependent, one CTA on each remaining SM (at least a quarter of them); its
+ * top-k into topk_next; the merge of the attention's splits.
+ *   topk_prev [dev] int32 [T, k]  the selection attended (like topk_in)
+ *   topk_next [dev] int32 [T, k]  this layer's selection (like topk_out)
+ *   ws        [dev] dsa_workspace_bytes(desc, max_seqlen, num_splits)
+ *             (num_splits 0 there covers the split count chosen here)
+ * Other arguments and errors as in dsa_decode_fused; the indexer inputs are
+ * required.  `out` equals dsa_decode_fused with topk_in = topk_prev up to the
+ * rounding of another split count, and topk_next equals the selection
+ * dsa_decode_fused writes to topk_out, bit for bit.
+ */
+dsa_status dsa_decode_mli(const dsa_decode_desc* desc,
+                          const uint8_t* q_fp8, const float* q_scale, const float* w,
+                          const uint8_t* k_fp8, const float* k_scale,
+                          const uint16_t* q, const uint16_t* kv,
+                          const int32_t* topk_prev, int32_t* topk_next,
+                          float sm_scale, int32_t num_splits, int32_t max_seqlen,
+                          float* out, void* ws, size_t ws_bytes, void* stream);
+
+/* The attention's split count dsa_decode_mli picks when 0 is passed: its CTAs
+ * (two per split and row) take about a fifth of the SMs, at least one split
+ * per row, at most ceil(k/64) splits. */
+int32_t dsa_num_splits_mli(const dsa_decode_desc* desc);
+
+/*
  * A decode step whose inputs start in host memory and whose output ends
  * there.  What changes from one step to the next (index queries and their
  * scales, head weights, MLA queries, seqlens, page table) is packed in one

@@ -138,6 +138,23 @@ def test_host_step_rejects_bad_arguments_before_any_copy(L):
                                   FAKE, 0.07, 1, 256, FAKE, FAKE, FAKE, n1, None) == 2
 
 
+def test_mli_validation(L):
+    d = ctypes.byref(_fake_desc())
+    n1 = L.dsa_workspace_bytes(d, 256, 0)
+    call = lambda prev, nxt, q_fp8=FAKE, ws_bytes=n1, splits=0: L.dsa_decode_mli(
+        d, q_fp8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, prev, nxt, 0.07, splits, 256, FAKE, FAKE,
+        ws_bytes, None)
+    assert call(None, FAKE) == 1                 # the selection to attend is required
+    assert call(FAKE, None) == 1                 # and the one to write
+    assert call(FAKE, FAKE + 2) == 1             # misaligned
+    assert call(FAKE, FAKE, q_fp8=None) == 1     # the indexer inputs are required
+    assert call(FAKE, FAKE, ws_bytes=16) == 3
+    assert call(FAKE, FAKE, splits=33) == 1      # more splits than 64-key tiles
+    s = L.dsa_num_splits_mli(d)
+    assert 1 <= s <= L.dsa_num_splits_auto(d)
+    assert L.dsa_workspace_bytes(d, 256, s) <= n1
+
+
 def test_merge_validation(L):
     assert L.dsa_merge(-1, 2, FAKE, FAKE, FAKE, None, None) == 1
     assert L.dsa_merge(4, 0, FAKE, FAKE, FAKE, None, None) == 1

@@ -338,6 +338,40 @@ def test_fused_reuses_given_selection_on_second_stream():
     assert overlap > 0.2
 
 
+@pytest.mark.parametrize("nq,splits", [(1, 0), (2, 0), (1, 1), (1, 3)],
+                         ids=["nq1-auto", "nq2-auto", "nq1-s1", "nq1-s3"])
+def test_mli_layer_matches_separate_calls(nq, splits):
+    # dsa_decode_mli: layer 2's attention over layer 1's selection, with layer
+    # 2's indexer + top-k on the SMs the attention leaves free (one stream).
+    # Its selection must equal the fused layer's bit for bit, its output the
+    # oracle's attention over layer 1's selection.
+    wl, g = _gpu_wl("mli_195k", batch=3, q_per_req=nq, num_heads=128, topk=2048,
+                    seqlens=[6000, 9000, 2500], seed=62 + nq)
+    T, k, H = wl.spec.num_tokens, wl.spec.topk, wl.spec.num_heads
+    desc = api.workload_desc(g)
+    sel1 = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    api.run_decode(g, layer=0, topk_out=sel1)
+    sel2_ref = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    api.run_decode(g, layer=1, topk_out=sel2_ref)
+    want = api.run_decode(g, layer=1, topk_in=sel1)
+    lc2 = g.layers[1]
+    ws = api.alloc_workspace(g, splits)
+    out = torch.full((T, H, 512), float("nan"), device="cuda")
+    sel2 = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    for _ in range(2):      # twice: the second call starts from the first call's workspace
+        api.dsa_decode_mli(desc, g.q_fp8, g.q_scale, g.w, lc2.k_fp8, lc2.k_scale, lc2.q, lc2.kv,
+                           sel1, sel2, out, ws, g.max_seqlen, wl.spec.sm_scale, splits)
+        torch.cuda.synchronize()
+        _assert_no_device_error()
+        assert torch.equal(sel2, sel2_ref)
+        # another split count rounds P (bf16) under other running maxima
+        _assert_close_att(out.cpu().numpy(), want.cpu().numpy(), "MLI vs fused (topk_in)")
+    a2 = W.host_arrays(wl, layer=1)
+    o2, _ = O.sparse_mla(a2["q"], a2["kv"], sel1.cpu().numpy(), a2["page_table"], a2["seqlens"],
+                         nq, a2["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o2, "MLI layer output on layer-1 selection")
+
+
 # ---------------------------------------------------------------- errors
 
 def test_device_check_flags_bad_page_id():
