@@ -486,13 +486,13 @@ dsa_status dsa_decode_fused_fp8kv(const dsa_decode_desc* d, const uint8_t* q_fp8
 
 int32_t dsa_num_splits_mli(const dsa_decode_desc* d) {
   if (!d || d->batch < 1 || d->q_per_req < 1 || d->topk < 1) return 1;
-  // The attention takes about a fifth of the SMs (two CTAs per split), the
-  // indexer beside it the rest; then the fewest splits with the same number
-  // of 64-key tiles per split.
+  // The attention shares the GPU with the top-k, which holds up to ~40 % of
+  // the SMs: its CTAs (two per split) take about 58 % of them; then the
+  // fewest splits with the same number of 64-key tiles per split.
   const int T = rows_of(d);
   const int sms = dsa::device_sm_count();
   const int tiles = max_splits(d);
-  int s = (sms + 5 * T) / (10 * T);
+  int s = (sms * 7 / 12) / (2 * T);
   if (s < 1) s = 1;
   if (s > tiles) s = tiles;
   const int per = (tiles + s - 1) / s;
@@ -520,30 +520,15 @@ dsa_status dsa_decode_mli(const dsa_decode_desc* d, const uint8_t* q_fp8, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int T = rows_of(d);
-  const int sms = dsa::device_sm_count();
 
-  // 1. The top-k histogram and control words start at zero.  A plain launch:
-  //    it completes before the attention starts, so the indexer (which starts
-  //    after the attention) sees the zeros without waiting for any kernel.
+  // 1-3. The layer's own selection, as in the fused layer: the workspace
+  //      clear, the indexer (one CTA per SM) as its programmatic dependent,
+  //      the top-k as the indexer's, writing topk_next.
   const long long n16 = static_cast<long long>((lay.cand - lay.hist) / 16);
   const int cgrid = static_cast<int>(std::min<long long>((n16 + 255) / 256, 148));
   cudaError_t e = dsa::launch_kernel(ws_clear_kernel, dim3(cgrid), dim3(256), 0, s, false, 1,
                                      reinterpret_cast<uint4*>(base + lay.hist), n16);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
-  // 2. The attention over the earlier layer's selection, on 2 * T * splits SMs.
-  dsa::MlaLaunch ma{};
-  ma.q = q; ma.kv = kv; ma.kv8 = nullptr; ma.topk_idx = topk_prev; ma.seqlens = d->seqlens;
-  ma.page_table = d->page_table;
-  ma.mid_o = splits > 1 ? reinterpret_cast<float*>(base + lay.mid_o) : out;
-  ma.mid_lse = reinterpret_cast<float*>(base + lay.mid_lse);
-  ma.batch = d->batch; ma.nq = d->q_per_req; ma.heads = d->num_heads; ma.k = d->topk;
-  ma.max_pages = d->max_pages; ma.num_pages = d->num_pages; ma.num_splits = splits;
-  ma.sm_scale = sm_scale; ma.pdl = 0;
-  e = dsa::launch_sparse_mla(ma, s);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
-  // 3. This layer's indexer as the attention's programmatic dependent: its
-  //    CTAs take the SMs the attention leaves free (one per SM) and read
-  //    nothing the attention writes; its grid completes after the attention's.
   dsa::IndexerLaunch ia{};
   ia.q_fp8 = q_fp8; ia.q_scale = q_scale; ia.w = w; ia.k_fp8 = k_fp8; ia.k_scale = k_scale;
   ia.seqlens = d->seqlens; ia.page_table = d->page_table;
@@ -551,17 +536,29 @@ dsa_status dsa_decode_mli(const dsa_decode_desc* d, const uint8_t* q_fp8, const 
   ia.hist = reinterpret_cast<uint32_t*>(base + lay.hist);
   ia.batch = d->batch; ia.nq = d->q_per_req; ia.max_pages = d->max_pages;
   ia.num_pages = d->num_pages; ia.topk = d->topk; ia.skip_short = 1; ia.pdl = 1;
-  ia.max_ctas = std::max(sms - 2 * T * splits, sms / 4);
-  ia.no_flush_wait = 1;
   e = dsa::launch_indexer(ia, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
-  // 4. Its top-k, writing the selection a later layer reuses.
   dsa::TopkLaunch ta{};
   ta.seqlens = d->seqlens; ta.logits = ia.logits; ta.ld = lay.ld; ta.out = topk_next;
   ta.hist = ia.hist; ta.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
   ta.cand = reinterpret_cast<uint2*>(base + lay.cand);
   ta.batch = d->batch; ta.nq = d->q_per_req; ta.k = d->topk; ta.hist_ready = 1; ta.pdl = 1;
   e = dsa::launch_topk(ta, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  // 4. The attention over the earlier layer's selection as the top-k's
+  //    programmatic dependent: its CTAs start once every top-k CTA runs,
+  //    on the SMs the top-k leaves free, and read topk_prev without waiting
+  //    (it was complete before this call); its grid completes after the
+  //    top-k's.
+  dsa::MlaLaunch ma{};
+  ma.q = q; ma.kv = kv; ma.kv8 = nullptr; ma.topk_idx = topk_prev; ma.seqlens = d->seqlens;
+  ma.page_table = d->page_table;
+  ma.mid_o = splits > 1 ? reinterpret_cast<float*>(base + lay.mid_o) : out;
+  ma.mid_lse = reinterpret_cast<float*>(base + lay.mid_lse);
+  ma.batch = d->batch; ma.nq = d->q_per_req; ma.heads = d->num_heads; ma.k = d->topk;
+  ma.max_pages = d->max_pages; ma.num_pages = d->num_pages; ma.num_splits = splits;
+  ma.sm_scale = sm_scale; ma.pdl = 1; ma.sel_ready = 1;
+  e = dsa::launch_sparse_mla(ma, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   // 5. The merge of the attention's splits.
   if (splits > 1) {

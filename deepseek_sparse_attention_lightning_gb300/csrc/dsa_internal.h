@@ -40,9 +40,6 @@ struct IndexerLaunch {
   int pdl;              // 1: launched as a programmatic dependent of the workspace clear
   int wait_tail;        // 1: that kernel also writes new tokens' keys: each request's last
                         //    two tiles are read only after it completed
-  int max_ctas;         // > 0: at most this many CTAs (one per SM), else one per SM
-  int no_flush_wait;    // 1: the histogram was zeroed by a kernel that completed before
-                        //    the kernel this one depends on started: flush without waiting
 };
 
 struct TopkLaunch {
@@ -83,6 +80,9 @@ struct MlaLaunch {
   int batch, nq, heads, k, max_pages, num_pages, num_splits;
   float sm_scale;
   int pdl;              // 1: launched as a programmatic dependent of the top-k
+  int sel_ready;        // 1: topk_idx was complete before the kernel this one depends on
+                        //    started (read without waiting); with pdl the grid then
+                        //    completes only after that kernel
 };
 
 cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t s);

@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto flush_hist = [&](int req) {
       // The histogram may be cleared by the kernel before (fused path): the
       // first global atomic waits for it; everything earlier does not.
-      if (!p.no_flush_wait) grid_dep_wait();
+      grid_dep_wait();
       named_bar_sync(bar_id, 128);
       for (int i = 0; i < NQ; ++i) {
         uint32_t* gh = p.hist + static_cast<long long>(req * NQ + i) * kHistBins;
@@ -510,8 +510,7 @@ cudaError_t launch_nq(const IndexerLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(indexer_kernel<NQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  int grid = device_sm_count();
-  if (a.max_ctas > 0 && a.max_ctas < grid) grid = a.max_ctas;
+  const int grid = device_sm_count();
   return launch_kernel(indexer_kernel<NQ>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream,
                        a.pdl != 0, 1, tk, tq, a);
 }

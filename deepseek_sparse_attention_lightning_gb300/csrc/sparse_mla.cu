@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (half == 0)
       for (int h = threadIdx.x; h < H; h += kThreads)
         p.mid_lse[(static_cast<long long>(t) * H + h) * S + split] = ninf;
+    if (p.pdl && p.sel_ready && threadIdx.x == 0) grid_dep_wait();
     return;
   }
 
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pg0 = ptab[0];
       if (pg0 >= 0 && pg0 < p.num_pages) safe_row = pg0 * kPage;
     }
-    grid_dep_wait();
+    if (!p.sel_ready) grid_dep_wait();
     // Resolve every position of the split first (logical index -> page table
     // -> cache row).  Groups of 32 positions go round-robin to the three
     // warps, 4 groups per batch so the loads overlap.
@@ -670,6 +671,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // A selection read without waiting: the grid still completes only after
+  // the kernel it depends on (what follows in the stream relies on that).
+  if (p.pdl && p.sel_ready && threadIdx.x == 0) grid_dep_wait();
 #undef KV_FULL
 #undef KV_EMPTY
 #undef KV_CONV

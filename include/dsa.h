@@ -344,13 +344,14 @@ dsa_status dsa_decode_fused_fp8kv(const dsa_decode_desc* desc,
  * abstract; "MTP and sparse attention: NSA and DSA", section "New demands on
  * inference engines", reusing selections): the layer's attention runs over
  * an earlier layer's selection (topk_prev) while the layer's own indexer and
- * top-k run at the same time and write the selection a later layer reuses
- * (topk_next).  On one stream: the workspace clear; the attention over
- * topk_prev with num_splits splits (0: dsa_num_splits_mli), i.e. on
- * 2 * T * splits SMs; the indexer launched as the attention's programmatic
- * dependent, one CTA on each remaining SM (at least a quarter of them); its
- * top-k into topk_next; the merge of the attention's splits.
- *   topk_prev [dev] int32 [T, k]  the selection attended (like topk_in)
+ * top-k run and write the selection a later layer reuses (topk_next).  On
+ * one stream: the workspace clear; the indexer (one CTA per SM) and its
+ * top-k into topk_next, as in dsa_decode_fused; the attention over
+ * topk_prev with num_splits splits (0: dsa_num_splits_mli), launched as the
+ * top-k's programmatic dependent so that it runs on the SMs the
+ * latency-bound top-k leaves free, beside it; the merge of its splits.
+ *   topk_prev [dev] int32 [T, k]  the selection attended (like topk_in);
+ *             complete before the call (written by earlier work on `stream`)
  *   topk_next [dev] int32 [T, k]  this layer's selection (like topk_out)
  *   ws        [dev] dsa_workspace_bytes(desc, max_seqlen, num_splits)
  *             (num_splits 0 there covers the split count chosen here)
@@ -368,8 +369,8 @@ dsa_status dsa_decode_mli(const dsa_decode_desc* desc,
                           float* out, void* ws, size_t ws_bytes, void* stream);
 
 /* The attention's split count dsa_decode_mli picks when 0 is passed: its CTAs
- * (two per split and row) take about a fifth of the SMs, at least one split
- * per row, at most ceil(k/64) splits. */
+ * (two per split and row) take about 58 % of the SMs (the top-k beside it
+ * holds up to ~40 %), at least one split per row, at most ceil(k/64). */
 int32_t dsa_num_splits_mli(const dsa_decode_desc* desc);
 
 /*
