@@ -664,7 +664,6 @@ def run_ours(args, world, rank, local):
     clocks = sampler.stop()
     if api.dsa_get_device_error() != 0:
         raise RuntimeError("device error during the timed steps")
-    del copies
 
     # For comparison: one layer per graph replay with L2 flushed before each
     # (the flush outside the events), so each step also pays the graph's
@@ -706,47 +705,59 @@ def run_ours(args, world, rank, local):
     ms_per_step = total_ms_max / K
     value = throughput(units["query_tokens"], K, world, total_ms_max)
 
-    # ---- end to end through the C ABI from pinned host buffers: each step is
-    # one dsa_decode_step_host call (the step's inputs packed in one pinned
-    # block: one host-to-device copy, the fused layer, one device-to-host copy
-    # of the output).  The caches stay resident in HBM as model state.
+    # ---- end to end from pinned host buffers: HostStepPipeline, one
+    # dsa_decode_fused layer per step with the step's inputs (one packed
+    # block) copied in and its output copied out on side streams, so that
+    # the copies of one step overlap the layers of its neighbours.  The
+    # steps cycle through the input copies' caches (no L2 reuse), and one
+    # event pair brackets all KE steps, copies included.
     e2e = None
     if not args.no_e2e:
         B, nq, mp = spec.batch, spec.q_per_req, wl.max_pages
-        lay = api.dsa_step_layout_get(B, nq, H, mp)
-        host_in = torch.zeros(lay.bytes, dtype=torch.uint8).pin_memory()
-        dev_in = torch.empty(lay.bytes, dtype=torch.uint8, device=dev)
-        hv = api.step_views(host_in, lay, B, nq, H, mp)
-        for n in ("q_fp8", "q_scale", "w", "q", "seqlens", "page_table"):
-            hv[n].copy_(getattr(wl, n).cpu())
-        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        pipe = api.HostStepPipeline(B, nq, H, k, mp, wl.num_pages, max_seqlen, spec.sm_scale,
+                                    splits, device=dev)
+        lay = pipe.layout
+        host_in = [torch.zeros(lay.bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        for hb in host_in:
+            hv = api.step_views(hb, lay, B, nq, H, mp)
+            for n in ("q_fp8", "q_scale", "w", "q", "seqlens", "page_table"):
+                hv[n].copy_(getattr(wl, n).cpu())
+        host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
         h2d = int(lay.bytes)
-        d2h = out_host.numel() * out_host.element_size()
+        d2h = host_out[0].numel() * host_out[0].element_size()
         KE = max(1, min(K, 500))
-        e_start = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
-        e_end = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
-        for i in range(KE + 3):
-            flush.zero_()
-            j = i - 3
-            if j >= 0:
-                e_start[j].record()
-            api.dsa_decode_step_host(desc, host_in, dev_in, wl.k_fp8, wl.k_scale, wl.kv, out,
-                                     out_host, ws, max_seqlen, spec.sm_scale, splits,
-                                     stream=stream)
-            if j >= 0:
-                e_end[j].record()
+
+        def e2e_step(i):
+            c = copies[i % len(copies)]
+            pipe.submit(host_in[i % 2], host_out[i % 2], c.k_fp8, c.k_scale, c.kv, stream=stream)
+
+        for i in range(4):
+            e2e_step(i)
+        pipe.drain(stream)
         torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_start, e_end))
-        e2e_ms = dist_max(e2e_ms, world)
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        for i in range(KE):
+            e2e_step(i)
+        pipe.drain(stream)
+        e_end.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = dist_max(e_start.elapsed_time(e_end), world)
         e2e = {"value": throughput(units["query_tokens"], KE, world, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / KE,
-               "note": "dsa_decode_step_host per step: the step's inputs (index/MLA queries, "
-                       "weights, scales, seqlens, page table) in one pinned host block, one "
-                       "host-to-device copy, the fused layer, one device-to-host copy of the "
-                       "output; the KV caches stay resident in HBM as model state"}
-        if not torch.allclose(out_host, out.cpu()):
+               "note": "HostStepPipeline: per step the inputs (index/MLA queries, weights, "
+                       "scales, seqlens, page table) in one pinned host block copied in, one "
+                       "dsa_decode_fused layer, the output copied back to pinned host memory; "
+                       "copies on side streams overlap the neighbouring steps' layers; one "
+                       "event pair around all steps; the KV caches stay resident in HBM as "
+                       "model state (the steps cycle through the input copies' caches)"}
+        if not torch.allclose(host_out[(KE - 1) % 2], out.cpu()):
             raise RuntimeError("e2e output differs from the device output")
+    del copies
 
     # ---- CPU oracle baseline (rank 0, N = 1)
     cpu = None

@@ -333,6 +333,93 @@ def step_views(block: torch.Tensor, layout: StepLayout, batch, q_per_req, num_he
     return views
 
 
+class HostStepPipeline:
+    """Decode layers whose per-step inputs start in host memory and whose
+    outputs end there, with the copies of one step overlapping the layers of
+    its neighbours.
+
+    Two device input blocks (the layout of ``dsa_step_layout_get``) and two
+    device outputs alternate between steps; the host-to-device copies run on
+    one side stream, the device-to-host copies on another, the layers on the
+    caller's stream, ordered by events: step i (buffer i % 2) copies its block
+    in once the layer of step i - 2 is done reading that buffer, its layer
+    waits for that copy and for the output copy of step i - 2, and its output
+    is copied out after its layer.  So while layer i runs, the inputs of step
+    i + 1 come in and the output of step i - 1 goes out.  Every layer is one
+    ``dsa_decode_fused`` call; the caches and the workspace stay in device
+    memory.  A host block may be rewritten once the copy of the step that
+    read it is done (``input_copied(i)``); ``host_out`` of step i is valid
+    once ``output_copied(i)`` (or ``drain``) has been waited on.
+    """
+
+    def __init__(self, batch, q_per_req, num_heads, topk, max_pages, num_pages, max_seqlen,
+                 sm_scale, num_splits=0, device=None):
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.layout = dsa_step_layout_get(batch, q_per_req, num_heads, max_pages)
+        self.dims = (batch, q_per_req, num_heads, max_pages)
+        self.dev_in = [torch.empty(self.layout.bytes, dtype=torch.uint8, device=device)
+                       for _ in range(2)]
+        self.views = [step_views(d, self.layout, *self.dims) for d in self.dev_in]
+        T = batch * q_per_req
+        self.out = [torch.empty((T, num_heads, 512), dtype=torch.float32, device=device)
+                    for _ in range(2)]
+        self.desc = [make_desc(v["seqlens"], v["page_table"], q_per_req, num_heads, topk, num_pages)
+                     for v in self.views]
+        self.splits = num_splits if num_splits else dsa_num_splits_auto(self.desc[0])
+        self.ws = torch.empty(dsa_workspace_bytes(self.desc[0], max_seqlen, self.splits),
+                              dtype=torch.uint8, device=device)
+        self.max_seqlen, self.sm_scale = int(max_seqlen), float(sm_scale)
+        self.h2d = torch.cuda.Stream(device)
+        self.d2h = torch.cuda.Stream(device)
+        mk = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.ev_in, self.ev_done, self.ev_out = mk(), mk(), mk()
+        self.steps = 0
+
+    def submit(self, host_in, host_out, k_fp8, k_scale, kv, stream=None):
+        """Queues one step: host_in (a pinned uint8 block) -> layer over the
+        given caches -> host_out (pinned float32 [T, H, 512])."""
+        if host_in.dtype != torch.uint8 or host_in.is_cuda or host_in.numel() < self.layout.bytes:
+            raise ValueError("host_in: a host uint8 block of at least layout.bytes")
+        if host_out.is_cuda or host_out.dtype != torch.float32 or host_out.shape != self.out[0].shape:
+            raise ValueError("host_out: a host float32 tensor shaped like the output")
+        comp = torch.cuda.current_stream() if stream is None else stream
+        b = self.steps % 2
+        if self.steps >= 2:
+            self.h2d.wait_event(self.ev_done[b])
+        with torch.cuda.stream(self.h2d):
+            self.dev_in[b].copy_(host_in[:self.layout.bytes], non_blocking=True)
+        self.ev_in[b].record(self.h2d)
+        comp.wait_event(self.ev_in[b])
+        if self.steps >= 2:
+            comp.wait_event(self.ev_out[b])
+        v = self.views[b]
+        dsa_decode_fused(self.desc[b], v["q_fp8"], v["q_scale"], v["w"], k_fp8, k_scale, v["q"], kv,
+                         self.out[b], self.ws, self.max_seqlen, self.sm_scale, self.splits,
+                         stream=comp)
+        self.ev_done[b].record(comp)
+        self.d2h.wait_event(self.ev_done[b])
+        with torch.cuda.stream(self.d2h):
+            host_out.copy_(self.out[b], non_blocking=True)
+        self.ev_out[b].record(self.d2h)
+        self.steps += 1
+
+    def input_copied(self, step):
+        """Event after which the host block of `step` may be rewritten (valid
+        until step + 2 is submitted)."""
+        return self.ev_in[step % 2]
+
+    def output_copied(self, step):
+        """Event after which host_out of `step` holds its output (valid until
+        step + 2 is submitted)."""
+        return self.ev_out[step % 2]
+
+    def drain(self, stream=None):
+        """Makes `stream` (default: the current one) wait for every queued copy."""
+        comp = torch.cuda.current_stream() if stream is None else stream
+        comp.wait_stream(self.h2d)
+        comp.wait_stream(self.d2h)
+
+
 def _host_ptr(t, dtype, name):
     if t is None:
         return None

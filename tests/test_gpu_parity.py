@@ -304,6 +304,41 @@ def test_host_step_equals_fused_layer(case):
         assert torch.equal(out, want), f"call {call}"
 
 
+def test_host_step_pipeline_matches_fused_layer():
+    # HostStepPipeline: five steps with other MLA queries each, copies on side
+    # streams overlapping the neighbouring layers; every step's host output
+    # must equal a direct dsa_decode_fused call on the same inputs, bit for bit.
+    case = dict(FUSED_CASES[0])
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    wl, g = _gpu_wl(base, seqlens=seqlens, **case)
+    spec = wl.spec
+    B, nq, H, mp, T = spec.batch, spec.q_per_req, spec.num_heads, g.max_pages, spec.num_tokens
+    pipe = api.HostStepPipeline(B, nq, H, spec.topk, mp, g.num_pages, g.max_seqlen, spec.sm_scale)
+    lay = pipe.layout
+    steps = 5
+    qs = [torch.randn(g.q.shape, generator=torch.Generator().manual_seed(100 + i)).to(torch.bfloat16)
+          for i in range(steps)]
+    host_in, host_out = [], []
+    for i in range(steps):
+        hb = torch.zeros(lay.bytes, dtype=torch.uint8).pin_memory()
+        hv = api.step_views(hb, lay, B, nq, H, mp)
+        for name in ("q_fp8", "q_scale", "w", "seqlens", "page_table"):
+            hv[name].copy_(getattr(g, name).cpu())
+        hv["q"].copy_(qs[i])
+        host_in.append(hb)
+        host_out.append(torch.full((T, H, 512), float("nan")).pin_memory())
+    for i in range(steps):
+        pipe.submit(host_in[i], host_out[i], g.k_fp8, g.k_scale, g.kv)
+    pipe.drain()
+    torch.cuda.synchronize()
+    _assert_no_device_error()
+    for i in range(steps):
+        g.layers[0].q.copy_(qs[i].cuda())
+        want = api.run_decode(g)
+        torch.cuda.synchronize()
+        assert torch.equal(host_out[i], want.cpu()), f"step {i}"
+
+
 def test_fused_reuses_given_selection_on_second_stream():
     # Multi-layer-indexer schedule: layer 2 attends layer 1's selection while
     # layer 2's own indexer + top-k run on another stream.
