@@ -175,12 +175,14 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ uint32_t s_allsel[kTopkClusterCtas];   // every chunk's selected count, pushed by each
   __shared__ uint32_t s_ccnt[kTopkClusterCtas];   // (CTA 0) every chunk's candidate count, pushed by each
 
-  // Everything this kernel reads may come from the kernel before it.
-  grid_dep_wait();
-  grid_dep_launch();
+  // seqlens is an input of the layer that no kernel before writes: its load
+  // is issued before the wait, so the score loads can follow it at once.
+  // Everything else this kernel reads may come from the kernel before it.
   const int t = blockIdx.y;
   const int k = p.k;
   const int vis = visible(p.seqlens, t, p.nq);
+  grid_dep_wait();
+  grid_dep_launch();
   const int lane = threadIdx.x & 31;
   int32_t* out_row = p.out + static_cast<long long>(t) * k;
 
