@@ -271,6 +271,37 @@ def cpu_cores():
         return os.cpu_count()
 
 
+class OneCore:
+    """Pins every thread of this process (BLAS workers included) to one of
+    its cores for the duration of a `with` block, then restores each thread's
+    affinity: the oracle then runs on a single core."""
+
+    def __enter__(self):
+        self.saved = {}
+        try:
+            allowed = sorted(os.sched_getaffinity(0))
+            self.core = allowed[0]
+            for tid in os.listdir("/proc/self/task"):
+                t = int(tid)
+                try:
+                    self.saved[t] = os.sched_getaffinity(t)
+                    os.sched_setaffinity(t, {self.core})
+                except OSError:
+                    pass
+            self.ok = True
+        except (AttributeError, OSError):
+            self.ok = False
+        return self
+
+    def __exit__(self, *exc):
+        for t, cpus in self.saved.items():
+            try:
+                os.sched_setaffinity(t, cpus)
+            except OSError:
+                pass
+        return False
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -768,6 +799,14 @@ def run_ours(args, world, rank, local):
                "sample": f"{n} query rows ({nreq} whole requests of {args.workload}, one at a time, "
                          f"cycling over its {spec.batch} requests, {spent:.1f} s of oracle time), "
                          "float64 numpy oracle (BLAS threads = cores)"}
+        # the same oracle with every thread pinned to one core
+        with OneCore() as one:
+            if one.ok:
+                n1, spent1, nreq1 = OracleSampler(wl).sample(args.cpu_seconds / 2)
+                cpu["one_core"] = {"value": n1 / spent1, "unit": UNIT, "cores": 1,
+                                   "sample": f"{n1} query rows ({nreq1} whole requests), "
+                                             f"{spent1:.1f} s of oracle time, every thread of "
+                                             "the process pinned to one core"}
 
     configs = None
     if rank == 0 and not args.no_configs:

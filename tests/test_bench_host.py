@@ -73,3 +73,23 @@ def test_layer_sequence_times_exactly_k_steps(steps):
         [j % bench.NCOPY for j in range(steps % G)]
     assert timed == expect
     assert len(barriers) == 2
+
+
+def test_one_core_pins_every_thread_and_restores_them():
+    import threading
+    import bench
+    stop = threading.Event()
+    worker = threading.Thread(target=stop.wait)
+    worker.start()
+    try:
+        tids = [int(t) for t in os.listdir("/proc/self/task")]
+        before = {t: os.sched_getaffinity(t) for t in tids}
+        with bench.OneCore() as one:
+            assert one.ok
+            for t in tids:
+                assert os.sched_getaffinity(t) == {one.core}
+        for t in tids:
+            assert os.sched_getaffinity(t) == before[t]
+    finally:
+        stop.set()
+        worker.join()
