@@ -14,7 +14,7 @@
 // One warp per new token: the 1152-byte latent row moves as 72 16-byte words;
 // each lane holds 4 of the key's 128 values, and a warp-wide maximum gives
 // amax.  The work is a few KB: the kernel is launch-bound, so on the fused
-// layer it also zero-fills the workspace counters, in CTAs of its own.
+// layer it also zero-fills the top-k histogram, in CTAs of its own.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -68,7 +68,7 @@ __device__ __forceinline__ void write_token(const CacheWriteLaunch& p, int t, in
 }
 
 // CTAs [0, ceil(T / kWarps)) write the new tokens; the CTAs after them, if
-// any, zero-fill p.clear (the layer's workspace counters).  The kernel lets
+// any, zero-fill p.clear (the layer's top-k histogram).  The kernel lets
 // its dependent (the indexer) start at once: that kernel waits for it before
 // it reads the new tokens' keys or its first histogram flush.
 __global__ void __launch_bounds__(kWarps * 32) cache_write_kernel(const CacheWriteLaunch p) {

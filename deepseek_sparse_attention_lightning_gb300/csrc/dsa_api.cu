@@ -78,7 +78,6 @@ int device_sm_count() {
 namespace {
 
 using dsa::kHistBins;
-using dsa::kTopkCtlWords;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -119,21 +118,20 @@ int resolve_splits(const dsa_decode_desc* d, int32_t num_splits) {
 dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
 struct TopkWs {
-  size_t hist, counters, cand, total;
+  size_t hist, cand, total;
 };
 
 TopkWs topk_ws_layout(int T, int64_t ld) {
   TopkWs w;
   w.hist = 0;
-  w.counters = w.hist + size_t(T) * kHistBins * 4;
-  w.cand = align256(w.counters + size_t(T) * kTopkCtlWords * 4);
+  w.cand = align256(w.hist + size_t(T) * kHistBins * 4);
   w.total = align256(w.cand + size_t(T) * size_t(ld) * 8);
   return w;
 }
 
 struct FusedWs {
   int64_t ld;
-  size_t logits, hist, counters, cand, topk, mid_o, mid_lse, total;
+  size_t logits, hist, cand, topk, mid_o, mid_lse, total;
 };
 
 FusedWs fused_ws_layout(const dsa_decode_desc* d, int32_t max_seqlen, int splits) {
@@ -142,8 +140,7 @@ FusedWs fused_ws_layout(const dsa_decode_desc* d, int32_t max_seqlen, int splits
   w.ld = ((static_cast<int64_t>(max_seqlen) + 127) / 128) * 128;
   w.logits = 0;
   w.hist = align256(w.logits + size_t(T) * size_t(w.ld) * 4);
-  w.counters = w.hist + size_t(T) * kHistBins * 4;
-  w.cand = align256(w.counters + size_t(T) * kTopkCtlWords * 4);
+  w.cand = align256(w.hist + size_t(T) * kHistBins * 4);
   w.topk = align256(w.cand + size_t(T) * size_t(w.ld) * 8);
   w.mid_o = align256(w.topk + size_t(T) * size_t(d->topk) * 4);
   const size_t mo = splits > 1 ? size_t(T) * d->num_heads * splits * dsa::kVDim * 4 : 0;
@@ -227,7 +224,6 @@ dsa_status dsa_topk(const dsa_decode_desc* d, const float* logits, int64_t ld, i
   dsa::TopkLaunch a{};
   a.seqlens = d->seqlens; a.logits = logits; a.ld = ld; a.out = topk_idx;
   a.hist = reinterpret_cast<uint32_t*>(base + lay.hist);
-  a.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
   a.cand = reinterpret_cast<uint2*>(base + lay.cand);
   a.batch = d->batch; a.nq = d->q_per_req; a.k = d->topk; a.hist_ready = 0;
   return cuda_status(dsa::launch_topk(a, s));
@@ -374,7 +370,7 @@ dsa_status fused_layer(const dsa_decode_desc* d, const dsa::CacheWriteLaunch* cw
   const int32_t* idx = topk_in;
   if (!topk_in) {
     int32_t* sel = topk_out ? topk_out : reinterpret_cast<int32_t*>(base + lay.topk);
-    // Histogram and control words start at zero: a small kernel clears them
+    // The histogram starts at zero: a small kernel clears it
     // and the indexer runs as its dependent (prologue and key stream overlap
     // the clear; only its first histogram flush waits for it).
     const long long n16 = static_cast<long long>((lay.cand - lay.hist) / 16);
@@ -403,7 +399,7 @@ dsa_status fused_layer(const dsa_decode_desc* d, const dsa::CacheWriteLaunch* cw
     if (e != cudaSuccess || !mark(1)) return DSA_ERR_CUDA;
     dsa::TopkLaunch ta{};
     ta.seqlens = d->seqlens; ta.logits = ia.logits; ta.ld = lay.ld; ta.out = sel;
-    ta.hist = ia.hist; ta.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
+    ta.hist = ia.hist;
     ta.cand = reinterpret_cast<uint2*>(base + lay.cand);
     ta.batch = d->batch; ta.nq = d->q_per_req; ta.k = d->topk; ta.hist_ready = 1;
     ta.pdl = 1;   // overlaps its launch with the indexer's last CTAs
@@ -540,7 +536,7 @@ dsa_status dsa_decode_mli(const dsa_decode_desc* d, const uint8_t* q_fp8, const 
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   dsa::TopkLaunch ta{};
   ta.seqlens = d->seqlens; ta.logits = ia.logits; ta.ld = lay.ld; ta.out = topk_next;
-  ta.hist = ia.hist; ta.counters = reinterpret_cast<uint32_t*>(base + lay.counters);
+  ta.hist = ia.hist;
   ta.cand = reinterpret_cast<uint2*>(base + lay.cand);
   ta.batch = d->batch; ta.nq = d->q_per_req; ta.k = d->topk; ta.hist_ready = 1; ta.pdl = 1;
   e = dsa::launch_topk(ta, s);

@@ -20,9 +20,6 @@ constexpr int kTopkChunk = 8192;    // logits per CTA in the top-k passes
 constexpr int kTopkClusterCtas = 16;  // CTAs (chunks) per query row in the select pass
 // Rows of up to 16 chunks of 4 x 8192 scores.
 constexpr int64_t kTopkMaxLd = int64_t(kTopkClusterCtas) * kTopkChunk * 4;
-// Top-k control words of one query row: [0..3] spare, [4 + c] candidate
-// count of chunk c.
-constexpr int kTopkCtlWords = 4 + kTopkClusterCtas;
 
 struct IndexerLaunch {
   const uint8_t* q_fp8;
@@ -48,7 +45,6 @@ struct TopkLaunch {
   int64_t ld;
   int32_t* out;         // [T][k]
   uint32_t* hist;       // [T][kHistBins], zeroed (or filled by the indexer)
-  uint32_t* counters;   // [T][kTopkCtlWords]
   uint2* cand;          // [T][ld]: chunk c's candidates at the chunk's first position
   int batch, nq, k;
   int hist_ready;       // 1: hist already holds the row histograms

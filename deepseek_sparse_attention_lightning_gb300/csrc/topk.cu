@@ -643,7 +643,7 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
 // Top-k without a caller-provided workspace (dsa_topk_noalloc).
 //
 // For callers that cannot allocate device memory at the point where they run
-// the selection, the histogram, control words and candidate lists live in one
+// the selection, the histogram and the candidate lists live in one
 // statically sized device array.  Every GPU that loads the library reserves
 // it (kNoAllocScratchBytes) until the process exits.
 // ---------------------------------------------------------------------------
@@ -652,9 +652,7 @@ namespace {
 constexpr int kNoAllocMaxRows = 64;                 // query rows T
 constexpr long long kNoAllocMaxScores = 1ll << 21;  // T * ld_logits
 constexpr size_t kNoAllocHistBytes = size_t(kNoAllocMaxRows) * kHistBins * 4;
-constexpr size_t kNoAllocCounterOff = kNoAllocHistBytes;
-constexpr size_t kNoAllocCandOff =
-    (kNoAllocCounterOff + size_t(kNoAllocMaxRows) * kTopkCtlWords * 4 + 255) & ~size_t(255);
+constexpr size_t kNoAllocCandOff = (kNoAllocHistBytes + 255) & ~size_t(255);
 constexpr size_t kNoAllocScratchBytes = kNoAllocCandOff + size_t(kNoAllocMaxScores) * 8;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
@@ -709,13 +707,12 @@ extern "C" dsa_status dsa_topk_noalloc(const dsa_decode_desc* d, const float* lo
   uint8_t* base = static_cast<uint8_t*>(noalloc_scratch(&e));
   if (!base) return DSA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The previous call's histogram and counters are still there: clear them.
+  // The previous call's histogram is still there: clear it.
   e = cudaMemsetAsync(base, 0, kNoAllocCandOff, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   TopkLaunch a{};
   a.seqlens = d->seqlens; a.logits = logits; a.ld = ld; a.out = topk_idx;
   a.hist = reinterpret_cast<uint32_t*>(base);
-  a.counters = reinterpret_cast<uint32_t*>(base + kNoAllocCounterOff);
   a.cand = reinterpret_cast<uint2*>(base + kNoAllocCandOff);
   a.batch = d->batch; a.nq = d->q_per_req; a.k = d->topk; a.hist_ready = 0;
   return launch_topk(a, s) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;

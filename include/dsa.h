@@ -149,7 +149,7 @@ size_t dsa_topk_workspace_bytes(const dsa_decode_desc* desc, int64_t ld_logits);
  * selection: an inference-engine plugin or step function that executes after
  * the engine has reserved all of the device's memory for its caches, or a
  * host runtime without a device allocator of its own, where a cudaMalloc
- * would fail or stall the device.  The histogram, counters and candidate
+ * would fail or stall the device.  The histogram and candidate
  * lists then live in a file-scope device array of fixed size (about 16.5 MB)
  * that every GPU loading this library reserves until the process exits.  No
  * call allocates or frees memory.
