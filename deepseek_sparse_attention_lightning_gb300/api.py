@@ -374,6 +374,8 @@ class HostStepPipeline:
         mk = lambda: [torch.cuda.Event() for _ in range(2)]
         self.ev_in, self.ev_done, self.ev_out = mk(), mk(), mk()
         self.steps = 0
+        self._fused = lib().dsa_decode_fused
+        self._calls = {}
 
     def submit(self, host_in, host_out, k_fp8, k_scale, kv, stream=None):
         """Queues one step: host_in (a pinned uint8 block) -> layer over the
@@ -392,10 +394,21 @@ class HostStepPipeline:
         comp.wait_event(self.ev_in[b])
         if self.steps >= 2:
             comp.wait_event(self.ev_out[b])
-        v = self.views[b]
-        dsa_decode_fused(self.desc[b], v["q_fp8"], v["q_scale"], v["w"], k_fp8, k_scale, v["q"], kv,
-                         self.out[b], self.ws, self.max_seqlen, self.sm_scale, self.splits,
-                         stream=comp)
+        # The layer call's arguments are checked and packed once per buffer,
+        # cache set and stream; later steps only issue the call.
+        key = (b, k_fp8.data_ptr(), k_scale.data_ptr(), kv.data_ptr(), k_fp8.dtype, k_scale.dtype,
+               kv.dtype, _stream(comp))
+        args = self._calls.get(key)
+        if args is None:
+            v = self.views[b]
+            args = (ctypes.byref(self.desc[b]), _ptr(v["q_fp8"], torch.uint8, "q_fp8"),
+                    _ptr(v["q_scale"], torch.float32, "q_scale"), _ptr(v["w"], torch.float32, "w"),
+                    _ptr(k_fp8, torch.uint8, "k_fp8"), _ptr(k_scale, torch.float32, "k_scale"),
+                    _u16(v["q"], "q"), _u16(kv, "kv"), None, None, self.sm_scale, self.splits,
+                    self.max_seqlen, _ptr(self.out[b], torch.float32, "out"),
+                    _ptr(self.ws, torch.uint8, "ws"), self.ws.numel(), key[-1])
+            self._calls[key] = args
+        _check(self._fused(*args), "dsa_decode_fused")
         self.ev_done[b].record(comp)
         self.d2h.wait_event(self.ev_done[b])
         with torch.cuda.stream(self.d2h):
