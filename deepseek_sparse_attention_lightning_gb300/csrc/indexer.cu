@@ -14,7 +14,7 @@
 // key scale with no cross-thread reduction, writes the fp32 logit and counts it
 // in a shared-memory histogram of the top 11 key bits (the first top-k pass).
 //
-// Warp roles (384 threads, one persistent CTA per SM):
+// Warp roles (one persistent CTA per SM; 512 threads at n_q = 1, else 384):
 //   warp 0   TMA producer: one 8 KB box per page into a ring of 5-12 stages
 //            (as many as shared memory holds next to the fixed buffers),
 //            issued by 8 lanes for 4 tiles at a time, and the request's FP8
@@ -23,12 +23,15 @@
 //            ~100-170 cycles.
 //   warps 1, 2  MMA issuers (one thread each, alternate tiles); warp 1 owns
 //            TMEM;
-//   warps 4-7, 8-11  two epilogue groups taking alternate tiles (one thread
-//            per TMEM lane / token); each thread loads its token's key scale
-//            three of its tiles ahead.
-// Accumulators: four TMEM buffers when they fit (n_q <= 2), else two, so the
-// MMAs of a tile do not wait for the epilogue of the tile two before it (with
-// two buffers that round trip, not HBM, set the pace).
+//   warps 4-7, 8-11 (and 12-15 at n_q = 1)  epilogue groups taking tiles in
+//            turn (one thread per TMEM lane / token); each thread loads its
+//            token's key scale three of its tiles ahead.  With two groups at
+//            n_q = 1 the epilogue set the pace: the MMA issuers waited for
+//            free accumulators and the producer for free stages a quarter of
+//            the time; a third group takes that wait off.
+// Accumulators: six TMEM buffers at n_q = 1, four when they fit (n_q = 2),
+// else two, so the MMAs of a tile do not wait for the epilogue of the tile
+// a few before it.
 // The page ids of the CTA's tile range are fetched once, by all threads, into
 // shared memory.  Keys are streamed exactly once per request; every query
 // token of the request is served by the same key tile (N = 64 * n_q).
@@ -42,9 +45,7 @@ namespace {
 
 constexpr int kTile = 128;                      // tokens per MMA tile (M)
 constexpr int kStageBytes = kTile * kIndexDim;  // 16 KB of FP8 keys
-constexpr int kThreads = 384;
-constexpr int kEpiWarp0 = 4;
-constexpr int kEpiGroups = 2;   // warps 4-7 take even tiles, warps 8-11 odd tiles
+constexpr int kEpiWarp0 = 4;   // epilogue groups: warps 4-7, 8-11 (, 12-15)
 constexpr int kMaxBatch = 1024;
 constexpr int kPageWin = 512;   // page ids cached in shared memory (256 tiles)
 constexpr int kScaleAhead = 3;  // epilogue scale prefetch distance (own tiles)
@@ -56,16 +57,24 @@ template <int NQ>
 struct Cfg {
   static constexpr int kN = 64 * NQ;
   static constexpr int kQBytes = kN * kIndexDim;
+  // Epilogue groups (four warps each, group gi takes the tiles it = gi mod
+  // kEpiGroups): three at n_q = 1, where the epilogue sets the streaming pace
+  // with two, else two.  Every accumulator buffer must be used by one group
+  // and one MMA issuer only (the tiles it = ab mod kAccBufs), so kAccBufs is
+  // a multiple of both: six buffers of 64 columns at n_q = 1.
+  static constexpr int kEpiGroups = NQ == 1 ? 3 : 2;
+  static constexpr int kThreads = 32 * (kEpiWarp0 + 4 * kEpiGroups);
   // Everything but the key ring; the ring then takes what shared memory is
   // left (up to 14 stages): the ring's bytes in flight set the bandwidth.
   static constexpr int kHistBytes = kEpiGroups * NQ * kHistBins * 2;   // 16-bit bins
   static constexpr int kFixed = 2 * kQBytes + kHistBytes + kEpiGroups * kN * 4 + kPageWin * 4 +
-                                (1024 + 4) * 4 + 64 * 4 + (2 * 14 + 4 + 2 * 4 + 1) * 8 + 16 + 1024;
+                                (1024 + 4) * 4 + 64 * 4 + (2 * 14 + 4 + 2 * 6 + 1) * 8 + 16 + 1024;
   static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesFit > 14 ? 14 : kStagesFit;
   // Accumulator buffers: four when they fit in TMEM, so the MMA of a tile
   // never waits for the epilogue of the tile two before it.
-  static constexpr int kAccBufs = (4 * kN <= 512) ? 4 : 2;
+  static constexpr int kAccBufs = NQ == 1 ? 6 : ((4 * kN <= 512) ? 4 : 2);
+  static_assert(kAccBufs % kEpiGroups == 0 && kAccBufs % 2 == 0, "one group, one issuer per buffer");
   static constexpr int kTmemCols =
       (kAccBufs * kN <= 128) ? 128 : ((kAccBufs * kN <= 256) ? 256 : 512);
   static constexpr int kOffStages = 0;
@@ -87,9 +96,10 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Exclusive prefix sum over the kThreads threads of the block (one value each).
+// Exclusive prefix sum over the Threads threads of the block (one value each).
+template <int Threads>
 __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) {
-  constexpr int kWarps = kThreads / 32;
+  constexpr int kWarps = Threads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -138,7 +148,7 @@ __device__ __forceinline__ int tile_page(const IndexerLaunch& p, const int* pref
 }
 
 template <int NQ>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_q, const IndexerLaunch p) {
   using C = Cfg<NQ>;
@@ -183,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sum += c;
     }
     int total;
-    int run = block_excl_scan(sum, scratch, &total);
+    int run = block_excl_scan<C::kThreads>(sum, scratch, &total);
     if (threadIdx.x == 0) prefix[0] = 0;
 #pragma unroll
     for (int e = 0; e < 3; ++e) {
@@ -192,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r < B) prefix[r + 1] = run;
     }
   }
-  for (int i = threadIdx.x; i < C::kHistBytes / 4; i += kThreads) shist[i] = 0u;
+  for (int i = threadIdx.x; i < C::kHistBytes / 4; i += C::kThreads) shist[i] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(KV_FULL(s), 1);
@@ -228,11 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // them: it looks up its first group's pages itself and starts streaming.
   if (warp != 0) {
     const int n = min(2 * (g1 - g0), kPageWin);
-    for (int i = threadIdx.x - 32; i < n; i += kThreads - 32) {
+    for (int i = threadIdx.x - 32; i < n; i += C::kThreads - 32) {
       const int g = g0 + (i >> 1);
       pages[i] = tile_page(p, prefix, find_request(prefix, B, g), g, i & 1);
     }
-    named_bar_sync(3, kThreads - 32);
+    named_bar_sync(5, C::kThreads - 32);
     if (threadIdx.x == 32) mbar_arrive(PAGES);
   }
   auto page_of = [&](int r, int g, int which) -> int {
@@ -396,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return pg >= 0 ? __ldg(p.k_scale + static_cast<long long>(pg) * kPage + (row & (kPage - 1)))
                      : 0.f;
     };
-    float sk0 = scale_of(g0 + gi), sk1 = scale_of(g0 + gi + kEpiGroups),
-          sk2 = scale_of(g0 + gi + 2 * kEpiGroups);
+    float sk0 = scale_of(g0 + gi), sk1 = scale_of(g0 + gi + C::kEpiGroups),
+          sk2 = scale_of(g0 + gi + 2 * C::kEpiGroups);
     static_assert(kScaleAhead == 3, "three scale registers");
     int r = 0, cur = -1, S = 0;
     bool ok = true;
@@ -420,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(bar_id, 128);
       seg_tiles = 0;
     };
-    for (int g = g0 + gi; g < g1; g += kEpiGroups) {
+    for (int g = g0 + gi; g < g1; g += C::kEpiGroups) {
       const uint32_t it = static_cast<uint32_t>(g - g0);
       while (prefix[r + 1] <= g) ++r;
       if (r != cur) {
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool tok_ok = s < S && page_of(r, g, row >> 6) >= 0;
       sk0 = sk1;
       sk1 = sk2;
-      sk2 = scale_of(g + kScaleAhead * kEpiGroups);
+      sk2 = scale_of(g + kScaleAhead * C::kEpiGroups);
       const uint32_t ab = it % C::kAccBufs;
       if (!mbar_wait(ACC_FULL(ab), (it / C::kAccBufs) & 1)) { ok = false; break; }
       tc_fence_after();
@@ -511,7 +521,7 @@ cudaError_t launch_nq(const IndexerLaunch& a, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = device_sm_count();
-  return launch_kernel(indexer_kernel<NQ>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream,
+  return launch_kernel(indexer_kernel<NQ>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream,
                        a.pdl != 0, 1, tk, tq, a);
 }
 
