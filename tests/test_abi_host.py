@@ -171,3 +171,32 @@ def test_package_import_does_not_load_and_missing_library_fails_loudly(monkeypat
     monkeypatch.setattr(api, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         api.lib()
+
+
+@pytest.mark.parametrize("batch,q_per_req,topk", [(1, 1, 2048), (8, 1, 2048), (4, 1, 2048),
+                                                  (32, 2, 2048), (128, 1, 2048), (1024, 1, 64),
+                                                  (3, 4, 512), (76, 1, 2048)])
+def test_split_rules_stay_in_range(L, batch, q_per_req, topk):
+    d = ctypes.byref(_fake_desc(batch=batch, q_per_req=q_per_req, topk=topk, max_pages=4096,
+                                num_pages=8192))
+    tiles = (topk + 63) // 64
+    auto, mli = L.dsa_num_splits_auto(d), L.dsa_num_splits_mli(d)
+    assert 1 <= mli <= auto <= tiles
+    # the split count divides the positions into equal 64-key-tile blocks with no empty one
+    for s in (auto, mli):
+        per = -(-tiles // s)
+        assert -(-tiles // per) == s
+    # a workspace sized for the automatic count also covers the MLI layer's
+    assert L.dsa_workspace_bytes(d, 4096 * 64, mli) <= L.dsa_workspace_bytes(d, 4096 * 64, 0)
+
+
+@pytest.mark.parametrize("batch,q_per_req,heads,max_pages", [(1, 1, 16, 1), (7, 3, 48, 33),
+                                                             (1024, 1, 128, 2048), (5, 4, 128, 3)])
+def test_step_layout_alignment_across_sizes(L, batch, q_per_req, heads, max_pages):
+    lay = api.dsa_step_layout_get(batch, q_per_req, heads, max_pages)
+    T = batch * q_per_req
+    sizes = [T * 64 * 128, T * 4, T * 64 * 4, T * heads * 576 * 2, batch * 4, batch * max_pages * 4]
+    offs = [lay.q_fp8, lay.q_scale, lay.w, lay.q, lay.seqlens, lay.page_table]
+    assert all(o % 256 == 0 for o in offs) and lay.bytes % 256 == 0
+    ends = [o + n for o, n in zip(offs, sizes)]
+    assert all(e <= o for e, o in zip(ends[:-1], offs[1:])) and ends[-1] <= lay.bytes
