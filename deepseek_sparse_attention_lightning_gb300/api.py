@@ -349,7 +349,9 @@ class HostStepPipeline:
     ``dsa_decode_fused`` call; the caches and the workspace stay in device
     memory.  A host block may be rewritten once the copy of the step that
     read it is done (``input_copied(i)``); ``host_out`` of step i is valid
-    once ``output_copied(i)`` (or ``drain``) has been waited on.
+    once ``output_copied(i)`` (or ``drain``) has been waited on.  Every step
+    of one pipeline runs its layer on the same stream (the steps share one
+    workspace); another stream raises.
     """
 
     def __init__(self, batch, q_per_req, num_heads, topk, max_pages, num_pages, max_seqlen,
@@ -376,6 +378,7 @@ class HostStepPipeline:
         self.steps = 0
         self._fused = lib().dsa_decode_fused
         self._calls = {}
+        self._stream = None
 
     def submit(self, host_in, host_out, k_fp8, k_scale, kv, stream=None):
         """Queues one step: host_in (a pinned uint8 block) -> layer over the
@@ -385,6 +388,10 @@ class HostStepPipeline:
         if host_out.is_cuda or host_out.dtype != torch.float32 or host_out.shape != self.out[0].shape:
             raise ValueError("host_out: a host float32 tensor shaped like the output")
         comp = torch.cuda.current_stream() if stream is None else stream
+        if self._stream is None:
+            self._stream = _stream(comp)
+        elif _stream(comp) != self._stream:
+            raise ValueError("every step of a HostStepPipeline runs on the same stream")
         b = self.steps % 2
         if self.steps >= 2:
             self.h2d.wait_event(self.ev_done[b])
