@@ -618,7 +618,8 @@ def _sampled_checks(wl, g, sel, out, logits, rows_to_check, n_pos=4096):
         _assert_close_att(out[t].cpu().numpy(), o, f"row {t}")
 
 
-@pytest.mark.parametrize("name", ["long_128k", "mtp_32k", "short_dense", "tiny_4k"])
+@pytest.mark.parametrize("name", ["long_128k", "mtp_32k", "short_dense", "tiny_4k", "long_varlen",
+                                  "mli_195k"])
 def test_workload_sized_sampled(name):
     wl = W.make_workload(name, device="cuda")
     T, k = wl.spec.num_tokens, wl.spec.topk
