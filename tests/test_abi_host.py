@@ -200,3 +200,20 @@ def test_step_layout_alignment_across_sizes(L, batch, q_per_req, heads, max_page
     assert all(o % 256 == 0 for o in offs) and lay.bytes % 256 == 0
     ends = [o + n for o, n in zip(offs, sizes)]
     assert all(e <= o for e, o in zip(ends[:-1], offs[1:])) and ends[-1] <= lay.bytes
+
+
+def _declared_prototypes():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(dsa_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text):
+        params = " ".join(m.group(2).split())
+        protos[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return protos
+
+
+def test_binding_signatures_match_the_header():
+    protos = _declared_prototypes()
+    assert protos, "no prototypes parsed"
+    for name, n in protos.items():
+        assert name in api._SIGS, f"{name} declared but not bound"
+        assert len(api._SIGS[name][1]) == n, f"{name}: header has {n} parameters, binding {len(api._SIGS[name][1])}"
