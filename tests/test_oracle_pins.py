@@ -328,6 +328,39 @@ def test_sparse_mla_all_selected_equals_dense_sdpa():
         assert np.allclose(lse[t], ref_lse, rtol=1e-12)
 
 
+def test_decode_layer_with_k_covering_the_context_is_dense_attention():
+    # The whole layer (indexer -> top-k -> sparse MLA) with k >= every visible
+    # length selects every visible token, so its output is dense softmax
+    # attention over the request, as torch computes it.
+    wl, a = _mla_inputs(seqlens=(70, 129), nq=2, seed=11)
+    res = O.decode_layer(a)
+    vis = O.visible_lengths(a["seqlens"], 2)
+    for t, n in enumerate(vis):
+        assert np.array_equal(res["idx"][t][:n], np.arange(n)) and (res["idx"][t][n:] == -1).all()
+        rows = O.physical_rows(a["page_table"][t // 2], np.arange(n))
+        lat = torch.from_numpy(O.decode_bf16(a["kv"][rows]))
+        q = torch.from_numpy(O.decode_bf16(a["q"][t]))
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[None, :, None, :], lat[None, None].expand(1, q.shape[0], n, 576),
+            lat[None, None, :, :512].expand(1, q.shape[0], n, 512), scale=a["sm_scale"])
+        assert np.allclose(res["out"][t], ref[0, :, 0].numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_decode_layer_selects_the_best_fp32_scores():
+    # With k below the visible length: k tokens per row, each with an fp32
+    # score at least that of every visible token left out.
+    wl, a = _mla_inputs(seqlens=(300, 517), nq=1, seed=12)
+    a = dict(a, topk=64)
+    res = O.decode_layer(a)
+    vis = O.visible_lengths(a["seqlens"], 1)
+    for t, n in enumerate(vis):
+        sel = res["idx"][t][res["idx"][t] >= 0]
+        assert len(sel) == 64 and len(np.unique(sel)) == 64 and (sel < n).all()
+        sc = res["scores"][t, :n].astype(np.float32)
+        out = np.setdiff1d(np.arange(n), sel)
+        assert sc[sel].min() >= sc[out].max()
+
+
 def test_sparse_mla_index_order_invariance_and_padding():
     wl, a = _mla_inputs(seqlens=(300,), nq=1)
     rng = np.random.default_rng(9)
