@@ -90,6 +90,7 @@ _SIGS = {
     "dsa_status_str": (ctypes.c_char_p, [c_int32]),
     "dsa_get_device_error": (c_int32, [c_void_p]),
     "dsa_version": (ctypes.c_char_p, []),
+    "dsa_debug_set_wait_cycles": (c_int32, [c_int64]),
 }
 
 _lib = None
@@ -478,6 +479,12 @@ def dsa_status_str(status: int) -> str:
 
 def dsa_version() -> str:
     return lib().dsa_version().decode()
+
+
+def dsa_debug_set_wait_cycles(cycles: int):
+    """Bound of the indexer's pipeline waits in SM cycles (0: the default);
+    a test hook for the timeout path (see include/dsa.h)."""
+    _check(lib().dsa_debug_set_wait_cycles(int(cycles)), "dsa_debug_set_wait_cycles")
 
 
 # ---------------------------------------------------------------------------

@@ -62,6 +62,23 @@ bool encode_tmap_nd(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
   return r == CUDA_SUCCESS;
 }
 
+int check_decode_desc(const ::dsa_decode_desc* d) {
+  if (!d) return ::DSA_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->q_per_req < 1 || d->num_heads < 1 || d->topk < 1 || d->max_pages < 1 ||
+      d->num_pages < 1)
+    return ::DSA_ERR_INVALID_ARG;
+  if (!d->seqlens || !d->page_table || (reinterpret_cast<uintptr_t>(d->seqlens) & 3) ||
+      (reinterpret_cast<uintptr_t>(d->page_table) & 3))
+    return ::DSA_ERR_INVALID_ARG;
+  if (d->batch > DSA_MAX_BATCH || d->q_per_req > DSA_MAX_Q_PER_REQ) return ::DSA_ERR_UNSUPPORTED;
+  if (d->num_heads > 128 || d->num_heads % 16 != 0) return ::DSA_ERR_UNSUPPORTED;
+  if (d->topk > DSA_MAX_TOPK || d->page_size != DSA_PAGE_SIZE) return ::DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->num_pages) * DSA_PAGE_SIZE >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE >= (int64_t(1) << 31))
+    return ::DSA_ERR_UNSUPPORTED;
+  return ::DSA_OK;
+}
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -84,19 +101,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 dsa_status check_desc(const dsa_decode_desc* d) {
-  if (!d) return DSA_ERR_INVALID_ARG;
-  if (d->batch < 1 || d->q_per_req < 1 || d->num_heads < 1 || d->topk < 1 || d->max_pages < 1 ||
-      d->num_pages < 1)
-    return DSA_ERR_INVALID_ARG;
-  if (!d->seqlens || !d->page_table || !aligned(d->seqlens, 4) || !aligned(d->page_table, 4))
-    return DSA_ERR_INVALID_ARG;
-  if (d->batch > DSA_MAX_BATCH || d->q_per_req > DSA_MAX_Q_PER_REQ) return DSA_ERR_UNSUPPORTED;
-  if (d->num_heads > 128 || d->num_heads % 16 != 0) return DSA_ERR_UNSUPPORTED;
-  if (d->topk > DSA_MAX_TOPK || d->page_size != DSA_PAGE_SIZE) return DSA_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(d->num_pages) * DSA_PAGE_SIZE >= (int64_t(1) << 31) ||
-      static_cast<int64_t>(d->max_pages) * DSA_PAGE_SIZE >= (int64_t(1) << 31))
-    return DSA_ERR_UNSUPPORTED;
-  return DSA_OK;
+  return static_cast<dsa_status>(dsa::check_decode_desc(d));
 }
 
 int rows_of(const dsa_decode_desc* d) { return d->batch * d->q_per_req; }
@@ -166,7 +171,13 @@ const char* dsa_status_str(dsa_status s) {
   return "DSA_ERR_UNKNOWN";
 }
 
-const char* dsa_version(void) { return "dsa-gb300 0.1 (sm_103a)"; }
+const char* dsa_version(void) { return "dsa-gb300 0.2 (sm_103a)"; }
+
+dsa_status dsa_debug_set_wait_cycles(int64_t cycles) {
+  if (cycles < 0) return DSA_ERR_INVALID_ARG;
+  dsa::set_indexer_wait_cycles(cycles);
+  return DSA_OK;
+}
 
 int32_t dsa_num_splits_auto(const dsa_decode_desc* d) {
   if (!d || d->batch < 1 || d->q_per_req < 1 || d->topk < 1) return 1;

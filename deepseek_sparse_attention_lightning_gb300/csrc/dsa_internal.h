@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+struct dsa_decode_desc;
+
 namespace dsa {
 
 constexpr int kIndexHeads = 64;
@@ -37,6 +39,7 @@ struct IndexerLaunch {
   int pdl;              // 1: launched as a programmatic dependent of the workspace clear
   int wait_tail;        // 1: that kernel also writes new tokens' keys: each request's last
                         //    two tiles are read only after it completed
+  long long wait_cycles;   // bound of the pipeline waits (set by launch_indexer)
 };
 
 struct TopkLaunch {
@@ -82,6 +85,9 @@ struct MlaLaunch {
 };
 
 cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t s);
+// Bound, in SM cycles, of the indexer's pipeline waits on later launches
+// (<= 0: the default kWaitCycles).
+void set_indexer_wait_cycles(long long cycles);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s);
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t s);
 cudaError_t launch_cache_write(const CacheWriteLaunch& a, cudaStream_t s);
@@ -129,6 +135,8 @@ int fetch_error_merge();
 int fetch_error_cache();
 
 // Host helpers (dsa_api.cu).
+// The checks every entry point applies to a decode descriptor: a dsa_status.
+int check_decode_desc(const ::dsa_decode_desc* d);
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                     uint32_t box_outer, CUtensorMapSwizzle swizzle);

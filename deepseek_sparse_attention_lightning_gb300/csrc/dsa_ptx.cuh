@@ -78,13 +78,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if it
-// did not within kWaitCycles.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// did not within `limit` SM cycles (kWaitCycles unless a caller passes a
+// shorter one).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          long long limit = kWaitCycles) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait(bar, parity, 20)) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
 }
 
@@ -149,30 +151,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// gather4 multicast to the CTAs of `cta_mask` in the cluster: the rows land
-// at offset `dst` of each destination CTA's shared memory and each
-// destination's mbarrier at offset `bar` counts their bytes.
-__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const CUtensorMap* map, int x,
-                                               int r0, int r1, int r2, int r3, uint32_t bar,
-                                               uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8, %9;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar),
-      "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
-// 2-D tiled load multicast to the CTAs of `cta_mask` (as tma_gather4_mc).
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                               uint32_t bar, uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -214,6 +192,18 @@ __device__ __forceinline__ void st_shared_cluster_v2(uint32_t cluster_addr, uint
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+
+// 1-D bulk copy from this CTA's shared memory to another CTA of the cluster:
+// `src` is a shared::cta address, `dst` and `bar` are shared::cluster
+// addresses (from mapa) in the destination CTA, whose mbarrier counts the
+// bytes.  Addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of
@@ -304,14 +294,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// tc_commit arriving on the mbarrier at offset `bar` of every CTA in `cta_mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
       : "memory");
 }
 

@@ -35,6 +35,8 @@
 // The page ids of the CTA's tile range are fetched once, by all threads, into
 // shared memory.  Keys are streamed exactly once per request; every query
 // token of the request is served by the same key tile (N = 64 * n_q).
+#include <atomic>
+
 #include "dsa_ptx.cuh"
 #include "dsa_internal.h"
 
@@ -274,7 +276,10 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
               cur = r;
               ++seg;
               const int qb = seg & 1;
-              if (seg >= 2 && !mbar_wait(Q_EMPTY(qb), ((seg >> 1) - 1) & 1)) { ok = false; break; }
+              if (seg >= 2 && !mbar_wait(Q_EMPTY(qb), ((seg >> 1) - 1) & 1, p.wait_cycles)) {
+                ok = false;
+                break;
+              }
               mbar_expect_tx(Q_FULL(qb), C::kQBytes);
               tma_load_2d(sbase + C::kOffQ + qb * C::kQBytes, &tmap_q, 0, r * C::kN, Q_FULL(qb),
                           pol_q);
@@ -289,7 +294,8 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         const uint32_t st = static_cast<uint32_t>(it) % C::kStages;
         bool armed = true;
         if (act && which == 0) {
-          if (it >= C::kStages) armed = mbar_wait(KV_EMPTY(st), ((it / C::kStages) - 1) & 1);
+          if (it >= C::kStages)
+            armed = mbar_wait(KV_EMPTY(st), ((it / C::kStages) - 1) & 1, p.wait_cycles);
           if (armed) mbar_expect_tx(KV_FULL(st), kStageBytes);
         }
         armed = __shfl_sync(0xffffffffu, armed, lane & ~1);
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         }
         done = min(it0 + kGroup, ntl);
         // From the second group on, the pages come from shared memory.
-        if (it0 == 0 && ntl > kGroup && !mbar_wait(PAGES, 0)) {
+        if (it0 == 0 && ntl > kGroup && !mbar_wait(PAGES, 0, p.wait_cycles)) {
           ok = false;
           break;
         }
@@ -352,13 +358,14 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         const uint32_t it = static_cast<uint32_t>(g - g0);
         if ((it & 1) != mi) continue;
         if (!q_ready) {
-          if (!mbar_wait(Q_FULL(seg & 1), (seg >> 1) & 1)) { ok = false; break; }
+          if (!mbar_wait(Q_FULL(seg & 1), (seg >> 1) & 1, p.wait_cycles)) { ok = false; break; }
           q_ready = true;
         }
         const uint32_t st = it % C::kStages;
-        if (!mbar_wait(KV_FULL(st), (it / C::kStages) & 1)) { ok = false; break; }
+        if (!mbar_wait(KV_FULL(st), (it / C::kStages) & 1, p.wait_cycles)) { ok = false; break; }
         const uint32_t ab = it % C::kAccBufs;
-        if (it >= C::kAccBufs && !mbar_wait(ACC_EMPTY(ab), ((it / C::kAccBufs) - 1) & 1)) {
+        if (it >= C::kAccBufs &&
+            !mbar_wait(ACC_EMPTY(ab), ((it / C::kAccBufs) - 1) & 1, p.wait_cycles)) {
           ok = false;
           break;
         }
@@ -452,35 +459,42 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
       sk1 = sk2;
       sk2 = scale_of(g + kScaleAhead * C::kEpiGroups);
       const uint32_t ab = it % C::kAccBufs;
-      if (!mbar_wait(ACC_FULL(ab), (it / C::kAccBufs) & 1)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + ab * C::kN;
+      // A wait that ran out stops this warp's work on every later tile, but
+      // the loop goes on (through the group's named barriers, which every
+      // thread must pass equally often); the decision is warp-wide because
+      // the TMEM loads are warp-collective.
+      if (!ok || !mbar_wait(ACC_FULL(ab), (it / C::kAccBufs) & 1, p.wait_cycles)) ok = false;
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t tl = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + ab * C::kN;
 #pragma unroll 1
-      for (int i = 0; i < NQ; ++i) {
-        uint32_t acc[64];
-        tmem_ld64(tl + i * 64, acc);
-        if (i == NQ - 1) {
-          tc_fence_before();
-          mbar_arrive(ACC_EMPTY(ab));
-        }
-        const float4* w4 = reinterpret_cast<const float4*>(gw + i * kIndexHeads);
-        float s0 = 0.f, s1 = 0.f;
+        for (int i = 0; i < NQ; ++i) {
+          uint32_t acc[64];
+          tmem_ld64(tl + i * 64, acc);
+          if (i == NQ - 1) {
+            tc_fence_before();
+            mbar_arrive(ACC_EMPTY(ab));
+          }
+          const float4* w4 = reinterpret_cast<const float4*>(gw + i * kIndexHeads);
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const float4 ww = w4[jj];
-          s0 = fmaf(ww.x, fmaxf(__uint_as_float(acc[4 * jj + 0]), 0.f), s0);
-          s1 = fmaf(ww.y, fmaxf(__uint_as_float(acc[4 * jj + 1]), 0.f), s1);
-          s0 = fmaf(ww.z, fmaxf(__uint_as_float(acc[4 * jj + 2]), 0.f), s0);
-          s1 = fmaf(ww.w, fmaxf(__uint_as_float(acc[4 * jj + 3]), 0.f), s1);
-        }
-        if (s < p.ld) {
-          const int vis = S - (NQ - 1 - i);
-          const bool live = tok_ok && s < vis;
-          const float v = live ? (s0 + s1) * sk : ninf;
-          p.logits[static_cast<long long>(r * NQ + i) * p.ld + s] = v;
-          if (p.hist && live) {
-            const uint32_t bin = float_key(v) >> kHistShift;
-            atomicAdd(&ghist[i * (kHistBins / 2) + (bin >> 1)], 1u << (16 * (bin & 1)));
+          for (int jj = 0; jj < 16; ++jj) {
+            const float4 ww = w4[jj];
+            s0 = fmaf(ww.x, fmaxf(__uint_as_float(acc[4 * jj + 0]), 0.f), s0);
+            s1 = fmaf(ww.y, fmaxf(__uint_as_float(acc[4 * jj + 1]), 0.f), s1);
+            s0 = fmaf(ww.z, fmaxf(__uint_as_float(acc[4 * jj + 2]), 0.f), s0);
+            s1 = fmaf(ww.w, fmaxf(__uint_as_float(acc[4 * jj + 3]), 0.f), s1);
+          }
+          if (s < p.ld) {
+            const int vis = S - (NQ - 1 - i);
+            const bool live = tok_ok && s < vis;
+            const float v = live ? (s0 + s1) * sk : ninf;
+            p.logits[static_cast<long long>(r * NQ + i) * p.ld + s] = v;
+            if (p.hist && live) {
+              const uint32_t bin = float_key(v) >> kHistShift;
+              atomicAdd(&ghist[i * (kHistBins / 2) + (bin >> 1)], 1u << (16 * (bin & 1)));
+            }
           }
         }
       }
@@ -505,9 +519,14 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
 #undef ACC_EMPTY
 }
 
+std::atomic<long long> g_wait_cycles{0};
+
 template <int NQ>
-cudaError_t launch_nq(const IndexerLaunch& a, cudaStream_t stream) {
+cudaError_t launch_nq(const IndexerLaunch& a_in, cudaStream_t stream) {
   using C = Cfg<NQ>;
+  IndexerLaunch a = a_in;
+  const long long wc = g_wait_cycles.load(std::memory_order_relaxed);
+  a.wait_cycles = wc > 0 ? wc : kWaitCycles;
   CUtensorMap tk, tq;
   const uint64_t rows = static_cast<uint64_t>(a.num_pages) * kPage;
   const uint64_t qrows = static_cast<uint64_t>(a.batch) * NQ * kIndexHeads;
@@ -526,6 +545,10 @@ cudaError_t launch_nq(const IndexerLaunch& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+void set_indexer_wait_cycles(long long cycles) {
+  g_wait_cycles.store(cycles > 0 ? cycles : 0, std::memory_order_relaxed);
+}
 
 cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t stream) {
   switch (a.nq) {

@@ -11,7 +11,9 @@
 //
 // Why halves: the fp32 output of 128 heads x 512 dims is 256 KB, all of a
 // SM's tensor memory, so one CTA keeps half of it (256 TMEM columns) and the
-// pair of CTAs of a (t, b) both compute S = Q K^T.
+// two CTAs of a (t, b) both compute S = Q K^T.  Each gathers whole rows
+// itself (the second fetch of a row mostly hits L2); no data moves between
+// CTAs.
 //
 // Tensor memory (512 columns):
 //   [  0,256)  O   fp32 accumulator, this CTA's 256 value dims
@@ -25,26 +27,40 @@
 // themselves): the SM's load/store path delivers only ~20 GB/s of scattered
 // 16-byte loads, the copy engine several times that.
 //
+// A stage is two parts with their own full / free barriers: the K part (the
+// other value half's four atoms and the rope atom, read only by Q K^T) and
+// the V part (this CTA's four value atoms, read by Q K^T and P V).  The K part
+// of a stage is free again as soon as Q K^T of its tile is done, so the
+// gathers of the tile two ahead start about a softmax and a P V earlier than
+// if the whole stage waited for P V; Q K^T takes the K part first.
+//
 // Per tile: S = Q K^T is 20 TMEM-A MMAs (dims 0..319) + 16 smem-A MMAs (dims
 // 320..575), M = 128, N = 64, K = 16 (kind::f16, bf16 in, fp32 out).  The
 // softmax threads (two per head = per TMEM lane, each with 32 of the tile's
 // 64 keys) read S, apply the scale in the exp2 domain, keep a running
 // maximum that is raised lazily (the accumulator is rescaled only when a
 // tile's maximum exceeds it by 2^8), write P to TMEM, and P V (4 MMAs,
-// N = 256, V read MN-major from the same smem stage) accumulates into O.  The
-// MMA thread issues P V of a tile as soon as its P is written, also between
-// the MMAs of the next tile's Q K^T, because that P V frees the stage the
-// gather two tiles ahead waits for.
+// N = 256, V read MN-major from the CTA's value atoms) accumulates into O.
+// The MMA thread issues P V of a tile as soon as its P is written, also
+// between the MMAs of the next tile's Q K^T, because that P V frees the
+// V part the gather two tiles ahead waits for.
 //
 // Warp roles (512 threads): warps 0, 2, 3 and 8-11 resolve every selected
 // position to its cache row (logical index -> page table -> row, fused here)
 // and gather the rows with TMA tile::gather4 copies (4 rows x 64 dims each,
-// written in the 128B-swizzled stage layout by the copy engine); 72 threads
-// spread over the seven warps issue one copy each per tile, because the copy
-// engine takes a warp's TMA instructions one lane at a time (~170 cycles
-// each) but the warps' in parallel.  Warp 1 issues the MMAs and owns TMEM;
-// warps 4-7 and 12-15 run the softmax and the epilogue (Mid_O written by
-// 128B-swizzled tensor stores of 32 heads x 32 dims).
+// written in the 128B-swizzled stage layout by the copy engine): 80 threads
+// spread over the seven warps issue one copy of each part per tile (64 of
+// them a V copy), because the copy engine takes a warp's TMA instructions one
+// lane at a time but the warps' in parallel.  Warp 1 issues the MMAs and owns TMEM; warps 4-7 and 12-15 run
+// the softmax and the epilogue (Mid_O written by 128B-swizzled tensor stores
+// of 32 heads x 32 dims).
+//
+// FP8 latent rows (kFp8): per tile 64 copies (the codes of each 4 rows as
+// two plain 256-byte boxes, their rope dims 128B-swizzled straight into atom
+// 8, their scales), issued by warps 0, 2, 3 into one full barrier; warps 8-11
+// dequantise the codes in place into bf16 atoms 0-7 and signal twice, so
+// that Q K^T on dims 0..255 starts after the first half; the stage is freed
+// as a whole after P V.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -72,7 +88,7 @@ constexpr int kOffXchg = kOffMask + (kMaxPos / 32) * 4;    // softmax groups' ex
 constexpr int kOffSc = kOffXchg + 2 * 2 * 128 * 4;         // FP8 rows' tile scales, 2 stages
 constexpr int kScStageBytes = (kBN / 4) * 128;             // 4 rows x 16 B per 128-byte slot
 constexpr int kOffBar = kOffSc + 2 * kScStageBytes;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 20;
 constexpr int kQStageAtoms = 4;                            // q dims [0, 256) via stage 1
 constexpr int kOffSlot = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;
@@ -81,8 +97,9 @@ constexpr int kTmemCols = 512;
 constexpr int kThreads = 512;
 constexpr int kSoftThreads = 256;                          // warps 4-7 and 12-15
 constexpr int kLoaderWarps = 7;                            // warps 0, 2, 3, 8-11
-constexpr int kGathers = (kBN / 4) * kAtoms;               // 144 gather4 copies per tile
-constexpr int kIssuers = kGathers / 2;                     // copies (and issuers) per CTA
+constexpr int kVCopies = 4 * (kBN / 4);                    // V part: 4 atoms x 16 row groups
+constexpr int kKCopies = 5 * (kBN / 4);                    // K part: 4 atoms + rope, 16 groups
+static_assert(kVCopies <= kKCopies && kKCopies <= 32 * kLoaderWarps, "issuers");
 constexpr int kResolveBatch = 4;                           // position groups in flight per loader
 constexpr int kOBoxBytes = 32 * 128;                       // Mid_O box: 32 heads x 32 fp32
 constexpr int kOChunkBytes = 4 * kOBoxBytes;               // the 4 warps' boxes of a chunk
@@ -92,10 +109,7 @@ constexpr float kRescaleLog2 = 8.0f;
 // scales, the 64 rope dims in bf16 -- 656 bytes.
 constexpr int kF8RowBytes = 656;
 constexpr int kF8Copies = (kBN / 4) * 4;                   // 2 code halves + rope + scales per 4 rows
-constexpr int kF8Issuers = kF8Copies / 2;                  // 32 per CTA (warps 0, 2, 3)
 constexpr int kRawHalfBytes = kBN * 256;                   // codes 0..255 / 256..511 of 64 rows
-constexpr int kF8TileBytes = kBN * (512 + 128 + 16);       // bytes landing per tile per CTA
-constexpr int kF8Rem = kF8TileBytes - kF8Issuers * (kF8TileBytes / kF8Issuers);
 constexpr int kRawOff = 4 * kAtomBytes;                    // codes land in stage bytes 32..64 KB
 constexpr int kConvThreads = 128;                          // warps 8-11 dequantise
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -176,16 +190,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
   const uint32_t bar0 = sbase + kOffBar;
   const uint32_t Q_FULL = bar0, Q_TMEM = bar0 + 8, S_FULL = bar0 + 16, S_FREE = bar0 + 24,
-                 P_FULL = bar0 + 32, PV_DONE = bar0 + 40, Q_STAGE = bar0 + 80,
-                 Q_PEER = bar0 + 88;
-  // The two value halves of a split form a cluster: every key row and query
-  // box is fetched once and multicast to both CTAs.
-  const uint32_t crank = cluster_ctarank(), peer = crank ^ 1u;
-  constexpr uint16_t kBoth = 0x3;
-#define KV_FULL(s) (bar0 + 48u + 8u * (s))
-#define KV_EMPTY(s) (bar0 + 64u + 8u * (s))
-#define KV_CONV(s) (bar0 + 96u + 8u * (s))
-#define KV_CONV_A(s) (bar0 + 112u + 8u * (s))
+                 P_FULL = bar0 + 32, PV_DONE = bar0 + 40, Q_STAGE = bar0 + 48,
+                 MMA_DRAIN = bar0 + 56;
+// K_FULL(s) / V_FULL(s): the K / V part of stage s landed (FP8: V_FULL is the
+// whole stage's copies).  K_EMPTY(s): Q K^T of the stage's tile is done (its K
+// part may be overwritten).  V_EMPTY(s): P V of the stage's tile is done (the
+// whole stage may be overwritten).  KV_CONV_A(s) / KV_CONV(s) (FP8): bf16
+// atoms 0-3 / 0-7 of stage s are dequantised.
+#define K_FULL(s) (bar0 + 64u + 8u * (s))
+#define V_FULL(s) (bar0 + 80u + 8u * (s))
+#define K_EMPTY(s) (bar0 + 96u + 8u * (s))
+#define V_EMPTY(s) (bar0 + 112u + 8u * (s))
+#define KV_CONV_A(s) (bar0 + 128u + 8u * (s))
+#define KV_CONV(s) (bar0 + 144u + 8u * (s))
 
   if (threadIdx.x == 0) {
     mbar_init(Q_FULL, 1);
@@ -195,12 +212,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(P_FULL, kSoftThreads);
     mbar_init(PV_DONE, 1);
     mbar_init(Q_STAGE, 1);
-    mbar_init(Q_PEER, 1);                         // the peer's softmax read its q staging
+    mbar_init(MMA_DRAIN, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(KV_FULL(s), kFp8 ? kF8Issuers : kIssuers);   // one expect-tx arrive per issuer
-      mbar_init(KV_EMPTY(s), 2);                  // both CTAs' MMAs done with the stage
-      mbar_init(KV_CONV(s), kConvThreads);        // FP8: the stage dequantised
-      mbar_init(KV_CONV_A(s), kConvThreads);      // FP8: its bf16 atoms 0-3 (dims 0..255)
+      mbar_init(K_FULL(s), kKCopies);             // one expect-tx arrive per copy
+      mbar_init(V_FULL(s), kFp8 ? kF8Copies : kVCopies);
+      mbar_init(K_EMPTY(s), 1);
+      mbar_init(V_EMPTY(s), 1);
+      mbar_init(KV_CONV_A(s), kConvThreads);
+      mbar_init(KV_CONV(s), kConvThreads);
     }
     fence_mbar_init();
   }
@@ -212,17 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   grid_dep_launch();
-  cluster_sync();   // both CTAs' barriers exist before any copy or arrive targets them
 
   if (warp == 0 || warp == 2 || warp == 3 || (warp >= 8 && warp < 12)) {
     // ------------------------------------------------------------ loaders
-    // Seven warps resolve the positions; 72 of their threads, spread evenly
-    // over the seven warps, gather the selected latent rows with TMA gather4
-    // copies into the 128B-swizzled stage layout; each issuing thread
-    // announces its own bytes on the stage's full barrier, then issues.
     const int lw = warp == 0 ? 0 : (warp < 4 ? warp - 1 : warp - 5);   // loader warp 0..6
     const int ltid = lw * 32 + lane;
-    const int gi = lane * kLoaderWarps + lw;   // this thread's copy of the tile (if < kIssuers)
     const int* ptab = p.page_table + static_cast<long long>(r) * p.max_pages;
     const int* idx_row = p.topk_idx + static_cast<long long>(t) * k;
     // Queries, page table and cache are inputs of the layer; only the
@@ -238,13 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_expect_tx(Q_FULL, kQSmemAtoms * kQAtomBytes);
       mbar_expect_tx(Q_STAGE, kQStageAtoms * kQAtomBytes);
-      const uint64_t pol_q = policy_evict_last();
-      for (int a = static_cast<int>(crank); a < kQSmemAtoms; a += 2)
-        tma_load_2d_mc(sbase + kOffQ + a * kQAtomBytes, &tmap_q, kQTmemDims + 64 * a, t * H, Q_FULL,
-                       kBoth, pol_q);
-      for (int a = static_cast<int>(crank); a < kQStageAtoms; a += 2)
-        tma_load_2d_mc(sbase + kOffStage + kStageBytes + a * kQAtomBytes, &tmap_q, 64 * a, t * H,
-                       Q_STAGE, kBoth, pol_q);
+      const uint64_t pol_q = policy_evict_last();   // the other value half reads the same query
+      for (int a = 0; a < kQSmemAtoms; ++a)
+        tma_load_2d(sbase + kOffQ + a * kQAtomBytes, &tmap_q, kQTmemDims + 64 * a, t * H, Q_FULL,
+                    pol_q);
+      for (int a = 0; a < kQStageAtoms; ++a)
+        tma_load_2d(sbase + kOffStage + kStageBytes + a * kQAtomBytes, &tmap_q, 64 * a, t * H,
+                    Q_STAGE, pol_q);
     }
     int safe_row = 0;
     {
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!p.sel_ready) grid_dep_wait();
     // Resolve every position of the split first (logical index -> page table
-    // -> cache row).  Groups of 32 positions go round-robin to the three
+    // -> cache row).  Groups of 32 positions go round-robin to the loader
     // warps, 4 groups per batch so the loads overlap.
     const int npos = ntiles * kBN;
     for (int g0 = lw; 32 * g0 < npos; g0 += kLoaderWarps * kResolveBatch) {
@@ -284,50 +297,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     named_bar_sync(1, kLoaderWarps * 32);   // rows_s / mask_s complete
-    const uint64_t pol_kv = policy_evict_last();   // the sibling half reads the same rows
-    int issued = 0;
+    // Every row is fetched by the two CTAs of its (t, b) at about the same
+    // time: the first fetch keeps it in L2 for the second.
+    const uint64_t pol_kv = policy_evict_last();
+    // Tiles this thread issued copies for, and of which parts (bit 0: K,
+    // bit 1: V or the FP8 stage).
+    int issued = 0, part = 0;
     if constexpr (kFp8) {
-      if (lw < 3) {
-        // Warps 0, 2, 3 gather: per tile 64 copies of 4 rows each (per row
-        // group: codes 0..255 and 256..511 as plain 256-byte rows into the
-        // raw halves at stage bytes 32 KB and 48 KB, the rope dims 128B-
-        // swizzled into atom 8, the scales into the scale area); this CTA
-        // issues c = crank mod 2, one per thread, announcing its share of
-        // the 41984 bytes that land in each CTA.
-        const int g8 = lane * 3 + lw;
-        for (int it = 0; it < ntiles && g8 < kF8Issuers; ++it) {
+      const bool conv = lw >= 3;                      // warps 8-11 dequantise
+      const int g8 = lane * 3 + lw;
+      if (!conv && g8 < kF8Copies) {
+        // Warps 0, 2, 3 gather, one copy per thread and tile: per row group
+        // g, codes 0..255 and 256..511 as plain 256-byte rows into the raw
+        // halves at stage bytes 32 KB and 48 KB, the rope dims 128B-swizzled
+        // into atom 8, the scales into the scale area.
+        part = 2;
+        for (int it = 0; it < ntiles; ++it) {
           const int st = it & 1;
-          if (it >= 2 && !mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1)) {
+          if (it >= 2 && !mbar_wait(V_EMPTY(st), ((it >> 1) - 1) & 1)) {
             raise_error(kErrTimeout);
             break;
           }
-          if (it == 1 && !(mbar_wait(Q_TMEM, 0) && mbar_wait(Q_PEER, 0))) {
+          if (it == 1 && !mbar_wait(Q_TMEM, 0)) {   // stage 1 held the q staging
             raise_error(kErrTimeout);
             break;
           }
           const uint32_t dst = sbase + kOffStage + st * kStageBytes;
           const int* rows = rows_s + it * kBN;
-          mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(kF8TileBytes / kF8Issuers +
-                                                             (g8 < kF8Rem ? 1 : 0)));
-          const int c = 2 * g8 + static_cast<int>(crank);
-          if (c < 32) {
-            const int g = c >> 1, h = c & 1;
+          if (g8 < 32) {
+            const int g = g8 >> 1, h = g8 & 1;
             const int* r4 = rows + 4 * g;
-            tma_gather4_mc(dst + kRawOff + h * kRawHalfBytes + g * 1024, &tmap_kv, 256 * h, r4[0],
-                           r4[1], r4[2], r4[3], KV_FULL(st), kBoth, pol_kv);
-          } else if (c < 48) {
-            const int* r4 = rows + 4 * (c - 32);
-            tma_gather4_mc(dst + 8 * kAtomBytes + (c - 32) * 512, &tmap_rope, 528, r4[0], r4[1],
-                           r4[2], r4[3], KV_FULL(st), kBoth, pol_kv);
+            mbar_expect_tx(V_FULL(st), 4 * 256);
+            tma_gather4(dst + kRawOff + h * kRawHalfBytes + g * 1024, &tmap_kv, 256 * h, r4[0],
+                        r4[1], r4[2], r4[3], V_FULL(st), pol_kv);
+          } else if (g8 < 48) {
+            const int* r4 = rows + 4 * (g8 - 32);
+            mbar_expect_tx(V_FULL(st), 4 * 128);
+            tma_gather4(dst + 8 * kAtomBytes + (g8 - 32) * 512, &tmap_rope, 528, r4[0], r4[1],
+                        r4[2], r4[3], V_FULL(st), pol_kv);
           } else {
-            const int* r4 = rows + 4 * (c - 48);
+            const int* r4 = rows + 4 * (g8 - 48);
             // (a tensor copy's shared-memory destination is 128-byte aligned)
-            tma_gather4_mc(sbase + kOffSc + st * kScStageBytes + (c - 48) * 128, &tmap_sc, 512, r4[0],
-                           r4[1], r4[2], r4[3], KV_FULL(st), kBoth, pol_kv);
+            mbar_expect_tx(V_FULL(st), 4 * 16);
+            tma_gather4(sbase + kOffSc + st * kScStageBytes + (g8 - 48) * 128, &tmap_sc, 512, r4[0],
+                        r4[1], r4[2], r4[3], V_FULL(st), pol_kv);
           }
           issued = it + 1;
         }
-      } else {
+      } else if (conv) {
         // Warps 8-11 dequantise each landed stage in place: code tiles 0, 1
         // (raw half 0) become bf16 atoms 0-3 (0-32 KB); tiles 2, 3 are read
         // into registers first, because their bf16 atoms 4-7 cover the codes
@@ -339,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int l8 = ctid & 7, qw = ctid >> 3;
         for (int it = 0; it < ntiles; ++it) {
           const int st = it & 1;
-          if (!mbar_wait(KV_FULL(st), (it >> 1) & 1)) {
+          if (!mbar_wait(V_FULL(st), (it >> 1) & 1)) {
             raise_error(kErrTimeout);
             break;
           }
@@ -377,41 +394,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-    for (int it = 0; it < ntiles && gi < kIssuers; ++it) {
-      const int st = it & 1;
-      if (it >= 2 && !mbar_wait(KV_EMPTY(st), ((it >> 1) - 1) & 1)) {
-        raise_error(kErrTimeout);
-        break;
+      // Every thread c = 7 lane + warp issues up to one copy of each part per
+      // tile (c < 80: of the K part, c < 64: of the V part), in the same
+      // order in every lane -- K part free, its copy, V part free, its copy --
+      // so that the warps stay converged (the copy engine serves a warp's
+      // lanes one after another).  Copy c of a part brings rows 4g..4g+3 of
+      // the tile, dims [64a, 64a+64), to atom a at byte 512 g (the copy
+      // engine applies the 128B swizzle).  K: the other half's atoms
+      // a = 4 (1 - half) + c / 16, g = c % 16 (c < 64), else the rope atom 8
+      // with g = c - 64.  V: a = 4 half + c / 16, g = c % 16.
+      const int c = lane * kLoaderWarps + lw;
+      if (c < kKCopies) {
+        part = c < kVCopies ? 3 : 1;
+        const int ka = c < 64 ? 4 * (1 - half) + (c >> 4) : 8;
+        const int kg = c < 64 ? (c & 15) : c - 64;
+        const int va = 4 * half + (c >> 4), vg = c & 15;
+        for (int it = 0; it < ntiles; ++it) {
+          const uint32_t st = it & 1;
+          const uint32_t dst = sbase + kOffStage + st * kStageBytes;
+          if (it >= 2 && !mbar_wait(K_EMPTY(st), ((it >> 1) - 1) & 1)) {
+            raise_error(kErrTimeout);
+            break;
+          }
+          // Stage 1 holds the q dims [0, 256) until the softmax threads
+          // moved them into TMEM.
+          if (it == 1 && !mbar_wait(Q_TMEM, 0)) {
+            raise_error(kErrTimeout);
+            break;
+          }
+          {
+            const int* r4 = rows_s + it * kBN + 4 * kg;
+            mbar_expect_tx(K_FULL(st), 4 * 128);
+            tma_gather4(dst + ka * kAtomBytes + kg * 512, &tmap_kv, 64 * ka, r4[0], r4[1], r4[2],
+                        r4[3], K_FULL(st), pol_kv);
+          }
+          if (it >= 2 && !mbar_wait(V_EMPTY(st), ((it >> 1) - 1) & 1)) {
+            raise_error(kErrTimeout);
+            issued = it + 1;   // this tile's K copy is in flight
+            break;
+          }
+          if (c < kVCopies) {
+            const int* r4 = rows_s + it * kBN + 4 * vg;
+            mbar_expect_tx(V_FULL(st), 4 * 128);
+            tma_gather4(dst + va * kAtomBytes + vg * 512, &tmap_kv, 64 * va, r4[0], r4[1], r4[2],
+                        r4[3], V_FULL(st), pol_kv);
+          }
+          issued = it + 1;
+        }
       }
-      // Stage 1 holds q dims [0, 256) until the softmax threads of both CTAs
-      // moved them (tile 1 lands in both).
-      if (it == 1 && !(mbar_wait(Q_TMEM, 0) && mbar_wait(Q_PEER, 0))) {
-        raise_error(kErrTimeout);
-        break;
-      }
-      // Copy c = 9 g + a brings rows 4g..4g+3 of the tile, dims [64a, 64a+64),
-      // to atom a at byte 512 g of both CTAs (the copy engine applies the 128B
-      // swizzle); this CTA issues the copies c = crank mod 2, one per issuing
-      // thread, each announcing 1/72 of the bytes landing here.
-      const uint32_t dst = sbase + kOffStage + st * kStageBytes;
-      const int* rows = rows_s + it * kBN;
-      mbar_expect_tx(KV_FULL(st), static_cast<uint32_t>(kStageBytes / kIssuers));
-      const int c = 2 * gi + static_cast<int>(crank);
-      const int g = c / kAtoms, a = c - g * kAtoms;
-      const int* r4 = rows + 4 * g;
-      tma_gather4_mc(dst + a * kAtomBytes + g * 512, &tmap_kv, 64 * a, r4[0], r4[1], r4[2], r4[3],
-                     KV_FULL(st), kBoth, pol_kv);
-      issued = it + 1;
     }
+    // No copy may still be in flight when the CTA exits: every issuing thread
+    // waits (with the default bound) for the phases of its last two tiles.
+    // They completed already unless a wait ran out somewhere, and then each
+    // either completes or its bound passes long after the copies landed.
+    for (int u = issued - 1; u >= 0 && u >= issued - 2; --u) {
+      if (part & 1) mbar_wait(K_FULL(u & 1), (u >> 1) & 1);
+      if (part & 2) mbar_wait(V_FULL(u & 1), (u >> 1) & 1);
     }
-    // No copy may still be in flight when the CTA exits: the last phase of
-    // each stage completes only once every byte (both CTAs' copies) landed.
-    // The peer's arrive on Q_PEER is consumed here too.
     if (ltid == 0) {
-      for (int u = issued - 1; u >= 0 && u >= issued - 2; --u) mbar_wait(KV_FULL(u & 1), (u >> 1) & 1);
       mbar_wait(Q_FULL, 0);
       mbar_wait(Q_STAGE, 0);
-      mbar_wait(Q_PEER, 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -420,76 +462,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = make_idesc(1, 1, 0, 0, kBN, 128);
       constexpr uint32_t idesc_pv = make_idesc(1, 1, 0, 1, 256, 128);
       const uint32_t tS = tmem + kColS, tO = tmem + kColO, tP = tmem + kColP, tQ = tmem + kColQ;
+      const uint32_t own_atoms = static_cast<uint32_t>(4 * half * kAtomBytes);
       bool ok = mbar_wait(Q_FULL, 0) && mbar_wait(Q_TMEM, 0);
       // P V of tile i goes out as soon as the softmax wrote P(i), also between
-      // the MMAs of a later tile's Q K^T: it frees the stage that the gather
+      // the MMAs of a later tile's Q K^T: it frees the V part that the gather
       // of tile i + 2 waits for, so the gathers do not queue behind the
       // arrival of the next tile.
       int npv = 0;
       auto pv_ready = [&](int nqk) { return npv < nqk && mbar_test_wait(P_FULL, npv & 1); };
+      // Descriptors are built once; a K-step adds its compile-time byte
+      // offset (>> 4) to the start-address field (addresses stay < 256 KB).
+      const uint64_t dstage0 = smem_desc_sw128(sbase + kOffStage, 16, 1024);
+      const uint64_t dq = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sbase + kOffStage + own_atoms, kAtomBytes, 1024);
       auto issue_pv = [&]() {
         tc_fence_after();
-        const uint32_t stage = sbase + kOffStage + (npv & 1) * kStageBytes + 4 * half * kAtomBytes;
+        const uint64_t dv = dv0 + static_cast<uint64_t>(((npv & 1) * kStageBytes) >> 4);
 #pragma unroll
         for (int j = 0; j < kBN / 16; ++j)
-          mma_f16_ts(tO, tP + 8 * j, smem_desc_sw128(stage + j * 2048, kAtomBytes, 1024), idesc_pv,
+          mma_f16_ts(tO, tP + 8 * j, dv + static_cast<uint64_t>((j * 2048) >> 4), idesc_pv,
                      (npv > 0 || j > 0) ? 1u : 0u);
-        // The stage is reused by tile npv + 2 (if any), whose copies land in
-        // both CTAs: both MMAs must be done with it.
-        if (npv + 2 < ntiles) tc_commit_mc(KV_EMPTY(npv & 1), kBoth);
+        tc_commit(V_EMPTY(npv & 1));
         tc_commit(PV_DONE);
         ++npv;
       };
+// K-step J (compile time) of Q K^T over the stage whose descriptor is DB:
+// dims [16 J, 16 J + 16), q from TMEM (J < 20) or shared memory.
+#define DSA_QK_STEP(J, DB, ACC)                                                               \
+  do {                                                                                       \
+    const uint64_t b_ = (DB) + static_cast<uint64_t>(                                        \
+                                   ((((J) >> 2) * kAtomBytes) + (((J) & 3) * 32)) >> 4);     \
+    if ((J) < kQTmemDims / 16) {                                                             \
+      mma_f16_ts(tS, tQ + 8 * (J), b_, idesc_qk, (ACC));                                     \
+    } else {                                                                                 \
+      const int jq_ = (J) - kQTmemDims / 16;                                                \
+      mma_f16_ss(tS, dq + static_cast<uint64_t>(((jq_ >> 2) * kQAtomBytes + (jq_ & 3) * 32) >> 4), \
+                 b_, idesc_qk, (ACC));                                                       \
+    }                                                                                        \
+  } while (0)
+      // Waits for a phase while issuing P V as soon as it is ready.
+      auto wait_issuing_pv = [&](uint32_t bar, uint32_t parity, int nqk) -> bool {
+        const long long t0 = clock64();
+        while (!mbar_test_wait(bar, parity)) {
+          if (pv_ready(nqk)) issue_pv();
+          if (clock64() - t0 > kWaitCycles) return false;
+        }
+        tc_fence_after();
+        return true;
+      };
       for (int it = 0; it < ntiles && ok; ++it) {
         const int st = it & 1;
-        // Tile it needs its keys and the softmax done reading S(it - 1).
-        const long long t0 = clock64();
-        for (;;) {
-          if (pv_ready(it)) {
-            issue_pv();
-            continue;
-          }
-          if (mbar_test_wait(kFp8 ? KV_CONV_A(st) : KV_FULL(st), (it >> 1) & 1) &&
-              (it == 0 || mbar_test_wait(S_FREE, (it - 1) & 1)))
-            break;
-          if (clock64() - t0 > kWaitCycles) {
-            ok = false;
-            break;
-          }
-        }
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t stage = sbase + kOffStage + st * kStageBytes;
+        const uint32_t ph = (it >> 1) & 1;
+        const uint64_t db = dstage0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+        // Tile it needs the softmax done reading S(it - 1).
+        if (it > 0 && !(ok = wait_issuing_pv(S_FREE, (it - 1) & 1, it))) break;
+        if constexpr (kFp8) {
+          // Dims 0..255 once dequantised, then 256..575.
+          if (!(ok = wait_issuing_pv(KV_CONV_A(st), ph, it))) break;
 #pragma unroll
-        for (int j = 0; j < kQTmemDims / 16; ++j) {
-          if (kFp8 && j == 16) {
-            // FP8: dims 256..575 (atoms 4-7; atom 8 came with the copies)
-            // once the second half of the stage is dequantised.
-            const long long t1 = clock64();
-            while (!mbar_test_wait(KV_CONV(st), (it >> 1) & 1)) {
-              if (pv_ready(it)) issue_pv();
-              if (clock64() - t1 > kWaitCycles) {
-                ok = false;
-                break;
+          for (int j = 0; j < kLatentDim / 16; ++j) {
+            if (j == 16 && !(ok = wait_issuing_pv(KV_CONV(st), ph, it))) break;
+            DSA_QK_STEP(j, db, j > 0 ? 1u : 0u);
+            if ((j & 7) == 7 && pv_ready(it)) issue_pv();
+          }
+        } else {
+          // The K part (K-steps of the other value half's atoms and of the
+          // rope atom), then this CTA's value atoms.
+          if (!(ok = wait_issuing_pv(K_FULL(st), ph, it))) break;
+          if (half == 0) {
+#pragma unroll
+            for (int jj = 0; jj < kLatentDim / 16; ++jj) {
+              if (jj == 20) {
+                tc_commit(K_EMPTY(st));   // freed when the K part's MMAs complete
+                if (!(ok = wait_issuing_pv(V_FULL(st), ph, it))) break;
               }
+              DSA_QK_STEP(jj < 20 ? 16 + jj : jj - 20, db, jj > 0 ? 1u : 0u);
+              if ((jj & 7) == 7 && pv_ready(it)) issue_pv();
             }
-            if (!ok) break;
-            tc_fence_after();
-          }
-          mma_f16_ts(tS, tQ + 8 * j, smem_desc_sw128(stage + (j >> 2) * kAtomBytes + (j & 3) * 32, 16, 1024),
-                     idesc_qk, j > 0 ? 1u : 0u);
-          if ((j & 7) == 7 && pv_ready(it)) issue_pv();
-        }
-        if (!ok) break;
+          } else {
 #pragma unroll
-        for (int j = kQTmemDims / 16; j < kLatentDim / 16; ++j) {
-          const int jq = j - kQTmemDims / 16;
-          mma_f16_ss(tS,
-                     smem_desc_sw128(sbase + kOffQ + (jq >> 2) * kQAtomBytes + (jq & 3) * 32, 16, 1024),
-                     smem_desc_sw128(stage + (j >> 2) * kAtomBytes + (j & 3) * 32, 16, 1024),
-                     idesc_qk, 1u);
-          if ((j & 7) == 7 && pv_ready(it)) issue_pv();
+            for (int jj = 0; jj < kLatentDim / 16; ++jj) {
+              if (jj == 20) {
+                tc_commit(K_EMPTY(st));
+                if (!(ok = wait_issuing_pv(V_FULL(st), ph, it))) break;
+              }
+              DSA_QK_STEP(jj < 16 ? jj : (jj < 20 ? 16 + jj : jj - 4), db, jj > 0 ? 1u : 0u);
+              if ((jj & 7) == 7 && pv_ready(it)) issue_pv();
+            }
+          }
         }
+#undef DSA_QK_STEP
+        if (!ok) break;
         tc_commit(S_FULL);
       }
       while (ok && npv < ntiles) {
@@ -500,8 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_pv();
       }
       if (!ok) raise_error(kErrTimeout);
-      const int pv_issued = npv;
-      if (pv_issued > 0) mbar_wait(PV_DONE, (pv_issued - 1) & 1);
+      // Every MMA issued has completed before TMEM is freed.
+      tc_commit(MMA_DRAIN);
+      mbar_wait(MMA_DRAIN, 0);
     }
     __syncwarp();
   } else {
@@ -559,15 +623,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(Q_TMEM);
-      named_bar_sync(2, kSoftThreads);   // this CTA's softmax threads all read stage 1
-      if (threadIdx.x == 128) mbar_arrive_remote(mapa_shared(Q_PEER, peer));
     }
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);   // [2 parities][2 groups][128 heads]
     const float sc = p.sm_scale * 1.4426950408889634f;  // exp -> exp2
     float mrun = ninf, lrun = 0.f;
     for (int it = 0; it < ntiles; ++it) {
-      const int st = it & 1;
-      if (ok && !(mbar_wait(S_FULL, it & 1) && mbar_wait(KV_FULL(st), (it >> 1) & 1))) ok = false;
+      if (ok && !mbar_wait(S_FULL, it & 1)) ok = false;
       tc_fence_after();
       uint32_t sr[32];
       tmem_ld32(tmem + lanebase + kColS + 32 * sg, sr);
@@ -665,8 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.mid_lse[(static_cast<long long>(t) * H + h) * S + split] =
           (ok && ltot > 0.f) ? (mrun + log2f(ltot)) * 0.6931471805599453f : ninf;
   }
-  // Neither CTA leaves while the other may still signal or copy into it.
-  cluster_sync();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -674,10 +734,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // A selection read without waiting: the grid still completes only after
   // the kernel it depends on (what follows in the stream relies on that).
   if (p.pdl && p.sel_ready && threadIdx.x == 0) grid_dep_wait();
-#undef KV_FULL
-#undef KV_EMPTY
-#undef KV_CONV
+#undef K_FULL
+#undef V_FULL
+#undef K_EMPTY
+#undef V_EMPTY
 #undef KV_CONV_A
+#undef KV_CONV
 }
 
 }  // namespace
@@ -725,7 +787,7 @@ cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * a.num_splits, a.batch * a.nq);
-  return launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0, 2, tq, tkv, to,
+  return launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0, 1, tq, tkv, to,
                        tsc, trope, a);
 }
 

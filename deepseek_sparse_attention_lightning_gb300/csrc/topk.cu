@@ -657,27 +657,14 @@ constexpr size_t kNoAllocScratchBytes = kNoAllocCandOff + size_t(kNoAllocMaxScor
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {nullptr};
-
-// Device address of the scratch array on the current device (looked up once
-// per device; the host-side symbol is not a device address).
+// Device address of the scratch array on the current device.  Looked up on
+// every call (cheap): the host-side symbol is not a device address, and an
+// address cached across calls would go stale if the device's context were
+// reset and the module loaded again.
 void* noalloc_scratch(cudaError_t* err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 64) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* ptr = nullptr;
-    *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    g_noalloc_ptr[dev] = ptr;
-  }
-  return g_noalloc_ptr[dev];
+  void* ptr = nullptr;
+  *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  return *err == cudaSuccess ? ptr : nullptr;
 }
 
 }  // namespace
@@ -686,14 +673,9 @@ void* noalloc_scratch(cudaError_t* err) {
 extern "C" dsa_status dsa_topk_noalloc(const dsa_decode_desc* d, const float* logits,
                                        int64_t ld, int32_t* topk_idx, void* stream) {
   using namespace dsa;
-  if (!d || d->batch < 1 || d->q_per_req < 1 || d->num_heads < 1 || d->topk < 1 ||
-      d->max_pages < 1 || d->num_pages < 1 || !d->seqlens || !d->page_table)
-    return DSA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(d->seqlens) & 3) || (reinterpret_cast<uintptr_t>(d->page_table) & 3))
-    return DSA_ERR_INVALID_ARG;
-  if (d->batch > DSA_MAX_BATCH || d->q_per_req > DSA_MAX_Q_PER_REQ || d->topk > DSA_MAX_TOPK ||
-      d->page_size != DSA_PAGE_SIZE)
-    return DSA_ERR_UNSUPPORTED;
+  // The descriptor checks of dsa_topk, so both entry points answer alike.
+  const int st = check_decode_desc(d);
+  if (st != DSA_OK) return static_cast<dsa_status>(st);
   if (!logits || !topk_idx || (reinterpret_cast<uintptr_t>(logits) & 15) ||
       (reinterpret_cast<uintptr_t>(topk_idx) & 3))
     return DSA_ERR_INVALID_ARG;

@@ -156,8 +156,9 @@ size_t dsa_topk_workspace_bytes(const dsa_decode_desc* desc, int64_t ld_logits);
  *   Limits: T = batch * q_per_req <= 64, T * ld_logits <= 2^21 scores and
  *   ld_logits <= 524288 (as dsa_topk);
  *   larger batches return DSA_ERR_UNSUPPORTED (use dsa_topk with a workspace).
- *   The first call on a device looks up the array's device address (once per
- *   device); make that first call before capturing the stream into a graph.
+ *   Every call looks up the array's device address on the current device
+ *   (the first lookup may load the library's device code); make the first
+ *   call on a device before capturing the stream into a graph.
  *   All calls on a device share the one array: each call clears the parts
  *   that must start at zero, and calls that may run at the same time on the
  *   GPU (different streams, no ordering between them) race on it.
@@ -435,6 +436,19 @@ const char* dsa_status_str(dsa_status status);
  * current device: DSA_OK, DSA_ERR_DEVICE_CHECK or DSA_ERR_TIMEOUT (or
  * DSA_ERR_CUDA if the synchronisation itself failed). */
 dsa_status dsa_get_device_error(void* stream);
+
+/*
+ * Test hook for the timeout path (a library facility; the pages have no
+ * counterpart).  Sets the bound, in SM cycles, on the waits of the indexer
+ * kernel's pipeline (copy engine -> tensor cores -> epilogue) for the
+ * launches that follow; 0 restores the default (about 1.5 s of SM cycles).
+ * With a bound of a few cycles a wait runs out: the kernel records
+ * DSA_ERR_TIMEOUT (read with dsa_get_device_error), stops its pipeline, waits
+ * with the default bound for its copies already in flight, frees its tensor
+ * memory and returns, and the CUDA context stays usable.  Process-wide;
+ * DSA_ERR_INVALID_ARG for a negative value.
+ */
+dsa_status dsa_debug_set_wait_cycles(int64_t cycles);
 
 /* Library version string. */
 const char* dsa_version(void);

@@ -421,6 +421,30 @@ def test_device_check_flags_bad_page_id():
     assert np.isfinite(row[:3 * 64]).all()
 
 
+def test_indexer_wait_timeout_is_reported_and_context_survives():
+    """A wait bound of one SM cycle makes the indexer's pipeline waits run out
+    (the copies they wait for take microseconds): the call must come back,
+    report DSA_ERR_TIMEOUT through dsa_get_device_error, and leave the context
+    usable -- the same call with the default bound then matches the oracle."""
+    wl, g = _gpu_wl("long_varlen", batch=2, q_per_req=1, num_heads=128, topk=2048,
+                    seqlens=[2500, 900], heavy="none", seed=73)
+    assert api.dsa_get_device_error() == 0
+    try:
+        api.dsa_debug_set_wait_cycles(1)
+        api.run_indexer(g)
+        assert api.dsa_get_device_error() == 6           # DSA_ERR_TIMEOUT
+    finally:
+        api.dsa_debug_set_wait_cycles(0)
+    assert api.dsa_get_device_error() == 0               # read-and-clear
+    logits = api.run_indexer(g).cpu().numpy()
+    _assert_no_device_error()
+    a = W.host_arrays(wl)
+    I, E = O.indexer_logits(a["q_fp8"], a["q_scale"], a["w"], a["k_fp8"], a["k_scale"],
+                            a["page_table"], a["seqlens"], a["q_per_req"])
+    for t, n in enumerate(O.visible_lengths(a["seqlens"], a["q_per_req"])):
+        assert (np.abs(logits[t, :n] - I[t, :n]) <= IDX_REL * E[t, :n] + 1e-30).all()
+
+
 # ---------------------------------------------------------------- cache write
 
 def _new_tokens(T, seed):
