@@ -35,6 +35,14 @@ class DecodeDesc(ctypes.Structure):
                 ("num_pages", c_int32), ("seqlens", c_void_p), ("page_table", c_void_p)]
 
 
+class StepRing(ctypes.Structure):
+    """The caller-owned resources of a ring of decode steps (dsa_step_ring)."""
+    _fields_ = [("dev_in", c_void_p * 2), ("out", c_void_p * 2), ("ws", c_void_p),
+                ("ws_bytes", c_size_t), ("copy_in_stream", c_void_p), ("copy_out_stream", c_void_p),
+                ("ev_in", c_void_p * 2), ("ev_done", c_void_p * 2), ("ev_out", c_void_p * 2),
+                ("step", c_int64)]
+
+
 class StepLayout(ctypes.Structure):
     """Byte offsets of a decode step's inputs in one host/device block."""
     _fields_ = [("q_fp8", c_size_t), ("q_scale", c_size_t), ("w", c_size_t), ("q", c_size_t),
@@ -85,6 +93,9 @@ _SIGS = {
     "dsa_decode_step_host": (c_int32, [ctypes.POINTER(DecodeDesc), c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_void_p, c_float, c_int32, c_int32, c_void_p,
                                        c_void_p, c_void_p, c_size_t, c_void_p]),
+    "dsa_decode_step_ring": (c_int32, [ctypes.POINTER(DecodeDesc), ctypes.POINTER(StepRing),
+                                       c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float,
+                                       c_int32, c_int32, c_void_p]),
     "dsa_workspace_bytes": (c_size_t, [ctypes.POINTER(DecodeDesc), c_int32, c_int32]),
     "dsa_num_splits_auto": (c_int32, [ctypes.POINTER(DecodeDesc)]),
     "dsa_status_str": (ctypes.c_char_p, [c_int32]),
@@ -337,22 +348,19 @@ def step_views(block: torch.Tensor, layout: StepLayout, batch, q_per_req, num_he
 class HostStepPipeline:
     """Decode layers whose per-step inputs start in host memory and whose
     outputs end there, with the copies of one step overlapping the layers of
-    its neighbours.
-
-    Two device input blocks (the layout of ``dsa_step_layout_get``) and two
-    device outputs alternate between steps; the host-to-device copies run on
-    one side stream, the device-to-host copies on another, the layers on the
-    caller's stream, ordered by events: step i (buffer i % 2) copies its block
-    in once the layer of step i - 2 is done reading that buffer, its layer
-    waits for that copy and for the output copy of step i - 2, and its output
-    is copied out after its layer.  So while layer i runs, the inputs of step
-    i + 1 come in and the output of step i - 1 goes out.  Every layer is one
-    ``dsa_decode_fused`` call; the caches and the workspace stay in device
-    memory.  A host block may be rewritten once the copy of the step that
-    read it is done (``input_copied(i)``); ``host_out`` of step i is valid
-    once ``output_copied(i)`` (or ``drain``) has been waited on.  Every step
-    of one pipeline runs its layer on the same stream (the steps share one
-    workspace); another stream raises.
+    its neighbours: the resources of a ``dsa_decode_step_ring`` (two device
+    input blocks laid out by ``dsa_step_layout_get``, two device outputs, the
+    workspace, a copy-in and a copy-out stream, six events), and one library
+    call per step.  Step i (slot i % 2) copies its block in once the layer of
+    step i - 2 is done reading that slot, its layer waits for that copy and
+    for the output copy of step i - 2, and its output is copied out after its
+    layer; so while layer i runs, the inputs of step i + 1 come in and the
+    output of step i - 1 goes out.  The caches and the workspace stay in
+    device memory.  A host block may be rewritten once the copy of the step
+    that read it is done (``input_copied(i)``); ``host_out`` of step i is
+    valid once ``output_copied(i)`` (or ``drain``) has been waited on.  Every
+    step of one pipeline runs its layer on the same stream (the steps share
+    one workspace); another stream raises.
     """
 
     def __init__(self, batch, q_per_req, num_heads, topk, max_pages, num_pages, max_seqlen,
@@ -366,63 +374,65 @@ class HostStepPipeline:
         T = batch * q_per_req
         self.out = [torch.empty((T, num_heads, 512), dtype=torch.float32, device=device)
                     for _ in range(2)]
-        self.desc = [make_desc(v["seqlens"], v["page_table"], q_per_req, num_heads, topk, num_pages)
-                     for v in self.views]
-        self.splits = num_splits if num_splits else dsa_num_splits_auto(self.desc[0])
-        self.ws = torch.empty(dsa_workspace_bytes(self.desc[0], max_seqlen, self.splits),
+        self.desc = make_desc(self.views[0]["seqlens"], self.views[0]["page_table"], q_per_req,
+                              num_heads, topk, num_pages)
+        self.splits = num_splits if num_splits else dsa_num_splits_auto(self.desc)
+        self.ws = torch.empty(dsa_workspace_bytes(self.desc, max_seqlen, self.splits),
                               dtype=torch.uint8, device=device)
         self.max_seqlen, self.sm_scale = int(max_seqlen), float(sm_scale)
         self.h2d = torch.cuda.Stream(device)
         self.d2h = torch.cuda.Stream(device)
         mk = lambda: [torch.cuda.Event() for _ in range(2)]
         self.ev_in, self.ev_done, self.ev_out = mk(), mk(), mk()
-        self.steps = 0
-        self._fused = lib().dsa_decode_fused
+        with torch.cuda.device(device):
+            for e in self.ev_in + self.ev_done + self.ev_out:
+                e.record()   # creates the event (torch creates them on first record)
+            torch.cuda.current_stream().synchronize()
+        r = StepRing()
+        for b in range(2):
+            r.dev_in[b] = _ptr(self.dev_in[b], torch.uint8, "dev_in")
+            r.out[b] = _ptr(self.out[b], torch.float32, "out")
+            r.ev_in[b], r.ev_done[b], r.ev_out[b] = (self.ev_in[b].cuda_event,
+                                                     self.ev_done[b].cuda_event,
+                                                     self.ev_out[b].cuda_event)
+        r.ws, r.ws_bytes = _ptr(self.ws, torch.uint8, "ws"), self.ws.numel()
+        r.copy_in_stream, r.copy_out_stream = self.h2d.cuda_stream, self.d2h.cuda_stream
+        r.step = 0
+        self.ring = r
+        self._ring_fn = lib().dsa_decode_step_ring
         self._calls = {}
         self._stream = None
+
+    @property
+    def steps(self) -> int:
+        return int(self.ring.step)
 
     def submit(self, host_in, host_out, k_fp8, k_scale, kv, stream=None):
         """Queues one step: host_in (a pinned uint8 block) -> layer over the
         given caches -> host_out (pinned float32 [T, H, 512])."""
-        if host_in.dtype != torch.uint8 or host_in.is_cuda or host_in.numel() < self.layout.bytes:
-            raise ValueError("host_in: a host uint8 block of at least layout.bytes")
-        if host_out.is_cuda or host_out.dtype != torch.float32 or host_out.shape != self.out[0].shape:
-            raise ValueError("host_out: a host float32 tensor shaped like the output")
         comp = torch.cuda.current_stream() if stream is None else stream
+        sid = _stream(comp)
         if self._stream is None:
-            self._stream = _stream(comp)
-        elif _stream(comp) != self._stream:
+            self._stream = sid
+        elif sid != self._stream:
             raise ValueError("every step of a HostStepPipeline runs on the same stream")
-        b = self.steps % 2
-        if self.steps >= 2:
-            self.h2d.wait_event(self.ev_done[b])
-        with torch.cuda.stream(self.h2d):
-            self.dev_in[b].copy_(host_in[:self.layout.bytes], non_blocking=True)
-        self.ev_in[b].record(self.h2d)
-        comp.wait_event(self.ev_in[b])
-        if self.steps >= 2:
-            comp.wait_event(self.ev_out[b])
-        # The layer call's arguments are checked and packed once per buffer,
-        # cache set and stream; later steps only issue the call.
-        key = (b, k_fp8.data_ptr(), k_scale.data_ptr(), kv.data_ptr(), k_fp8.dtype, k_scale.dtype,
-               kv.dtype, _stream(comp))
+        # The call's arguments are checked and packed once per host buffer
+        # pair, cache set and stream; later steps only issue the call.
+        key = (host_in.data_ptr(), host_out.data_ptr(), k_fp8.data_ptr(), k_scale.data_ptr(),
+               kv.data_ptr(), k_fp8.dtype, k_scale.dtype, kv.dtype, sid)
         args = self._calls.get(key)
         if args is None:
-            v = self.views[b]
-            args = (ctypes.byref(self.desc[b]), _ptr(v["q_fp8"], torch.uint8, "q_fp8"),
-                    _ptr(v["q_scale"], torch.float32, "q_scale"), _ptr(v["w"], torch.float32, "w"),
+            if host_in.dtype != torch.uint8 or host_in.is_cuda or host_in.numel() < self.layout.bytes:
+                raise ValueError("host_in: a host uint8 block of at least layout.bytes")
+            if host_out.is_cuda or host_out.dtype != torch.float32 or host_out.shape != self.out[0].shape:
+                raise ValueError("host_out: a host float32 tensor shaped like the output")
+            args = (ctypes.byref(self.desc), ctypes.byref(self.ring),
+                    _host_ptr(host_in, torch.uint8, "host_in"),
+                    _host_ptr(host_out, torch.float32, "host_out"),
                     _ptr(k_fp8, torch.uint8, "k_fp8"), _ptr(k_scale, torch.float32, "k_scale"),
-                    _u16(v["q"], "q"), _u16(kv, "kv"), None, None, self.sm_scale, self.splits,
-                    self.max_seqlen, _ptr(self.out[b], torch.float32, "out"),
-                    _ptr(self.ws, torch.uint8, "ws"), self.ws.numel(), key[-1])
+                    _u16(kv, "kv"), self.sm_scale, self.splits, self.max_seqlen, sid)
             self._calls[key] = args
-        _check(self._fused(*args), "dsa_decode_fused")
-        self.ev_done[b].record(comp)
-        self.d2h.wait_event(self.ev_done[b])
-        with torch.cuda.stream(self.d2h):
-            host_out.copy_(self.out[b], non_blocking=True)
-        self.ev_out[b].record(self.d2h)
-        self.steps += 1
+        _check(self._ring_fn(*args), "dsa_decode_step_ring")
 
     def input_copied(self, step):
         """Event after which the host block of `step` may be rewritten (valid

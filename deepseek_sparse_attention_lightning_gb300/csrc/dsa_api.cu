@@ -645,6 +645,60 @@ dsa_status dsa_decode_step_host(const dsa_decode_desc* desc, const void* host_in
   return DSA_OK;
 }
 
+dsa_status dsa_decode_step_ring(const dsa_decode_desc* desc, dsa_step_ring* ring,
+                                const void* host_in, float* host_out, const uint8_t* k_fp8,
+                                const float* k_scale, const uint16_t* kv, float sm_scale,
+                                int32_t num_splits, int32_t max_seqlen, void* stream) {
+  if (!desc || !ring || !host_in || !host_out || ring->step < 0) return DSA_ERR_INVALID_ARG;
+  for (int b = 0; b < 2; ++b)
+    if (!ring->dev_in[b] || !aligned(ring->dev_in[b], 256) || !ring->out[b] ||
+        !ring->ev_in[b] || !ring->ev_done[b] || !ring->ev_out[b])
+      return DSA_ERR_INVALID_ARG;
+  dsa_step_layout L;
+  dsa_status st = dsa_step_layout_get(desc->batch, desc->q_per_req, desc->num_heads,
+                                      desc->max_pages, &L);
+  if (st != DSA_OK) return st;
+  const int b = static_cast<int>(ring->step & 1);
+  uint8_t* in = static_cast<uint8_t*>(ring->dev_in[b]);
+  dsa_decode_desc d = *desc;
+  d.seqlens = reinterpret_cast<const int32_t*>(in + L.seqlens);
+  d.page_table = reinterpret_cast<const int32_t*>(in + L.page_table);
+  const uint8_t* q_fp8 = in + L.q_fp8;
+  const float* q_scale = reinterpret_cast<const float*>(in + L.q_scale);
+  const float* w = reinterpret_cast<const float*>(in + L.w);
+  const uint16_t* q = reinterpret_cast<const uint16_t*>(in + L.q);
+  // Both slots are checked before the first call queues anything.
+  for (int s2 = 0; s2 < 2; ++s2) {
+    st = fused_layer(&d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, nullptr, nullptr,
+                     nullptr, sm_scale, num_splits, max_seqlen, ring->out[s2], ring->ws,
+                     ring->ws_bytes, stream, nullptr, /*check_only=*/true);
+    if (st != DSA_OK) return st;
+  }
+  cudaStream_t comp = static_cast<cudaStream_t>(stream);
+  cudaStream_t cin = static_cast<cudaStream_t>(ring->copy_in_stream);
+  cudaStream_t cout = static_cast<cudaStream_t>(ring->copy_out_stream);
+  auto ev = [](void* e) { return static_cast<cudaEvent_t>(e); };
+  const bool again = ring->step >= 2;
+  if (again && cudaStreamWaitEvent(cin, ev(ring->ev_done[b]), 0) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaMemcpyAsync(in, host_in, L.bytes, cudaMemcpyHostToDevice, cin) != cudaSuccess ||
+      cudaEventRecord(ev(ring->ev_in[b]), cin) != cudaSuccess ||
+      cudaStreamWaitEvent(comp, ev(ring->ev_in[b]), 0) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (again && cudaStreamWaitEvent(comp, ev(ring->ev_out[b]), 0) != cudaSuccess) return DSA_ERR_CUDA;
+  st = fused_layer(&d, nullptr, q_fp8, q_scale, w, k_fp8, k_scale, q, kv, nullptr, nullptr,
+                   nullptr, sm_scale, num_splits, max_seqlen, ring->out[b], ring->ws,
+                   ring->ws_bytes, stream, nullptr);
+  if (st != DSA_OK) return st;
+  const size_t ob = static_cast<size_t>(rows_of(&d)) * d.num_heads * DSA_V_DIM * sizeof(float);
+  if (cudaEventRecord(ev(ring->ev_done[b]), comp) != cudaSuccess ||
+      cudaStreamWaitEvent(cout, ev(ring->ev_done[b]), 0) != cudaSuccess ||
+      cudaMemcpyAsync(host_out, ring->out[b], ob, cudaMemcpyDeviceToHost, cout) != cudaSuccess ||
+      cudaEventRecord(ev(ring->ev_out[b]), cout) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  ++ring->step;
+  return DSA_OK;
+}
+
 dsa_status dsa_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
   const int codes[5] = {dsa::fetch_error_indexer(), dsa::fetch_error_topk(), dsa::fetch_error_mla(),

@@ -194,38 +194,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                : "memory");
 }
 
-// 1-D bulk copy from this CTA's shared memory to another CTA of the cluster:
-// `src` is a shared::cta address, `dst` and `bar` are shared::cluster
-// addresses (from mapa) in the destination CTA, whose mbarrier counts the
-// bytes.  Addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
-                                                  uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst), "r"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of
-// 16), completion counted on `bar` in bytes.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// 1-D bulk copy shared -> global (both 16-byte aligned, bytes a multiple of
-// 16), tracked by this thread's bulk async-group.
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                   reinterpret_cast<uint64_t>(dst)),
-               "r"(src), "r"(bytes)
-               : "memory");
-}
-
 // Tiled 4-D TMA store: the box at coordinates (x, y, z, w) of the tensor map
 // is written from shared memory (laid out as the map's swizzle says);
 // elements outside the tensor are not written.

@@ -421,6 +421,55 @@ dsa_status dsa_decode_step_host(const dsa_decode_desc* desc, const void* host_in
                                 float* out, float* host_out, void* ws, size_t ws_bytes,
                                 void* stream);
 
+/*
+ * Decode steps from host buffers with the copies of one step overlapping the
+ * layers of its neighbours (the pages give no host interface; this is the
+ * library's).  Every resource is the caller's: two device input blocks and
+ * two device outputs that alternate between steps, the workspace, a stream
+ * for the host-to-device copies, one for the device-to-host copies, and six
+ * events (cudaEvent_t, e.g. created with cudaEventDisableTiming).  Step i
+ * uses slot b = i % 2:
+ *   1. on copy_in_stream: wait for the layer of step i - 2 (ev_done[b]), copy
+ *      host_in -> dev_in[b] (layout.bytes), record ev_in[b];
+ *   2. on `stream`: wait for ev_in[b] and for the output copy of step i - 2
+ *      (ev_out[b]), run dsa_decode_fused over dev_in[b] into out[b], record
+ *      ev_done[b];
+ *   3. on copy_out_stream: wait for ev_done[b], copy out[b] -> host_out
+ *      (T * H * 512 floats), record ev_out[b].
+ * So while the layer of step i runs, the inputs of step i + 1 come in and
+ * the output of step i - 1 goes out.  host_in may be rewritten once ev_in[b]
+ * has completed; host_out is valid once ev_out[b] has.  `step` is the count
+ * of steps submitted so far (start at 0; the call increments it); every step
+ * of one ring runs its layer on the same `stream` (the steps share one
+ * workspace).
+ */
+typedef struct dsa_step_ring {
+  void* dev_in[2];          /* [dev] layout.bytes each, 256-byte aligned          */
+  float* out[2];            /* [dev] float [T, H, 512] each, 16-byte aligned       */
+  void* ws;                 /* [dev] dsa_workspace_bytes(desc, max_seqlen, splits) */
+  size_t ws_bytes;
+  void* copy_in_stream;     /* cudaStream_t of the host-to-device copies           */
+  void* copy_out_stream;    /* cudaStream_t of the device-to-host copies           */
+  void* ev_in[2];           /* cudaEvent_t: input block b copied in                */
+  void* ev_done[2];         /* cudaEvent_t: the layer of slot b done               */
+  void* ev_out[2];          /* cudaEvent_t: output b copied out                    */
+  int64_t step;             /* steps submitted so far                              */
+} dsa_step_ring;
+
+/*
+ * Queues one step of `ring` as described above.  desc gives the sizes (its
+ * seqlens and page_table fields are ignored: they are taken from dev_in[b]);
+ * host_in [host] is the step's block laid out by dsa_step_layout_get,
+ * host_out [host] float [T, H, 512] (page-locked memory keeps the copies
+ * asynchronous).  Other arguments as in dsa_decode_fused.  Every argument is
+ * checked before anything is queued; DSA_ERR_INVALID_ARG for a null event,
+ * buffer or misaligned block, else the errors of dsa_decode_fused.
+ */
+dsa_status dsa_decode_step_ring(const dsa_decode_desc* desc, dsa_step_ring* ring,
+                                const void* host_in, float* host_out, const uint8_t* k_fp8,
+                                const float* k_scale, const uint16_t* kv, float sm_scale,
+                                int32_t num_splits, int32_t max_seqlen, void* stream);
+
 /* Workspace bytes dsa_decode_fused needs (num_splits 0 = auto). */
 size_t dsa_workspace_bytes(const dsa_decode_desc* desc, int32_t max_seqlen,
                            int32_t num_splits);

@@ -138,6 +138,30 @@ def test_host_step_rejects_bad_arguments_before_any_copy(L):
                                   FAKE, 0.07, 1, 256, FAKE, FAKE, FAKE, n1, None) == 2
 
 
+def test_step_ring_rejects_bad_arguments_before_any_copy(L):
+    d = _fake_desc()
+    r = api.StepRing()
+    for b in range(2):
+        r.dev_in[b], r.out[b] = FAKE + 0x100000 * b, FAKE + 0x200000 + 0x100000 * b
+        r.ev_in[b] = r.ev_done[b] = r.ev_out[b] = 0x1000 + b
+    r.ws, r.ws_bytes, r.step = FAKE, 1 << 40, 0
+    args = lambda: (ctypes.byref(d), ctypes.byref(r), FAKE, FAKE, FAKE, FAKE, FAKE, 0.07, 0, 256,
+                    None)
+    assert L.dsa_decode_step_ring(None, ctypes.byref(r), FAKE, FAKE, FAKE, FAKE, FAKE, 0.07, 0,
+                                  256, None) == 1
+    r.ev_out[1] = None                                    # a missing event
+    assert L.dsa_decode_step_ring(*args()) == 1
+    r.ev_out[1] = 0x1001
+    r.dev_in[0] = FAKE + 16                               # block not 256-byte aligned
+    assert L.dsa_decode_step_ring(*args()) == 1
+    r.dev_in[0] = FAKE
+    assert L.dsa_decode_step_ring(ctypes.byref(_fake_desc(num_heads=100)), ctypes.byref(r), FAKE,
+                                  FAKE, FAKE, FAKE, FAKE, 0.07, 0, 256, None) == 2
+    r.ws_bytes = 16                                       # workspace too small
+    assert L.dsa_decode_step_ring(*args()) == 3
+    assert r.step == 0                                    # nothing was queued
+
+
 def test_mli_validation(L):
     d = ctypes.byref(_fake_desc())
     n1 = L.dsa_workspace_bytes(d, 256, 0)
