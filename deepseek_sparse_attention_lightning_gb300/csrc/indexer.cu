@@ -14,7 +14,8 @@
 // key scale with no cross-thread reduction, writes the fp32 logit and counts it
 // in a shared-memory histogram of the top 11 key bits (the first top-k pass).
 //
-// Warp roles (one persistent CTA per SM; 512 threads at n_q = 1, else 384):
+// Warp roles (one persistent CTA per SM; 512 threads at n_q = 1, 640 at
+// n_q = 2, else 384):
 //   warp 0   TMA producer: one 8 KB box per page into a ring of 5-12 stages
 //            (as many as shared memory holds next to the fixed buffers),
 //            issued by 8 lanes for 4 tiles at a time, and the request's FP8
@@ -23,15 +24,15 @@
 //            ~100-170 cycles.
 //   warps 1, 2  MMA issuers (one thread each, alternate tiles); warp 1 owns
 //            TMEM;
-//   warps 4-7, 8-11 (and 12-15 at n_q = 1)  epilogue groups taking tiles in
+//   warps 4-7, 8-11 (and 12-15 at n_q = 1, 12-19 at n_q = 2)  epilogue groups taking tiles in
 //            turn (one thread per TMEM lane / token); each thread loads its
 //            token's key scale three of its tiles ahead.  With two groups at
 //            n_q = 1 the epilogue set the pace: the MMA issuers waited for
 //            free accumulators and the producer for free stages a quarter of
 //            the time; a third group takes that wait off.
-// Accumulators: six TMEM buffers at n_q = 1, four when they fit (n_q = 2),
-// else two, so the MMAs of a tile do not wait for the epilogue of the tile
-// a few before it.
+// Accumulators: six TMEM buffers at n_q = 1, four at n_q = 2 (one per
+// epilogue group), else two, so the MMAs of a tile do not wait for the
+// epilogue of the tile a few before it.
 // The page ids of the CTA's tile range are fetched once, by all threads, into
 // shared memory.  Keys are streamed exactly once per request; every query
 // token of the request is served by the same key tile (N = 64 * n_q).
@@ -60,11 +61,14 @@ struct Cfg {
   static constexpr int kN = 64 * NQ;
   static constexpr int kQBytes = kN * kIndexDim;
   // Epilogue groups (four warps each, group gi takes the tiles it = gi mod
-  // kEpiGroups): three at n_q = 1, where the epilogue sets the streaming pace
-  // with two, else two.  Every accumulator buffer must be used by one group
-  // and one MMA issuer only (the tiles it = ab mod kAccBufs), so kAccBufs is
-  // a multiple of both: six buffers of 64 columns at n_q = 1.
-  static constexpr int kEpiGroups = NQ == 1 ? 3 : 2;
+  // kEpiGroups): three at n_q = 1 and four at n_q = 2, where the epilogue
+  // sets the streaming pace with two, else two.  Every accumulator buffer
+  // must be used by one group and one MMA issuer only (the tiles it = ab mod
+  // kAccBufs), so kAccBufs is a multiple of both: six buffers of 64 columns
+  // at n_q = 1, four of 128 at n_q = 2.  At n_q = 2 the block has 640
+  // threads (at most 96 registers each), so the epilogue loads a query
+  // token's 64 columns in two halves of 32.
+  static constexpr int kEpiGroups = NQ == 1 ? 3 : (NQ == 2 ? 4 : 2);
   static constexpr int kThreads = 32 * (kEpiWarp0 + 4 * kEpiGroups);
   // Everything but the key ring; the ring then takes what shared memory is
   // left (up to 14 stages): the ring's bytes in flight set the bandwidth.
@@ -470,21 +474,41 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + ab * C::kN;
 #pragma unroll 1
         for (int i = 0; i < NQ; ++i) {
-          uint32_t acc[64];
-          tmem_ld64(tl + i * 64, acc);
-          if (i == NQ - 1) {
-            tc_fence_before();
-            mbar_arrive(ACC_EMPTY(ab));
-          }
           const float4* w4 = reinterpret_cast<const float4*>(gw + i * kIndexHeads);
           float s0 = 0.f, s1 = 0.f;
+          if constexpr (NQ == 2) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const float4 ww = w4[jj];
-            s0 = fmaf(ww.x, fmaxf(__uint_as_float(acc[4 * jj + 0]), 0.f), s0);
-            s1 = fmaf(ww.y, fmaxf(__uint_as_float(acc[4 * jj + 1]), 0.f), s1);
-            s0 = fmaf(ww.z, fmaxf(__uint_as_float(acc[4 * jj + 2]), 0.f), s0);
-            s1 = fmaf(ww.w, fmaxf(__uint_as_float(acc[4 * jj + 3]), 0.f), s1);
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t acc[32];
+              tmem_ld32(tl + i * 64 + hf * 32, acc);
+              if (i == NQ - 1 && hf == 1) {
+                tc_fence_before();
+                mbar_arrive(ACC_EMPTY(ab));
+              }
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const float4 ww = w4[8 * hf + jj];
+                s0 = fmaf(ww.x, fmaxf(__uint_as_float(acc[4 * jj + 0]), 0.f), s0);
+                s1 = fmaf(ww.y, fmaxf(__uint_as_float(acc[4 * jj + 1]), 0.f), s1);
+                s0 = fmaf(ww.z, fmaxf(__uint_as_float(acc[4 * jj + 2]), 0.f), s0);
+                s1 = fmaf(ww.w, fmaxf(__uint_as_float(acc[4 * jj + 3]), 0.f), s1);
+              }
+            }
+          } else {
+            uint32_t acc[64];
+            tmem_ld64(tl + i * 64, acc);
+            if (i == NQ - 1) {
+              tc_fence_before();
+              mbar_arrive(ACC_EMPTY(ab));
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const float4 ww = w4[jj];
+              s0 = fmaf(ww.x, fmaxf(__uint_as_float(acc[4 * jj + 0]), 0.f), s0);
+              s1 = fmaf(ww.y, fmaxf(__uint_as_float(acc[4 * jj + 1]), 0.f), s1);
+              s0 = fmaf(ww.z, fmaxf(__uint_as_float(acc[4 * jj + 2]), 0.f), s0);
+              s1 = fmaf(ww.w, fmaxf(__uint_as_float(acc[4 * jj + 3]), 0.f), s1);
+            }
           }
           if (s < p.ld) {
             const int vis = S - (NQ - 1 - i);
