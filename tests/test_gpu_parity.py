@@ -407,6 +407,47 @@ def test_mli_layer_matches_separate_calls(nq, splits):
     _assert_close_att(out.cpu().numpy(), o2, "MLI layer output on layer-1 selection")
 
 
+# ---------------------------------------------------------------- context parallel
+
+def test_context_parallel_emulated_matches_fused_layer():
+    """Three ranks, each holding a page-aligned slice of every request (its
+    caches seen through the slice's page table), emulated one after another:
+    local scores and top-k, the global top-k over the ranks' candidates, the
+    attention over each rank's own winners, the merge of the three partials.
+    Scores of a token do not depend on the slice it is scored in, so the
+    selection equals the fused layer's bit for bit; the output matches it
+    and the oracle within the attention tolerance."""
+    from deepseek_sparse_attention_lightning_gb300 import cp
+    wl, g = _gpu_wl("long_varlen", batch=2, q_per_req=1, num_heads=128, topk=2048,
+                    seqlens=[9000, 5200], heavy="runs:0.005:8", seed=81)
+    spec, lc = wl.spec, g.layers[0]
+    T, k, H, R = spec.num_tokens, spec.topk, spec.num_heads, 3
+    want_sel = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    want = api.run_decode(g, topk_out=want_sel)
+    seqlens = g.seqlens.cpu().tolist()
+    bounds = [cp.slice_bounds(int(S), R) for S in seqlens]
+    steps, slices = [], []
+    for r in range(R):
+        mine = [(b[r], b[r + 1]) for b in bounds]
+        npg = [(hi - lo + 63) // 64 for lo, hi in mine]
+        table = torch.full((len(mine), max(npg)), -1, dtype=torch.int32, device="cuda")
+        for i, (lo, _) in enumerate(mine):
+            table[i, :npg[i]] = g.page_table[i, lo // 64: lo // 64 + npg[i]]
+        seq = torch.tensor([hi - lo for lo, hi in mine], dtype=torch.int32, device="cuda")
+        steps.append(cp.DeviceSteps(g.q_fp8, g.q_scale, g.w, lc.q, lc.k_fp8, lc.k_scale, lc.kv, seq,
+                                    table, g.num_pages, k, H, spec.sm_scale))
+        slices.append(cp.RankSlice(start=[lo for lo, _ in mine], length=[hi - lo for lo, hi in mine]))
+    out, sel = cp.run_emulated(steps, slices)
+    torch.cuda.synchronize()
+    _assert_no_device_error()
+    assert torch.equal(sel, want_sel)
+    _assert_close_att(out.cpu().numpy(), want.cpu().numpy(), "context parallel vs fused layer")
+    a = W.host_arrays(wl)
+    o, _ = O.sparse_mla(a["q"], a["kv"], sel.cpu().numpy(), a["page_table"], a["seqlens"], 1,
+                        a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "context parallel vs oracle")
+
+
 # ---------------------------------------------------------------- errors
 
 def test_device_check_flags_bad_page_id():
