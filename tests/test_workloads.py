@@ -75,3 +75,25 @@ def test_fp8_scales_and_second_layer_keys():
     d = (k2 - k1).flatten()
     assert 0.15 < float(d.std()) < 0.25
     assert float(torch.corrcoef(torch.stack([k1.flatten(), k2.flatten()]))[0, 1]) > 0.95
+
+
+def test_mtp_queries_share_few_selections():
+    """The two query tokens of an mtp_32k request draw independent index
+    queries, so their selections overlap little (the heavy tokens and
+    chance): the oracle's selections of four requests share < 10 % of their
+    positions, i.e. a gather of the union would read > 90 % of 2k rows."""
+    import numpy as np
+    import oracle as O
+    from deepseek_sparse_attention_lightning_gb300 import workloads as W
+    a = W.host_arrays(W.make_workload("mtp_32k"))
+    nq, k = a["q_per_req"], a["topk"]
+    shared = []
+    for r in range(4):
+        sl = slice(r * nq, (r + 1) * nq)
+        I, _ = O.indexer_logits(a["q_fp8"][sl], a["q_scale"][sl], a["w"][sl], a["k_fp8"],
+                                a["k_scale"], a["page_table"][r:r + 1], a["seqlens"][r:r + 1], nq,
+                                with_bound=False)
+        sel = O.topk(I.astype(np.float32), O.visible_lengths(a["seqlens"][r:r + 1], nq), k)
+        assert (sel >= 0).sum(axis=1).tolist() == [k, k]
+        shared.append(len(set(sel[0].tolist()) & set(sel[1].tolist())))
+    assert 0 < np.mean(shared) < 0.1 * k
