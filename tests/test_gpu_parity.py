@@ -486,6 +486,118 @@ def test_indexer_wait_timeout_is_reported_and_context_survives():
         assert (np.abs(logits[t, :n] - I[t, :n]) <= IDX_REL * E[t, :n] + 1e-30).all()
 
 
+def test_fused_layer_wait_timeout_is_reported_and_context_survives():
+    """The fused layer with the indexer's waits bounded by one SM cycle: the
+    call comes back with DSA_ERR_TIMEOUT, and the next call with the default
+    bound selects exactly and attends correctly (the context stays usable)."""
+    wl, g = _gpu_wl("long_varlen", batch=2, q_per_req=1, num_heads=32, topk=2048,
+                    seqlens=[9000, 5000], heavy="none", seed=74)
+    T, k = wl.spec.num_tokens, wl.spec.topk
+    assert api.dsa_get_device_error() == 0
+    try:
+        api.dsa_debug_set_wait_cycles(1)
+        api.run_decode(g)
+        assert api.dsa_get_device_error() == 6           # DSA_ERR_TIMEOUT
+    finally:
+        api.dsa_debug_set_wait_cycles(0)
+    sel = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    out = api.run_decode(g, topk_out=sel)
+    logits = api.run_indexer(g)
+    _assert_no_device_error()
+    a = W.host_arrays(wl)
+    vis = O.visible_lengths(a["seqlens"], 1)
+    sel_np = sel.cpu().numpy()
+    assert np.array_equal(sel_np, O.topk(logits.cpu().numpy(), vis, k))
+    o, _ = O.sparse_mla(a["q"], a["kv"], sel_np, a["page_table"], a["seqlens"], 1, a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "O after a timed-out call")
+
+
+# ---------------------------------------------------------------- fused selection
+
+# The fused layer's selection (the indexer's histogram, then the top-k) must
+# be the top-k of the same scores bit for bit, across query counts, k, row
+# lengths and batch sizes.
+SEL_CASES = [
+    # n_q = 3: rows at, just above and far above k, several requests
+    dict(base="mtp_32k", batch=4, q_per_req=3, num_heads=16, topk=2048,
+         seqlens=[2049, 7000, 2050, 15000], heavy="frac:0.01", seed=81),
+    # n_q = 4
+    dict(base="mtp_32k", batch=3, q_per_req=4, num_heads=32, topk=2048,
+         seqlens=[9000, 2051, 4100], heavy="frac:0.01", seed=82),
+    # n_q = 2: a row far longer than the rest (170000 scores: a cluster of 6 x 32768)
+    dict(base="mtp_32k", batch=2, q_per_req=2, num_heads=16, topk=2048,
+         seqlens=[170000, 3000], heavy="frac:0.01", seed=83),
+    # another k, rows shorter than k next to a longer one
+    dict(base="long_varlen", batch=3, q_per_req=1, num_heads=16, topk=100,
+         seqlens=[5000, 90, 333], heavy="runs:0.005:8", seed=84),
+    # many requests: most indexer CTAs score tiles of two of them
+    dict(base="long_varlen", batch=40, q_per_req=1, num_heads=16, topk=2048,
+         seqlens=(2000, 12000), heavy="runs:0.005:8", seed=86),
+]
+
+
+def _check_fused_selection(wl, g):
+    T, k = wl.spec.num_tokens, wl.spec.topk
+    sel = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    out = api.run_decode(g, topk_out=sel)
+    logits = api.run_indexer(g)
+    torch.cuda.synchronize()
+    _assert_no_device_error()
+    a = W.host_arrays(wl)
+    vis = O.visible_lengths(a["seqlens"], a["q_per_req"])
+    sel_np = sel.cpu().numpy()
+    want = O.topk(logits.cpu().numpy(), vis, k)
+    bad = [t for t in range(T) if not np.array_equal(sel_np[t], want[t])]
+    assert not bad, f"rows {bad[:8]} differ from the top-k of the kernel's scores"
+    o, _ = O.sparse_mla(a["q"], a["kv"], sel_np, a["page_table"], a["seqlens"], a["q_per_req"],
+                        a["sm_scale"])
+    _assert_close_att(out.cpu().numpy(), o, "O")
+    return sel_np, logits
+
+
+@pytest.mark.parametrize("case", SEL_CASES,
+                         ids=["nq3", "nq4", "nq2-long-row", "k100", "b40"])
+def test_fused_selection_matches_topk_of_the_scores(case):
+    case = dict(case)
+    base, seqlens = case.pop("base"), case.pop("seqlens")
+    if isinstance(seqlens, tuple):
+        rng = np.random.default_rng(case["seed"])
+        seqlens = rng.integers(seqlens[0], seqlens[1] + 1, size=case["batch"]).tolist()
+    wl, g = _gpu_wl(base, seqlens=seqlens, **case)
+    _check_fused_selection(wl, g)
+
+
+@pytest.mark.parametrize("nq", [1, 2])
+def test_fused_selection_breaks_exact_ties_by_position(nq):
+    """Index keys of zeros score exactly 0: with all but a few hundred keys
+    zeroed, the k-th score is 0 and the selection must take the lowest
+    positions among tens of thousands of equal scores (the top-k's tie
+    resolution over positions, with candidate lists far beyond its shared
+    memory); the last request's keys are all zero (every score ties)."""
+    wl = W.make_workload(W.small_spec("long_varlen", batch=3, q_per_req=nq, num_heads=16,
+                                      topk=2048, heavy="none", seed=85 + nq),
+                         seqlens=[30000, 12000, 5000])
+    rows = wl.k_fp8.shape[0]
+    keep = torch.zeros(rows, dtype=torch.bool)
+    keep[torch.from_numpy(np.random.default_rng(nq).choice(rows, 400, replace=False))] = True
+    pt = wl.page_table[2]
+    last = pt[pt >= 0].long()
+    for pg in last.tolist():
+        keep[pg * 64:(pg + 1) * 64] = False
+    wl.layers[0].k_fp8[~keep] = 0
+    g = wl.to("cuda")
+    sel_np, logits = _check_fused_selection(wl, g)
+    lg = logits.cpu().numpy()
+    T = wl.spec.num_tokens
+    vis = O.visible_lengths(wl.seqlens.numpy().astype(np.int64), nq)
+    for t in range(T):
+        kth = np.sort(lg[t, :vis[t]])[::-1][2047]
+        assert kth == 0.0, "the threshold must lie among the zero scores"
+    # the all-zero request selects its first k positions
+    for t in range((T // 3) * 2, T):
+        assert np.array_equal(sel_np[t], np.arange(2048))
+
+
 # ---------------------------------------------------------------- cache write
 
 def _new_tokens(T, seed):
