@@ -82,6 +82,7 @@ constexpr int kQAtomBytes = 128 * 128;                   // 128 heads x 64 dims 
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kOffQ + kQSmemAtoms * kQAtomBytes;
 constexpr int kMaxPos = 2048;                            // positions of one split (<= k)
+constexpr int kMaxRank = 512;                            // rows ranked by length (else index order)
 constexpr int kOffRows = kOffStage + 2 * kStageBytes;    // cache row of every position
 constexpr int kOffMask = kOffRows + kMaxPos * 4;         // validity bits, 32 per word
 constexpr int kOffXchg = kOffMask + (kMaxPos / 32) * 4;    // softmax groups' exchange, 2 KB
@@ -147,7 +148,7 @@ __device__ __forceinline__ void dequant_chunk(uint8_t* stage, int a, int j, int 
 // bytes with plain 256-byte boxes (codes), tmap_rope with 128B-swizzled
 // 128-byte boxes (the rope dims) and tmap_sc with 16-byte boxes (the
 // scales).  Otherwise tmap_kv maps the bf16 cache and the others are unused.
-template <bool kFp8>
+template <bool kFp8, bool kRank>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_kv,
@@ -155,9 +156,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmap_sc,
                       const __grid_constant__ CUtensorMap tmap_rope, const MlaLaunch p) {
   extern __shared__ uint8_t smem_raw[];
-  const int split = blockIdx.x >> 1, half = blockIdx.x & 1, t = blockIdx.y;
+  const int split = blockIdx.x >> 1, half = blockIdx.x & 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.heads, S = p.num_splits, k = p.k;
+  // The query row.  With kRank (a grid of more CTAs than the GPU has SMs),
+  // blockIdx.y is the row's rank in the order of selected counts
+  // min(vis, k), longest first (equal counts: lower row first): the
+  // scheduler hands out CTAs in index order, so rows of different lengths
+  // are taken longest first and the SMs end close together.  (Up to
+  // kMaxRank rows; the counts go through the row-index area, unused until
+  // the loaders fill it.)
+  int t = blockIdx.y;
+  if constexpr (kRank) {
+    __shared__ int s_row;
+    const int T = p.batch * p.nq;
+    if (T > 1 && T <= kMaxRank) {
+      int* cnt = reinterpret_cast<int*>(align1024(smem_raw) + kOffRows);
+      for (int i = threadIdx.x; i < T; i += kThreads) {
+        const int v = p.seqlens[i / p.nq] - (p.nq - 1 - i % p.nq);
+        cnt[i] = v <= 0 ? 0 : (v < k ? v : k);
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < T; i += kThreads) {
+        const int ci = cnt[i];
+        int rank = 0;
+        for (int j = 0; j < T; ++j) {
+          const int cj = cnt[j];
+          rank += (cj > ci || (cj == ci && j < i)) ? 1 : 0;
+        }
+        if (rank == static_cast<int>(blockIdx.y)) s_row = i;
+      }
+      __syncthreads();
+      t = s_row;
+    }
+  }
   const int r = t / p.nq, qi = t % p.nq;
   const int vis = p.seqlens[r] - (p.nq - 1 - qi);
   const int n = vis <= 0 ? 0 : (vis < k ? vis : k);
@@ -783,10 +815,13 @@ cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
                         CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  auto kern = fp8 ? sparse_mla_kernel<true> : sparse_mla_kernel<false>;
+  dim3 grid(2 * a.num_splits, a.batch * a.nq);
+  // Rows are taken longest first only when the CTAs come in several waves.
+  const bool rank = static_cast<long long>(grid.x) * grid.y > device_sm_count();
+  auto kern = fp8 ? (rank ? sparse_mla_kernel<true, true> : sparse_mla_kernel<true, false>)
+                  : (rank ? sparse_mla_kernel<false, true> : sparse_mla_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(2 * a.num_splits, a.batch * a.nq);
   return launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, stream, a.pdl != 0, 1, tq, tkv, to,
                        tsc, trope, a);
 }

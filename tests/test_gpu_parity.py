@@ -207,6 +207,29 @@ def test_sparse_mla_split_and_merge_match_oracle(case, splits):
     _assert_close_att(lse.cpu().numpy(), l, "LSE")
 
 
+def test_sparse_mla_rows_of_mixed_lengths_in_a_multi_wave_grid():
+    """160 rows of 1 to 2048 selected keys, one split: 320 CTAs, more than
+    the GPU has SMs, so the CTAs take the rows longest first (the kernel
+    ranks them by their selected count).  Every row's Mid_O / LSE must still
+    land in its own place: element-wise against the oracle."""
+    B = 160
+    rng = np.random.default_rng(46)
+    lens = rng.integers(1, 2049, size=B)
+    lens[:3] = [1, 2048, 64]                              # the extremes and one full tile
+    wl, g = _gpu_wl("short_dense", batch=B, q_per_req=1, num_heads=16, topk=2048,
+                    seqlens=lens.tolist(), heavy="none", seed=47)
+    a = W.host_arrays(wl)
+    idx = np.full((B, 2048), -1, dtype=np.int64)
+    for t, n in enumerate(lens):
+        idx[t, :n] = np.arange(n)
+    mid_o, mid_lse = api.run_sparse_mla_split(g, torch.from_numpy(idx.astype(np.int32)).cuda(), 1)
+    _assert_no_device_error()
+    mo, ml = O.sparse_mla_split(a["q"], a["kv"], idx, a["page_table"], a["seqlens"], 1,
+                                a["sm_scale"], 1)
+    _assert_close_att(mid_o.cpu().numpy(), mo, "Mid_O")
+    _assert_close_att(mid_lse.cpu().numpy(), ml, "Mid_LSE")
+
+
 def test_sparse_mla_skips_padding_and_many_empty_splits():
     wl, g = _gpu_wl("long_varlen", batch=2, q_per_req=1, num_heads=128, topk=2048,
                     seqlens=[100, 70], heavy="none", seed=45)
