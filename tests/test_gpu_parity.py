@@ -818,6 +818,39 @@ def _sampled_checks(wl, g, sel, out, logits, rows_to_check, n_pos=4096):
         _assert_close_att(out[t].cpu().numpy(), o, f"row {t}")
 
 
+def test_mli_layer_workload_sized():
+    """dsa_decode_mli on the full mli_195k workload (4 requests of 196608
+    tokens, two layers): layer 2's own selection equals the fused layer's on
+    layer 2 bit for bit (rows of 196608 scores, selected beside the
+    attention), and its output at sampled rows is the oracle's attention of
+    layer 2's queries over layer 1's selection."""
+    wl = W.make_workload("mli_195k", device="cuda")
+    T, k, H = wl.spec.num_tokens, wl.spec.topk, wl.spec.num_heads
+    desc = api.workload_desc(wl)
+    sel1 = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    api.run_decode(wl, layer=0, topk_out=sel1)
+    sel2_ref = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    api.run_decode(wl, layer=1, topk_out=sel2_ref)
+    lc2 = wl.layers[1]
+    sel2 = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    out = torch.full((T, H, 512), float("nan"), device="cuda")
+    api.dsa_decode_mli(desc, wl.q_fp8, wl.q_scale, wl.w, lc2.k_fp8, lc2.k_scale, lc2.q, lc2.kv,
+                       sel1, sel2, out, api.alloc_workspace(wl, 0), wl.max_seqlen,
+                       wl.spec.sm_scale, 0)
+    torch.cuda.synchronize()
+    _assert_no_device_error()
+    assert torch.equal(sel2, sel2_ref)
+    table = wl.page_table.cpu().numpy()
+    s1 = sel1.cpu().numpy()
+    for t in sorted({0, T - 1}):
+        chosen = s1[t][s1[t] >= 0]
+        lat = lc2.kv[torch.from_numpy(O.physical_rows(table[t], chosen)).cuda()]
+        o, _ = O.attend(W.bf16_bits(lc2.q[t]), W.bf16_bits(lat), wl.spec.sm_scale)
+        _assert_close_att(out[t].cpu().numpy(), o, f"row {t}")
+    del wl
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("name", ["long_128k", "mtp_32k", "short_dense", "tiny_4k", "long_varlen",
                                   "mli_195k"])
 def test_workload_sized_sampled(name):
@@ -886,8 +919,7 @@ def test_sparse_mla_fp8_split_and_merge_match_oracle(case, splits):
     _assert_close_att(lse.cpu().numpy(), l, "LSE")
 
 
-@pytest.mark.parametrize("case", [c for c in FUSED_CASES if c["base"] != "short_dense"],
-                         ids=lambda c: c["base"])
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: c["base"])
 def test_fused_layer_fp8_latent(case):
     """The layer over the FP8 latent cache: the same selection as the bf16
     layer (the indexer and top-k do not read the latent cache), and the
@@ -914,7 +946,7 @@ def test_fused_layer_fp8_latent(case):
     _assert_close_att(out.cpu().numpy(), o, "O")
 
 
-@pytest.mark.parametrize("name", ["long_128k", "mtp_32k"])
+@pytest.mark.parametrize("name", ["long_128k", "mtp_32k", "short_dense"])
 def test_fused_layer_fp8_latent_workload_sized(name):
     wl = W.make_workload(name, device="cuda")
     T, k, H = wl.spec.num_tokens, wl.spec.topk, wl.spec.num_heads
