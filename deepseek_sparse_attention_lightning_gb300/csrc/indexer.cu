@@ -74,7 +74,8 @@ struct Cfg {
   // left (up to 14 stages): the ring's bytes in flight set the bandwidth.
   static constexpr int kHistBytes = kEpiGroups * NQ * kHistBins * 2;   // 16-bit bins
   static constexpr int kFixed = 2 * kQBytes + kHistBytes + kEpiGroups * kN * 4 + kPageWin * 4 +
-                                (1024 + 4) * 4 + 64 * 4 + (2 * 14 + 4 + 2 * 6 + 1) * 8 + 16 + 1024;
+                                (1024 + 4) * 4 + 1024 * 4 + 64 * 4 + (2 * 14 + 4 + 2 * 6 + 1) * 8 + 16 +
+                                1024;
   static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesFit > 14 ? 14 : kStagesFit;
   // Accumulator buffers: four when they fit in TMEM, so the MMA of a tile
@@ -89,7 +90,8 @@ struct Cfg {
   static constexpr int kOffW = kOffHist + kHistBytes;
   static constexpr int kOffPages = kOffW + kEpiGroups * kN * 4;
   static constexpr int kOffPrefix = kOffPages + kPageWin * 4;
-  static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 4) * 4;
+  static constexpr int kOffSeq = kOffPrefix + (kMaxBatch + 4) * 4;
+  static constexpr int kOffScratch = kOffSeq + kMaxBatch * 4;
   static constexpr int kOffBar = kOffScratch + 64 * 4;
   static constexpr int kNumBars = 2 * kStages + 4 + 2 * kAccBufs + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -143,9 +145,9 @@ __device__ __forceinline__ int find_request(const int* prefix, int B, int g) {
 // Page id of page `which` (0/1) of flattened tile g, or -1 if it lies outside
 // the cache.  The tile's second page, past the request's last page, repeats
 // the first.
-__device__ __forceinline__ int tile_page(const IndexerLaunch& p, const int* prefix, int r, int g,
-                                         int which) {
-  const int S = p.seqlens[r];
+__device__ __forceinline__ int tile_page(const IndexerLaunch& p, const int* prefix, const int* seq,
+                                         int r, int g, int which) {
+  const int S = seq[r];
   const int npg = (S + kPage - 1) / kPage;
   int lp = 2 * (g - prefix[r]) + which;
   if (lp >= npg) lp = lp - 1;
@@ -162,6 +164,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sbase = smem_u32(smem);
   int* prefix = reinterpret_cast<int*>(smem + C::kOffPrefix);
+  int* seq_s = reinterpret_cast<int*>(smem + C::kOffSeq);   // every request's length
   int* scratch = reinterpret_cast<int*>(smem + C::kOffScratch);
   uint32_t* shist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
   float* wbuf = reinterpret_cast<float*>(smem + C::kOffW);
@@ -193,6 +196,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
       int c = 0;
       if (r < B) {
         const int S = p.seqlens[r];
+        seq_s[r] = S;
         if (S > 0 && !(p.skip_short && S <= p.topk)) c = (S + kTile - 1) / kTile;
       }
       cnt[e] = c;
@@ -246,14 +250,14 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
     const int n = min(2 * (g1 - g0), kPageWin);
     for (int i = threadIdx.x - 32; i < n; i += C::kThreads - 32) {
       const int g = g0 + (i >> 1);
-      pages[i] = tile_page(p, prefix, find_request(prefix, B, g), g, i & 1);
+      pages[i] = tile_page(p, prefix, seq_s, find_request(prefix, B, g), g, i & 1);
     }
     named_bar_sync(5, C::kThreads - 32);
     if (threadIdx.x == 32) mbar_arrive(PAGES);
   }
   auto page_of = [&](int r, int g, int which) -> int {
     const int i = 2 * (g - g0) + which;
-    return i < kPageWin ? pages[i] : tile_page(p, prefix, r, g, which);
+    return i < kPageWin ? pages[i] : tile_page(p, prefix, seq_s, r, g, which);
   };
 
   if (warp == 0) {
@@ -272,6 +276,26 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
       int done = 0;                    // tiles whose copies were all issued
       bool ok = true;
       for (int it0 = 0; it0 < ntl; it0 += kGroup) {
+        // This lane's tile and its page id first: the first group's page-table
+        // reads are then in flight while lane 0 issues the query copy.
+        const int it = it0 + (lane >> 1);
+        const int which = lane & 1;
+        const bool act = lane < 2 * kGroup && it < ntl;
+        int pg = -1;
+        if (act) {
+          const int g = g0 + it;
+          while (prefix[rl + 1] <= g) ++rl;
+          if (it0 == 0) {
+            // tile_page's lookup, its range check deferred to the copy below
+            // so that nothing waits for the load before the query copy.
+            const int npg = (seq_s[rl] + kPage - 1) / kPage;
+            int lp = 2 * (g - prefix[rl]) + which;
+            if (lp >= npg) lp = lp - 1;
+            pg = p.page_table[static_cast<long long>(rl) * p.max_pages + lp];
+          } else {
+            pg = page_of(rl, g, which);
+          }
+        }
         if (lane == 0) {
           for (int u = 0; u < kGroup && it0 + u < ntl && ok; ++u) {
             const int g = g0 + it0 + u;
@@ -292,9 +316,6 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        const int it = it0 + (lane >> 1);
-        const int which = lane & 1;
-        const bool act = lane < 2 * kGroup && it < ntl;
         const uint32_t st = static_cast<uint32_t>(it) % C::kStages;
         bool armed = true;
         if (act && which == 0) {
@@ -307,12 +328,12 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         if (act) {
           // An out-of-range page id (-1 here) is reported and read past the
           // cache end (TMA fills zeros); the epilogue masks its tokens.
-          const int g = g0 + it;
-          while (prefix[rl + 1] <= g) ++rl;
           // A request's new tokens (its last n_q <= 4) lie in its last two
-          // tiles, which the kernel before may still be writing.
+          // tiles, which the kernel before may still be writing (their keys,
+          // not the page table).
+          const int g = g0 + it;
           if (p.wait_tail && g >= prefix[rl + 1] - 2) grid_dep_wait();
-          const int pg = it0 == 0 ? tile_page(p, prefix, rl, g, which) : page_of(rl, g, which);
+          if (pg >= p.num_pages) pg = -1;
           if (pg < 0) raise_error(kErrCheck);
           const int y = pg >= 0 ? pg * kPage : p.num_pages * kPage;
           tma_load_2d(sbase + C::kOffStages + st * kStageBytes + which * (kPage * kIndexDim), &tmap_k,
@@ -449,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         seg_tiles = 0;
         named_bar_sync(bar_id, 128);
         cur = r;
-        S = p.seqlens[r];
+        S = seq_s[r];
         for (int e = tid; e < C::kN; e += 128) {
           const int t = r * NQ + e / kIndexHeads;
           gw[e] = p.w[static_cast<long long>(t) * kIndexHeads + (e % kIndexHeads)] * p.q_scale[t];
