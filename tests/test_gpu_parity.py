@@ -485,6 +485,33 @@ def test_device_check_flags_bad_page_id():
     assert np.isfinite(row[:3 * 64]).all()
 
 
+def test_device_check_flags_bad_page_ids_in_both_lookup_paths():
+    """One 131072-token request: every CTA of the indexer's grid streams 6-7
+    tiles of 128 tokens, its first four looked up by the producer itself and
+    the rest from the page ids the other warps stage in shared memory.  An
+    out-of-range page id in CTA 0's fifth tile (the staged path) and a
+    negative one in CTA 1's second tile (the producer's own lookup) must both
+    be reported and mask exactly their 64 tokens."""
+    wl, g = _gpu_wl("long_varlen", batch=1, q_per_req=1, num_heads=16, topk=2048,
+                    seqlens=[131072], heavy="none", seed=74)
+    ctas = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = 131072 // 128
+    assert tiles // ctas >= 5
+    page_a = 2 * 4 + 1                       # CTA 0, tile 4, its second page
+    page_b = 2 * (tiles // ctas + 1)         # CTA 1, its second tile, first page
+    g.page_table[0, page_a] = wl.num_pages + 5
+    g.page_table[0, page_b] = -3
+    assert api.dsa_get_device_error() == 0
+    logits = api.run_indexer(g)
+    assert api.dsa_get_device_error() == 5               # DSA_ERR_DEVICE_CHECK
+    row = logits[0].cpu().numpy()[:131072]
+    bad = np.zeros(131072, dtype=bool)
+    for pg in (page_a, page_b):
+        bad[pg * 64:(pg + 1) * 64] = True
+    assert np.isneginf(row[bad]).all()
+    assert np.isfinite(row[~bad]).all()
+
+
 def test_indexer_wait_timeout_is_reported_and_context_survives():
     """A wait bound of one SM cycle makes the indexer's pipeline waits run out
     (the copies they wait for take microseconds): the call must come back,
