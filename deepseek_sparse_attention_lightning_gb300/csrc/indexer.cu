@@ -29,13 +29,16 @@
 //            token's key scale three of its tiles ahead.  With two groups at
 //            n_q = 1 the epilogue set the pace: the MMA issuers waited for
 //            free accumulators and the producer for free stages a quarter of
-//            the time; a third group takes that wait off.
+//            the time; a third group takes most of that wait off.
 // Accumulators: six TMEM buffers at n_q = 1, four at n_q = 2 (one per
 // epilogue group), else two, so the MMAs of a tile do not wait for the
 // epilogue of the tile a few before it.
-// The page ids of the CTA's tile range are fetched once, by all threads, into
-// shared memory.  Keys are streamed exactly once per request; every query
-// token of the request is served by the same key tile (N = 64 * n_q).
+// The requests' lengths are kept in shared memory from the tile scan; the
+// producer looks up its first four tiles' page ids itself (one global load
+// each, in flight while it issues the query copy) and the other warps fetch
+// the rest of the range's page ids once into shared memory.  Keys are
+// streamed exactly once per request; every query token of the request is
+// served by the same key tile (N = 64 * n_q).
 #include <atomic>
 
 #include "dsa_ptx.cuh"
