@@ -52,24 +52,6 @@ __device__ __forceinline__ int visible(const int32_t* seqlens, int t, int nq) {
   return seqlens[t / nq] - (nq - 1 - t % nq);
 }
 
-// Index of the n-th (0-based) set bit of m (m has more than n set bits).
-__device__ __forceinline__ int nth_set_bit(uint32_t m, int n) {
-  int pos = 0;
-#pragma unroll
-  for (int width = 16; width > 0; width >>= 1) {
-    const uint32_t low = m & ((1u << width) - 1u);
-    const int c = __popc(low);
-    if (n >= c) {
-      n -= c;
-      m >>= width;
-      pos += width;
-    } else {
-      m = low;
-    }
-  }
-  return pos;
-}
-
 // Exclusive scan of one value per thread over a 512-thread block.
 __device__ __forceinline__ uint32_t block_excl_scan_512(uint32_t v, uint32_t* scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
